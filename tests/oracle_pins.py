@@ -1,0 +1,328 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each check takes an ``oracle.OracleLib`` so that the same battery can be run
+against the real oracle (tests/test_oracle_pins.py) and against copies with a
+planted mistake (tests/test_oracle_mutants.py), which must fail at least one.
+
+Independent references used here, none of which is the oracle's own code:
+  * the library float32 -> bf16 cast (torch), which rounds to nearest even;
+  * "round to odd" to binary32 followed by that library cast, which gives the
+    correctly rounded bf16 of any double because binary32 keeps more than two
+    extra bits (Boldo and Melquiond, "Emulation of FMA and correctly rounded
+    sums: proved algorithms using rounding to odd", IEEE TC 2008);
+  * exact rational arithmetic (fractions.Fraction) for dequantisation and sums;
+  * numpy int64 matmul for the integer special case;
+  * values worked by hand (tests/golden/hand_2x8.json).
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+from quantized_swiglu_mlp_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+MATCH, F32, DEBUG_GATE, DEBUG_UP = 0, 1, 2, 3
+
+
+# ----------------------------------------------------------- references ----
+
+def lib_bf16_bits(v32: np.ndarray) -> np.ndarray:
+    """Library cast float32 -> bf16 (round to nearest even), as uint16 bits."""
+    t = torch.from_numpy(np.ascontiguousarray(v32, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def round_to_odd_f32(v: float) -> np.float32:
+    f = np.float32(v)
+    if float(f) == v or not math.isfinite(v):
+        return f
+    bits = f.view(np.uint32)
+    if bits & 1:
+        return f
+    # f was rounded to an even neighbour: step to the odd neighbour on v's side
+    return np.nextafter(f, np.float32(math.copysign(math.inf, v - float(f))), dtype=np.float32)
+
+
+def ref_bf16(v: float) -> int:
+    """Correctly rounded bf16 of a double via round-to-odd + library cast."""
+    return int(lib_bf16_bits(np.array([round_to_odd_f32(float(v))], dtype=np.float32))[0])
+
+
+def bf16_val(h: int) -> float:
+    return float(np.array([h << 16], dtype=np.uint32).view(np.float32)[0])
+
+
+def ref_round(v: float) -> float:
+    return bf16_val(ref_bf16(v))
+
+
+def ref_codes_from_words(words, n, bits):
+    """Unpack by string manipulation of the binary representation (LSB first)."""
+    out = []
+    pf = 32 // bits
+    for w in words:
+        s = format(int(w), "032b")[::-1]          # s[j] = bit j
+        for c in range(pf):
+            out.append(int(s[c * bits:(c + 1) * bits][::-1], 2))
+    return out[:n]
+
+
+def brute_force(case: inputs.Case, variant: int) -> np.ndarray:
+    """Dequantise whole matrices with Fractions, then a triple loop."""
+    x = [[Fraction(bf16_val(int(h))) for h in row] for row in case.x]
+    M, H, I = case.M, case.H, case.I
+
+    def deq(qm: inputs.QuantMatrix):
+        codes = [ref_codes_from_words(r, H, qm.bits) for r in qm.packed]
+        W = []
+        for i in range(I):
+            row = []
+            for k in range(H):
+                s = Fraction(bf16_val(int(qm.scales[i, k // qm.gs])))
+                b = Fraction(bf16_val(int(qm.biases[i, k // qm.gs])))
+                row.append(Fraction(ref_round(float(s * codes[i][k] + b))))
+            W.append(row)
+        return W
+
+    Wg, Wu = deq(case.gate), deq(case.up)
+    out = np.zeros((M, I), dtype=np.uint16)
+    for m in range(M):
+        for i in range(I):
+            g = float(sum(x[m][k] * Wg[i][k] for k in range(H)))
+            u = float(sum(x[m][k] * Wu[i][k] for k in range(H)))
+            if variant == MATCH:
+                gb, ub = ref_round(g), ref_round(u)
+                sig = ref_round(1.0 / (1.0 + math.exp(-gb)))
+                silu = ref_round(gb * sig)
+                out[m, i] = ref_bf16(silu * ub)
+            elif variant == F32:
+                out[m, i] = ref_bf16(g * u / (1.0 + math.exp(-g)))
+            elif variant == DEBUG_GATE:
+                out[m, i] = ref_bf16(g)
+            else:
+                out[m, i] = ref_bf16(u)
+    return out
+
+
+# ------------------------------------------------------------ the pins -----
+
+def pin_bf16_binary32(orc, n=20000, seed=0):
+    rng = np.random.default_rng(seed)
+    bits = rng.integers(0, 1 << 32, size=n, dtype=np.uint64).astype(np.uint32)
+    bits[: n // 4] = (bits[: n // 4] & 0xFFFF0000) | 0x8000        # exact ties
+    bits[n // 4: n // 2] = (bits[n // 4: n // 2] & 0xFFFF0000) | 0x7FFF
+    vals = bits.view(np.float32)
+    vals = vals[np.isfinite(vals) & (np.abs(vals) < np.float32(3.0e38))]
+    got = orc.bf16_round_array(vals.astype(np.float64))
+    want = lib_bf16_bits(vals)
+    assert np.array_equal(got, want), "bf16 rounding disagrees with the library cast"
+
+
+def pin_bf16_double(orc, n=5000, seed=1):
+    rng = np.random.default_rng(seed)
+    vals = []
+    for _ in range(n):
+        # a bf16 midpoint nudged by a few double ulps: binary32 would round it
+        # to the midpoint itself, so a two-step rounding gives the wrong answer
+        h = int(rng.integers(0x0080, 0x7F00))
+        lo, hi = bf16_val(h), bf16_val(h + 1)
+        mid = (lo + hi) / 2
+        for d in (-3, -1, 1, 3):
+            vals.append(math.copysign(1.0, rng.standard_normal()) * (mid + d * math.ulp(mid)))
+    vals += [1e-40, -3e-39, 2.0 ** -133, 2.0 ** -134, 3 * 2.0 ** -135, 3.3895313892515355e38,
+             3.4e38, -1.0, 0.0, 65536.0 + 255.0]
+    got = [orc.f64_to_bf16(v) for v in vals]
+    want = [ref_bf16(v) for v in vals]
+    assert got == want, "bf16 rounding of doubles is not a single correct rounding"
+
+
+def pin_unpack(orc):
+    assert list(orc.unpack(np.array([0x76543210], np.uint32), 8, 4)) == list(range(8))
+    assert list(orc.unpack(np.array([0x89ABCDEF], np.uint32), 8, 4)) == list(range(15, 7, -1))
+    assert list(orc.unpack(np.array([0x04030201], np.uint32), 4, 8)) == [1, 2, 3, 4]
+    assert list(orc.unpack(np.array([0xE4], np.uint32), 4, 2)) == [0, 1, 2, 3]
+    rng = np.random.default_rng(2)
+    for bits in (2, 4, 8):
+        codes = rng.integers(0, 1 << bits, size=(3, 64), dtype=np.uint8)
+        words = inputs.pack_codes(codes, bits)
+        got = orc.unpack(words.ravel(), codes.size, bits)
+        assert np.array_equal(got, codes.ravel())
+        assert ref_codes_from_words(words.ravel(), codes.size, bits) == list(codes.ravel())
+
+
+def _hand_case():
+    with open(os.path.join(GOLDEN, "hand_2x8.json")) as f:
+        gd = json.load(f)
+
+    def b16(vals):
+        return lib_bf16_bits(np.asarray(vals, dtype=np.float32))
+
+    gate = inputs.QuantMatrix(np.array(gd["wg_words"], np.uint32).reshape(2, 1),
+                              b16(gd["sg"]).reshape(2, 1), b16(gd["bg"]).reshape(2, 1), 8, 4)
+    up = inputs.QuantMatrix(np.array(gd["wu_words"], np.uint32).reshape(2, 1),
+                            b16(gd["su"]).reshape(2, 1), b16(gd["bu"]).reshape(2, 1), 8, 4)
+    x = b16(gd["x"]).reshape(2, 8)
+    return gd, inputs.Case(x=x, gate=gate, up=up)
+
+
+def pin_hand_example(orc):
+    gd, case = _hand_case()
+    out, g, u = orc.qswiglu(*case.oracle_args(), variant=MATCH, return_acc=True)
+    assert np.array_equal(g, np.array(gd["g"])) and np.array_equal(u, np.array(gd["u"]))
+    want = lib_bf16_bits(np.asarray(gd["match"], np.float32))
+    assert np.array_equal(out, want), (out, want)
+    out = orc.qswiglu(*case.oracle_args(), variant=F32)
+    assert np.array_equal(out, lib_bf16_bits(np.asarray(gd["f32"], np.float32)))
+    dg = orc.qswiglu(*case.oracle_args(), variant=DEBUG_GATE)
+    du = orc.qswiglu(*case.oracle_args(), variant=DEBUG_UP)
+    assert np.array_equal(dg, lib_bf16_bits(np.asarray(gd["g"], np.float32)))
+    assert np.array_equal(du, lib_bf16_bits(np.asarray(gd["u"], np.float32)))
+    # the unfused elementwise step on the stored bf16 projections, same values
+    sm = orc.silu_mul(dg.ravel(), du.ravel(), MATCH).reshape(2, 2)
+    assert np.array_equal(sm, lib_bf16_bits(np.asarray(gd["match"], np.float32)))
+    # dequantised rows
+    w = orc.dequant(case.gate.packed, case.gate.scales, case.gate.biases, 8, 8, 4)
+    assert list(w[0]) == [-4, -3, -2, -1, 0, 1, 2, 3]
+    assert list(w[1]) == [3.5, 3, 2.5, 2, 1.5, 1, 0.5, 0]
+
+
+def pin_zero_input(orc):
+    case = inputs.make_case(3, 128, 24, seed=3)
+    case.x[:] = 0
+    for v in (MATCH, F32, DEBUG_GATE, DEBUG_UP):
+        out = orc.qswiglu(*case.oracle_args(), variant=v)
+        assert np.all(out == 0), f"x=0 must give +0 (variant {v})"
+
+
+def pin_integer_case(orc, seed=4):
+    rng = np.random.default_rng(seed)
+    M, H, I = 5, 96, 7
+    for bits, gs in ((4, 32), (8, 32), (2, 96)):
+        qg = rng.integers(0, 1 << bits, size=(I, H), dtype=np.uint8)
+        qu = rng.integers(0, 1 << bits, size=(I, H), dtype=np.uint8)
+        xi = rng.integers(-2, 3, size=(M, H))
+        one = lib_bf16_bits(np.ones((I, H // gs), np.float32))
+        zero = np.zeros((I, H // gs), np.uint16)
+        case = inputs.Case(x=lib_bf16_bits(xi.astype(np.float32)),
+                           gate=inputs.QuantMatrix(inputs.pack_codes(qg, bits), one, zero, gs, bits),
+                           up=inputs.QuantMatrix(inputs.pack_codes(qu, bits), one, zero, gs, bits))
+        g_int = xi.astype(np.int64) @ qg.astype(np.int64).T
+        u_int = xi.astype(np.int64) @ qu.astype(np.int64).T
+        dg = orc.qswiglu(*case.oracle_args(), variant=DEBUG_GATE)
+        du = orc.qswiglu(*case.oracle_args(), variant=DEBUG_UP)
+        assert np.array_equal(dg, lib_bf16_bits(g_int.astype(np.float32)))
+        assert np.array_equal(du, lib_bf16_bits(u_int.astype(np.float32)))
+        y = orc.qmm(case.x, case.gate.packed, one, zero, gs, bits)
+        assert np.array_equal(y, lib_bf16_bits(g_int.astype(np.float32)))
+
+
+def pin_brute_force(orc):
+    cases = [
+        inputs.make_case(2, 64, 3, bits_g=4, gs_g=32, seed=5),
+        inputs.make_case(3, 64, 2, bits_g=8, gs_g=64, bits_u=4, gs_u=32, seed=6),
+        inputs.make_case(1, 32, 4, bits_g=2, gs_g=32, bits_u=8, gs_u=32, seed=7,
+                         scale_range=(0.05, 0.3)),
+    ]
+    for case in cases:
+        for v in (MATCH, F32, DEBUG_GATE, DEBUG_UP):
+            got = orc.qswiglu(*case.oracle_args(), variant=v)
+            want = brute_force(case, v)
+            assert np.array_equal(got, want), (case.meta, v, got, want)
+        y = orc.qmm(case.x, case.up.packed, case.up.scales, case.up.biases, case.up.gs, case.up.bits)
+        assert np.array_equal(y, brute_force(case, DEBUG_UP))
+
+
+def pin_k_permutation(orc):
+    """Permuting whole groups of K in x and both weights leaves g and u unchanged."""
+    case = inputs.make_case(4, 256, 16, bits_g=4, gs_g=64, bits_u=8, gs_u=32, seed=8,
+                            keep_codes=True)
+    gs = 64
+    perm_groups = np.random.default_rng(9).permutation(256 // gs)
+    kperm = np.concatenate([np.arange(p * gs, (p + 1) * gs) for p in perm_groups])
+
+    def permute(qm: inputs.QuantMatrix):
+        codes = qm.codes[:, kperm]
+        gperm = np.concatenate([np.arange(p * gs // qm.gs, (p + 1) * gs // qm.gs) for p in perm_groups])
+        return inputs.QuantMatrix(inputs.pack_codes(codes, qm.bits), qm.scales[:, gperm].copy(),
+                                  qm.biases[:, gperm].copy(), qm.gs, qm.bits)
+
+    pc = inputs.Case(x=case.x[:, kperm].copy(), gate=permute(case.gate), up=permute(case.up))
+    _, g0, u0 = orc.qswiglu(*case.oracle_args(), variant=MATCH, return_acc=True)
+    _, g1, u1 = orc.qswiglu(*pc.oracle_args(), variant=MATCH, return_acc=True)
+    assert np.allclose(g0, g1, rtol=1e-12, atol=1e-12) and np.allclose(u0, u1, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(orc.qswiglu(*case.oracle_args(), variant=F32),
+                          orc.qswiglu(*pc.oracle_args(), variant=F32))
+
+
+def pin_silu_values(orc):
+    """Closed forms of the elementwise step: silu(0)=0, silu(g)->g for large g,
+    silu(g) - silu(-g) = g, and sigmoid(0) = 1/2 exactly."""
+    g = lib_bf16_bits(np.array([0.0, 0.0, 20.0, 40.0, -40.0, 2.0], np.float32))
+    u = lib_bf16_bits(np.array([5.0, -3.0, 1.0, 2.0, 1.0, 1.0], np.float32))
+    for v in (MATCH, F32):
+        h = orc.silu_mul(g, u, v)
+        vals = [bf16_val(int(t)) for t in h]
+        assert vals[0] == 0.0 and vals[1] == 0.0
+        assert vals[2] == 20.0 and vals[3] == 80.0
+        assert abs(vals[4]) < 1e-15
+        # silu(2) = 2 / (1 + e^-2) = 1.76159..
+        assert abs(vals[5] - 2.0 / (1.0 + math.exp(-2.0))) <= 2 ** -7 * 2
+    rng = np.random.default_rng(10)
+    gv = rng.uniform(-6, 6, size=200).astype(np.float32)
+    gp, gn = lib_bf16_bits(gv), lib_bf16_bits(-gv)
+    one = lib_bf16_bits(np.ones(200, np.float32))
+    hp = np.array([bf16_val(int(t)) for t in orc.silu_mul(gp, one, F32)])
+    hn = np.array([bf16_val(int(t)) for t in orc.silu_mul(gn, one, F32)])
+    gb = np.array([bf16_val(int(t)) for t in gp])
+    assert np.allclose(hp - hn, gb, atol=2 ** -6 * (np.abs(gb) + 1))
+
+
+def pin_silu_exhaustive(orc):
+    """Every bf16 gate value in [-16, 16] (and a few u), against the step-by-step
+    definition built from the reference rounding and the C library exp."""
+    hs = np.arange(0, 0x10000, dtype=np.uint32)
+    vals = (hs << 16).view(np.float32)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 16.0)
+    g = hs[keep].astype(np.uint16)
+    for uval in (1.0, -3.0, 0.3):
+        u = lib_bf16_bits(np.full(g.shape, uval, np.float32))
+        ub = bf16_val(int(u[0]))
+        got_m = orc.silu_mul(g, u, MATCH)
+        got_f = orc.silu_mul(g, u, F32)
+        for j, h in enumerate(g[::3]):
+            gv = bf16_val(int(h))
+            sig = ref_round(1.0 / (1.0 + math.exp(-gv)))
+            want_m = ref_bf16(ref_round(gv * sig) * ub)
+            want_f = ref_bf16(gv * ub / (1.0 + math.exp(-gv)))
+            assert got_m[3 * j] == want_m, (gv, uval)
+            assert got_f[3 * j] == want_f, (gv, uval)
+
+
+def pin_match_is_unfused(orc):
+    """MATCH is defined as the unfused composition qmm, qmm, sigmoid, mul, mul."""
+    case = inputs.make_case(5, 192, 40, bits_g=4, gs_g=64, bits_u=8, gs_u=32, seed=11)
+    fused = orc.qswiglu(*case.oracle_args(), variant=MATCH)
+    g = orc.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, 64, 4)
+    u = orc.qmm(case.x, case.up.packed, case.up.scales, case.up.biases, 32, 8)
+    assert np.array_equal(fused, orc.silu_mul(g, u, MATCH))
+
+
+def pin_sampled_pairs(orc):
+    case = inputs.make_case(6, 128, 30, seed=12)
+    full = orc.qswiglu(*case.oracle_args(), variant=MATCH)
+    pairs = np.array([[0, 0], [5, 29], [3, 17], [2, 2]])
+    got = orc.qswiglu_pairs(*case.oracle_args(), MATCH, pairs)
+    assert np.array_equal(got, full[pairs[:, 0], pairs[:, 1]])
+    rows = orc.qswiglu(*case.oracle_args(), variant=MATCH, rows=[4, 1])
+    assert np.array_equal(rows, full[[4, 1]])
+
+
+ALL_PINS = [pin_bf16_binary32, pin_bf16_double, pin_unpack, pin_hand_example,
+            pin_zero_input, pin_integer_case, pin_brute_force, pin_k_permutation,
+            pin_silu_values, pin_silu_exhaustive, pin_match_is_unfused, pin_sampled_pairs]

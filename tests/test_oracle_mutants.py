@@ -1,0 +1,44 @@
+"""Plant plausible mistakes in copies of the oracle and check that the pins
+catch every one (CPU only).  Each mutation is an exact text edit of
+oracle/qsw_oracle.c; the edited copy is compiled into a temporary directory and
+the whole pin battery is run against it."""
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+MUTANTS = {
+    "codes_msb_first": ("unsigned shift = (unsigned)((k % pf) * bits);",
+                        "unsigned shift = (unsigned)((pf - 1 - k % pf) * bits);"),
+    "bias_sign": ("sc * q + bi", "sc * q - bi"),
+    "group_index": ("s[r * groups_per_row + k / gs]", "s[r * groups_per_row + (k / gs + 1) % groups_per_row]"),
+    "sigmoid_sign": ("double sig = rb(1.0 / (1.0 + exp(-gb)));", "double sig = rb(1.0 / (1.0 + exp(gb)));"),
+    "match_drops_silu_rounding": ("double silu = rb(gb * sig);", "double silu = gb * sig;"),
+    "match_drops_sigma_rounding": ("double sig = rb(1.0 / (1.0 + exp(-gb)));", "double sig = 1.0 / (1.0 + exp(-gb));"),
+    "f32_rounds_gate": ("case ORC_F32:        return orc_f64_to_bf16(f32_epilogue(g, u));",
+                        "case ORC_F32:        return orc_f64_to_bf16(f32_epilogue(rb(g), u));"),
+    "ties_away": ("return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;", "return fl + 1.0;"),
+    "bf16_one_bit_short": ("int ulp_exp = e - 7;", "int ulp_exp = e - 6;"),
+    "up_uses_gate": ("double u = dot_f64(xd + j * H, wur, H);", "double u = dot_f64(xd + j * H, wgr, H);"),
+    "dropped_term": ("for (int64_t k = 0; k < K; ++k) acc += xr[k] * wr[k];",
+                     "for (int64_t k = 1; k < K; ++k) acc += xr[k] * wr[k];"),
+    "silu_uses_up": ("return rb(silu * ub);", "return rb(silu * gb);"),
+    "qmm_transposed": ("y[m * N + n] = orc_f64_to_bf16(dot_f64(xd + m * K, wr, K));",
+                       "y[(n % M) * N + (m + n / M) % N] = orc_f64_to_bf16(dot_f64(xd + m * K, wr, K));"),
+    "subnormal_spacing": ("if (ulp_exp < -133) ulp_exp = -133;", "if (ulp_exp < -126) ulp_exp = -126;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = oracle.source_text()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    lib = oracle.OracleLib(oracle.build_variant(src.replace(old, new), str(tmp_path / f"{name}.so")))
+    failures = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError, IndexError):
+            failures.append(pin.__name__)
+    assert failures, f"no pin caught the planted mistake {name}"
