@@ -1,0 +1,476 @@
+"""Benchmark of the fused weight-quantized SwiGLU expansion on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload (one step = one fused call over one token):
+  decode   x bf16 [1, 2048]; Wg, Wu [8192, 2048] 4-bit affine, gs=64; MATCH.
+  metric   weight GB/s = (packed codes + scales + biases of Wg and Wu) / step time.
+           The weights rotate through enough replicas (> 3x the L2 size) that
+           every step streams them from HBM.
+Also reported on the same line (key "prefill"):
+  large prefill  M=4096 H=4096 I=14336, MATCH and F32: TFLOP/s (4*M*H*I / time)
+  mid prefill    M=512 H=2048 I=8192: fused vs the unfused GPU path
+                 (2x affine_qmm + silu*mul) in the same run.
+
+--impl reference times the CPU oracle (the plain C definition, OpenMP over
+rows) on a bounded sample of the same workload and prints the same JSON line.
+
+With torchrun (--gpus N > 1) every rank runs its own replica of the workload
+on its own GPU (weak scaling, no collective on the data path); the step time is
+the maximum over ranks and `value` counts the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------ helpers -------
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        out = {}
+        for k in FALLBACK_PEAKS:
+            v = d.get(k)
+            if isinstance(v, dict):
+                v = v.get("value")
+            if v is None:
+                raise KeyError(k)
+            out[k] = float(v)
+        return out, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def weight_bytes(case) -> int:
+    g, u = case.gate, case.up
+    return int(g.packed.nbytes + g.scales.nbytes + g.biases.nbytes
+               + u.packed.nbytes + u.scales.nbytes + u.biases.nbytes)
+
+
+def read_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel's
+    source has not changed since (matching source hash)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    try:
+        from quantized_swiglu_mlp_gb300 import build as qbuild
+        cur = qbuild.source_hash()
+        with open(path) as f:
+            for line in f:
+                kv = dict(t.split("=", 1) for t in line.split() if "=" in t)
+                if kv.get("kernel") == kernel and kv.get("workload") == workload:
+                    if kv.get("source_sha") != cur:
+                        return None
+                    return float(kv["bytes_per_launch"])
+    except Exception:
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU is under load."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return self
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self._t is not None:
+            self._t.join(timeout=5)
+        return self.summary()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_timing(elapsed_ms: float, units: float, group=None):
+    """Max elapsed time and summed work over the ranks of `group` (or this
+    process alone when torch.distributed is not initialised)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return elapsed_ms, units
+    backend = dist.get_backend(group)
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM, group=group)
+    return float(t.item()), float(u.item())
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------ our arm -------
+
+def to_device(case, dev):
+    from quantized_swiglu_mlp_gb300.inputs import device_args
+    return device_args(case, dev)
+
+
+def time_calls(fn, steps: int, warmup: int, stream):
+    """Warm up, then time `steps` calls with CUDA events on `stream`
+    (synchronised, with a barrier across ranks, on both sides)."""
+    import torch
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        fn(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end)
+
+
+def bench_decode(args, dev, stream, peaks, peak_src):
+    import torch
+    from quantized_swiglu_mlp_gb300 import inputs, ops
+
+    case = inputs.workload_case("decode")
+    wbytes = weight_bytes(case)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    replicas = max(4, int(np.ceil(3.2 * l2 / wbytes)))
+    base = to_device(case, dev)
+    x = base[0]
+    reps = [tuple(t.clone() if isinstance(t, torch.Tensor) else t for t in base[1:])
+            for _ in range(replicas)]
+    out = torch.empty((1, case.I), dtype=torch.bfloat16, device=dev)
+    algo_bytes = wbytes + case.x.nbytes + 2 * case.I
+    variant = ops.VARIANTS[args.variant]
+
+    def step(i):
+        ops.qswiglu_forward(x, *reps[i % replicas], variant=variant, out=out, stream=stream)
+
+    # soak so that the clock sampler sees the GPU under this load
+    sampler = ClockSampler(dev.index).start()
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        for i in range(200):
+            step(i)
+        torch.cuda.synchronize()
+    ops.qsw_reset_counters()
+    ms = time_calls(step, args.steps, args.warmup, stream)
+    counters = ops.qsw_get_counters()
+    clocks = sampler.stop()
+    ops.qsw_check_device_errors(stream)
+    launches = counters[ops.CNT_FUSED_GEMV] + counters[ops.CNT_FUSED_TC]
+    timed_launches = launches - args.warmup
+
+    # end to end through the public API with pinned host buffers
+    x_host = torch.empty((1, case.H), dtype=torch.bfloat16, pin_memory=True)
+    x_host.copy_(x.cpu())
+    out_host = torch.empty((1, case.I), dtype=torch.bfloat16, pin_memory=True)
+    x_dev = torch.empty_like(x)
+
+    def e2e_step(i):
+        with torch.cuda.stream(stream):
+            x_dev.copy_(x_host, non_blocking=True)
+            ops.qswiglu_forward(x_dev, *reps[i % replicas], variant=variant, out=out, stream=stream)
+            out_host.copy_(out, non_blocking=True)
+
+    e2e_ms = time_calls(e2e_step, args.steps, args.warmup, stream)
+    world, rank, _ = dist_info()
+    max_ms, total_bytes = reduce_timing(ms, wbytes * args.steps)
+    e2e_max_ms, e2e_bytes = reduce_timing(e2e_ms, wbytes * args.steps)
+    per_launch_s = ms / 1e3 / args.steps
+    achieved = algo_bytes / per_launch_s / 1e9
+    return dict(
+        case=case, wbytes=wbytes, replicas=replicas, ms=max_ms, total_bytes=total_bytes,
+        e2e_ms=e2e_max_ms, e2e_bytes=e2e_bytes, clocks=clocks, launches=timed_launches,
+        roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                  "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                  "traffic": read_traffic("gemv", "decode"), "peak_source": peak_src,
+                  "kernel": "gemv_kernel (small-M, mma.sync reduction)",
+                  "algorithmic_bytes_per_launch": algo_bytes},
+        l2_bytes=l2)
+
+
+def bench_prefill(args, dev, stream, peaks, peak_src):
+    import torch
+    from quantized_swiglu_mlp_gb300 import inputs, ops
+
+    res = {}
+    case = inputs.workload_case("large_prefill")
+    a = to_device(case, dev)
+    out = torch.empty((case.M, case.I), dtype=torch.bfloat16, device=dev)
+    flops = 4.0 * case.M * case.H * case.I
+    for vname in ("match", "f32"):
+        v = ops.VARIANTS[vname]
+        ms = time_calls(lambda i: ops.qswiglu_forward(*a, variant=v, out=out, stream=stream),
+                        args.prefill_steps, 3, stream)
+        per = ms / 1e3 / args.prefill_steps
+        tf = flops / per / 1e12
+        res[f"large_{vname}"] = {"tflops": round(tf, 1), "us_per_call": round(per * 1e6, 1)}
+    tf = res["large_match"]["tflops"]
+    res["large_roofline"] = {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": round(tf / peaks["bf16_tflops"], 4),
+                             "traffic": read_traffic("prefill", "large_prefill"), "peak_source": peak_src,
+                             "kernel": "prefill_kernel (tcgen05 + TMA)",
+                             "algorithmic_flops_per_launch": flops}
+    del a, out
+    torch.cuda.empty_cache()
+
+    case = inputs.workload_case("mid_prefill")
+    a = to_device(case, dev)
+    out = torch.empty((case.M, case.I), dtype=torch.bfloat16, device=dev)
+    g = torch.empty_like(out)
+    u = torch.empty_like(out)
+    flops = 4.0 * case.M * case.H * case.I
+    ms_f = time_calls(lambda i: ops.qswiglu_forward(*a, variant=ops.MATCH, out=out, stream=stream),
+                      args.prefill_steps, 3, stream)
+    x, wg, sg, bg, gsg, btg, wu, su, bu, gsu, btu = a
+
+    def unfused(i):
+        ops.affine_qmm(x, wg, sg, bg, gsg, btg, y=g, stream=stream)
+        ops.affine_qmm(x, wu, su, bu, gsu, btu, y=u, stream=stream)
+        ops.qsw_silu_mul(g, u, ops.MATCH, out=out, stream=stream)
+
+    ms_u = time_calls(unfused, args.prefill_steps, 3, stream)
+    ops.qsw_check_device_errors(stream)
+    pf, pu = ms_f / 1e3 / args.prefill_steps, ms_u / 1e3 / args.prefill_steps
+    res["mid_fused"] = {"tflops": round(flops / pf / 1e12, 1), "us_per_call": round(pf * 1e6, 1)}
+    res["mid_unfused"] = {"tflops": round(flops / pu / 1e12, 1), "us_per_call": round(pu * 1e6, 1)}
+    res["mid_speedup_vs_unfused"] = round(pu / pf, 3)
+    return res
+
+
+def cpu_baseline_decode(budget_s: float):
+    """The oracle, as it stands, on the host cores: whole decode calls until
+    the time budget is spent.  Returns (GB/s of weights, threads, sample)."""
+    import oracle
+    from quantized_swiglu_mlp_gb300 import inputs
+    case = inputs.workload_case("decode")
+    wbytes = weight_bytes(case)
+    calls, t0 = 0, time.perf_counter()
+    while True:
+        oracle.qswiglu(*case.oracle_args(), variant=oracle.MATCH)
+        calls += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return wbytes * calls / dt / 1e9, oracle.num_threads(), f"{calls} full decode calls (M=1, all 8192 rows)"
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from quantized_swiglu_mlp_gb300 import ops
+    ops.load_library()
+    stream = torch.cuda.Stream(device=dev)
+    peaks, peak_src = load_peaks()
+
+    with torch.cuda.stream(stream):
+        d = bench_decode(args, dev, stream, peaks, peak_src)
+        prefill = bench_prefill(args, dev, stream, peaks, peak_src) if not args.no_prefill else None
+
+    value = d["total_bytes"] / (d["ms"] / 1e3) / 1e9
+    e2e = d["e2e_bytes"] / (d["e2e_ms"] / 1e3) / 1e9
+    line = {
+        "metric": "fused qSwiGLU decode weight GB/s",
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(d["ms"] / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "decode GEMV: x bf16 [1,2048], Wg/Wu [8192,2048] 4-bit affine gs=64, "
+                               f"{args.variant.upper()}",
+                   "M": 1, "H": 2048, "I": 8192, "bits": 4, "gs": 64, "variant": args.variant,
+                   "weight_bytes_per_step": d["wbytes"],
+                   "l2": f"weights rotated over {d['replicas']} replicas "
+                         f"({d['replicas'] * d['wbytes'] / 1e6:.0f} MB > 3x L2 {d['l2_bytes'] / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": d["roofline"],
+        "e2e": {"value": round(e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": 2 * 2048,
+                "d2h_bytes_per_step": 2 * 8192},
+        "gpu_launches": d["launches"] * world,
+        "clocks": d["clocks"],
+    }
+    if prefill is not None:
+        line["prefill"] = prefill
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, cores, sample = cpu_baseline_decode(args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------ reference arm -------
+
+def run_reference(args):
+    """The oracle on the host cores, timed on bounded samples of the decode
+    workload: each step computes a slice of the output rows."""
+    world, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    from quantized_swiglu_mlp_gb300 import inputs
+    case = inputs.workload_case("decode")
+    wbytes_full = weight_bytes(case)
+    # size the per-step row slice so that warmup + steps fit in ~2 minutes
+    t0 = time.perf_counter()
+    probe_rows = 512
+    sub = _row_slice(case, probe_rows)
+    oracle.qswiglu(*sub.oracle_args(), variant=oracle.MATCH)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(min(case.I, max(16, budget / max(per_row, 1e-9))))
+    sub = _row_slice(case, rows)
+    step_bytes = wbytes_full * rows / case.I
+    for _ in range(args.warmup):
+        oracle.qswiglu(*sub.oracle_args(), variant=oracle.MATCH)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.qswiglu(*sub.oracle_args(), variant=oracle.MATCH)
+    dt = time.perf_counter() - t0
+    value = step_bytes * args.steps / dt / 1e9
+    sample = f"{rows} of 8192 output rows per step (M=1, H=2048, 4-bit gs=64, MATCH)"
+    line = {
+        "impl": "reference",
+        "metric": "fused qSwiGLU decode weight GB/s",
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": "decode GEMV: x bf16 [1,2048], Wg/Wu [8192,2048] 4-bit affine gs=64, MATCH",
+                   "M": 1, "H": 2048, "I": 8192, "bits": 4, "gs": 64, "variant": "match"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _row_slice(case, rows):
+    from quantized_swiglu_mlp_gb300 import inputs
+    g, u = case.gate, case.up
+
+    def cut(q):
+        return inputs.QuantMatrix(q.packed[:rows], q.scales[:rows], q.biases[:rows], q.gs, q.bits)
+    return inputs.Case(x=case.x, gate=cut(g), up=cut(u))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--variant", choices=["match", "f32"], default="match")
+    ap.add_argument("--prefill-steps", type=int, default=10)
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

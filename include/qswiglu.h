@@ -1,0 +1,150 @@
+/*
+ * qswiglu.h -- C ABI of libqswiglu.so, the GB300 (sm_103a) fused
+ * weight-quantised SwiGLU expansion
+ *
+ *     hidden = silu(x . Wg^T) * (x . Wu^T)
+ *
+ * Source of the operation: mlx-bun source-diff pages ("mlx-bun 0.0.7 -> 0.0.9,
+ * page 42" and "mlx-bun 0.0.8 -> 0.0.10, page 41"), file
+ * src/model/fused-swiglu-kernel.ts: the header comment (what is fused, the MATCH
+ * and F32 precision variants, down_proj left as a separate quantised matmul),
+ * fusedSwigluSupported() (accepted quantisation specs) and fusedSwiglu()
+ * (shapes, "caller owns" the result).  The standalone quantised linear follows
+ * src/model/steel-linear-kernel.ts, steelLinear(), on page 43 ("mlx-bun 0.0.7 ->
+ * 0.0.9, page 43").
+ *
+ * Data layout (all row-major, contiguous, device memory unless stated):
+ *   x        bf16  [M, H]                 activation
+ *   w        uint32 [rows, H*bits/32]     packed codes; code k of a row sits at
+ *                                         bits (k mod pf)*bits of word k/pf,
+ *                                         pf = 32/bits (little-endian, LSB first)
+ *   scales   bf16  [rows, H/gs]           one scale per group of gs consecutive k
+ *   biases   bf16  [rows, H/gs]           affine offsets ("zero points")
+ *   dequantised weight  w[r,k] = bf16_rne(scale[r,k/gs] * q[r,k] + bias[r,k/gs])
+ *   hidden   bf16  [M, I]
+ *
+ * Ownership: the caller allocates and owns every buffer; the library keeps no
+ * pointer after a call returns and allocates no device memory.
+ *
+ * Execution: every entry point that takes `stream` (a cudaStream_t passed as
+ * void*, NULL = the legacy default stream) only enqueues work on that stream
+ * and returns; results are ready when the stream is synchronised.  The calling
+ * thread's current CUDA device must be the one that owns the buffers.
+ *
+ * Errors: argument errors are detected on the host before anything is launched
+ * (QSW_ERR_INVALID_ARG / QSW_ERR_UNSUPPORTED, nothing enqueued).  A failed
+ * launch returns QSW_ERR_CUDA.  Kernels never trap: a device-side wait that
+ * runs past its limit sets a device error word and the kernel exits; the word
+ * is read (and cleared) by qsw_check_device_errors().  Nothing is thrown across
+ * the ABI.
+ */
+#ifndef QSWIGLU_H_
+#define QSWIGLU_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QSW_API __attribute__((visibility("default")))
+#else
+#define QSW_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QSW_OK = 0,
+    QSW_ERR_INVALID_ARG = 1,   /* null pointer, negative size, shape inconsistency */
+    QSW_ERR_UNSUPPORTED = 2,   /* valid but not handled: bits, gs, H, alignment, size */
+    QSW_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
+    QSW_ERR_TIMEOUT = 4        /* a kernel gave up on a device-side wait */
+} qsw_status;
+
+/* Rounding variants of the fused expansion (fused-swiglu-kernel.ts, header
+ * comment "PRECISION"; debug variants mirror its SWIGLU_DEBUG_GATE switch). */
+typedef enum {
+    QSW_MATCH = 0,       /* gate,up -> bf16; sigma, silu, product each rounded to bf16 */
+    QSW_F32 = 1,         /* gate, up, sigma, silu kept f32; one rounding at the store */
+    QSW_DEBUG_GATE = 2,  /* hidden := bf16(x . Wg^T), the stored gate projection */
+    QSW_DEBUG_UP = 3     /* hidden := bf16(x . Wu^T), the stored up projection */
+} qsw_variant;
+
+/* Indices into the dispatch counters (fused-swiglu-kernel.ts keeps a call
+ * counter so a test can prove the kernel ran). */
+enum {
+    QSW_CNT_FUSED_TC = 0,     /* fused expansion, tensor-core (tcgen05) kernel */
+    QSW_CNT_FUSED_GEMV = 1,   /* fused expansion, small-M kernel */
+    QSW_CNT_QMM_TC = 2,       /* affine_qmm, tensor-core kernel */
+    QSW_CNT_QMM_GEMV = 3,     /* affine_qmm, small-M kernel */
+    QSW_CNT_SILU_MUL = 4,     /* elementwise silu*mul */
+    QSW_NUM_COUNTERS = 5
+};
+
+/*
+ * Fused expansion hidden[M,I] = epilogue(x . Wg^T, x . Wu^T).
+ * Gate and up carry their own (gs, bits): fusedSwigluSupported() allows mixed
+ * specs.  Accepted: M >= 0 (M = 0 enqueues nothing), H >= 32, I >= 1,
+ * bits in {2,4,8}, gs a multiple of 32 dividing H, H a multiple of 32 (of 64
+ * for 2-bit codes), variant in qsw_variant.  Pointers x, wg, wu, out must be
+ * 16-byte aligned; scales/biases 2-byte aligned.  x and out must not overlap.
+ * Rows M <= the small-M limit (qsw_set_gemv_max_m) run the memory-bound
+ * kernel, the rest the tcgen05 tensor-core kernel; both compute the same
+ * function.
+ */
+QSW_API qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I,
+                           const uint32_t *wg, const void *sg, const void *bg,
+                           int gs_g, int bits_g,
+                           const uint32_t *wu, const void *su, const void *bu,
+                           int gs_u, int bits_u,
+                           int variant, void *out, void *stream);
+
+/*
+ * Quantised linear y[M,N] = bf16(x[M,K] . W^T), W packed [N, K*bits/32]
+ * with scales/biases [N, K/gs] (steel-linear-kernel.ts, steelLinear(): float
+ * accumulator cast to bf16 at the store).  Used for the unfused comparison
+ * path and for down_proj.  Same accepted shapes and alignment as above with
+ * (H, I) -> (K, N).
+ */
+QSW_API qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N,
+                      const uint32_t *w, const void *s, const void *b,
+                      int gs, int bits, void *y, void *stream);
+
+/*
+ * Elementwise out[i] = silu(g[i]) * u[i] over n bf16 values, the last step of
+ * the unfused path (qwen3.ts, Qwen3MLP.forward: sigmoid, mul, mul).
+ * variant QSW_MATCH rounds sigma, silu and the product to bf16; QSW_F32 rounds
+ * once.  n >= 0; g, u, out 16-byte aligned; out may alias g or u.
+ */
+QSW_API qsw_status qsw_silu_mul(const void *g, const void *u, int64_t n, int variant,
+                        void *out, void *stream);
+
+/* Synchronise `stream`, then read and clear the device error word.
+ * Returns QSW_ERR_TIMEOUT if any kernel gave up on a wait since the last call,
+ * QSW_ERR_CUDA if synchronisation failed, else QSW_OK. */
+QSW_API qsw_status qsw_check_device_errors(void *stream);
+
+/* Largest M routed to the small-M kernel (default 16; 0 sends every M to the
+ * tensor-core kernel).  Values above 32 are clamped to 32.  Process-wide. */
+QSW_API void qsw_set_gemv_max_m(int m);
+QSW_API int qsw_get_gemv_max_m(void);
+
+/* Per-wait limit for device-side waits, in nanoseconds (default 4e9). */
+QSW_API void qsw_set_wait_timeout_ns(uint64_t ns);
+
+/* Dispatch counters (process-wide, monotonically increasing). `out` receives
+ * min(n, QSW_NUM_COUNTERS) values. */
+QSW_API void qsw_get_counters(uint64_t *out, int n);
+QSW_API void qsw_reset_counters(void);
+
+/* Static string for a status code. */
+QSW_API const char *qsw_status_string(qsw_status s);
+
+/* Library ABI version (major*100 + minor). */
+QSW_API int qsw_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSWIGLU_H_ */

@@ -1,0 +1,181 @@
+// C ABI of libqswiglu.so (declared in include/qswiglu.h): argument checks,
+// routing between the small-M and tensor-core kernels, dispatch counters and
+// the device error word.
+//
+// Accepted specs follow fusedSwigluSupported() in the mlx-bun pages
+// (src/model/fused-swiglu-kernel.ts): bits in {2,4,8}, group size a multiple of
+// 32, H a multiple of 32, gate and up specs independent.
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/qswiglu.h"
+#include "qsw_internal.h"
+
+namespace qsw {
+cudaError_t prefill_take_errors(unsigned int *out);
+}
+
+namespace {
+
+std::atomic<uint64_t> g_counters[QSW_NUM_COUNTERS];
+std::atomic<int> g_gemv_max_m{-1};   // -1: not yet initialised
+std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+
+int gemv_max_m() {
+  int v = g_gemv_max_m.load(std::memory_order_relaxed);
+  if (v < 0) {
+    int init = 16;
+    if (const char *env = std::getenv("QSW_GEMV_MAX_M")) init = std::atoi(env);
+    if (init < 0) init = 0;
+    if (init > qsw::kGemvMaxM) init = static_cast<int>(qsw::kGemvMaxM);
+    int expected = -1;
+    g_gemv_max_m.compare_exchange_strong(expected, init);
+    v = g_gemv_max_m.load();
+  }
+  return v;
+}
+
+int sm_count() {
+  static int counts[64];
+  static std::once_flag flags[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::call_once(flags[dev], [dev] {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    counts[dev] = n;
+  });
+  return counts[dev];
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qsw_status check_spec(int64_t K, int gs, int bits) {
+  if (gs <= 0 || K <= 0) return QSW_ERR_INVALID_ARG;
+  if (bits != 2 && bits != 4 && bits != 8) return QSW_ERR_UNSUPPORTED;
+  if (gs % 32 != 0 || K % gs != 0) return QSW_ERR_UNSUPPORTED;
+  if (bits == 2 && K % 64 != 0) return QSW_ERR_UNSUPPORTED;
+  return QSW_OK;
+}
+
+qsw_status check_operand(const uint32_t *w, const void *s, const void *b, int64_t K, int gs, int bits) {
+  if (!w || !s || !b) return QSW_ERR_INVALID_ARG;
+  const qsw_status st = check_spec(K, gs, bits);
+  if (st != QSW_OK) return st;
+  if (!aligned(w, 16) || !aligned(s, 2) || !aligned(b, 2)) return QSW_ERR_UNSUPPORTED;
+  return QSW_OK;
+}
+
+qsw_status check_shape(int64_t M, int64_t K, int64_t N) {
+  if (M < 0 || K <= 0 || N <= 0) return QSW_ERR_INVALID_ARG;
+  if (K % 32 != 0) return QSW_ERR_UNSUPPORTED;
+  // TMA coordinates and tile counts are 32-bit
+  if (K > (int64_t(1) << 30) || N > (int64_t(1) << 30) || M > (int64_t(1) << 30)) return QSW_ERR_UNSUPPORTED;
+  return QSW_OK;
+}
+
+qsw_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSW_OK : QSW_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
+                           const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su, const void *bu,
+                           int gs_u, int bits_u, int variant, void *out, void *stream) {
+  qsw_status st = check_shape(M, H, I);
+  if (st != QSW_OK) return st;
+  if (variant < QSW_MATCH || variant > QSW_DEBUG_UP) return QSW_ERR_INVALID_ARG;
+  if ((st = check_operand(wg, sg, bg, H, gs_g, bits_g)) != QSW_OK) return st;
+  if ((st = check_operand(wu, su, bu, H, gs_u, bits_u)) != QSW_OK) return st;
+  if (!x || !out) return QSW_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16)) return QSW_ERR_UNSUPPORTED;
+  if (M == 0) return QSW_OK;
+
+  const qsw::QuantOperand g{wg, static_cast<const uint16_t *>(sg), static_cast<const uint16_t *>(bg), gs_g, bits_g};
+  const qsw::QuantOperand u{wu, static_cast<const uint16_t *>(su), static_cast<const uint16_t *>(bu), gs_u, bits_u};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M <= gemv_max_m()) {
+    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, out, s));
+    if (st == QSW_OK) g_counters[QSW_CNT_FUSED_GEMV].fetch_add(1, std::memory_order_relaxed);
+  } else {
+    st = from_cuda(qsw::launch_prefill(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count()));
+    if (st == QSW_OK) g_counters[QSW_CNT_FUSED_TC].fetch_add(1, std::memory_order_relaxed);
+  }
+  return st;
+}
+
+qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
+                      const void *b, int gs, int bits, void *y, void *stream) {
+  qsw_status st = check_shape(M, K, N);
+  if (st != QSW_OK) return st;
+  if ((st = check_operand(w, s, b, K, gs, bits)) != QSW_OK) return st;
+  if (!x || !y) return QSW_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16)) return QSW_ERR_UNSUPPORTED;
+  if (M == 0) return QSW_OK;
+
+  const qsw::QuantOperand op{w, static_cast<const uint16_t *>(s), static_cast<const uint16_t *>(b), gs, bits};
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (M <= gemv_max_m()) {
+    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs));
+    if (st == QSW_OK) g_counters[QSW_CNT_QMM_GEMV].fetch_add(1, std::memory_order_relaxed);
+  } else {
+    st = from_cuda(qsw::launch_prefill(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs, g_timeout_ns.load(),
+                                       sm_count()));
+    if (st == QSW_OK) g_counters[QSW_CNT_QMM_TC].fetch_add(1, std::memory_order_relaxed);
+  }
+  return st;
+}
+
+qsw_status qsw_silu_mul(const void *g, const void *u, int64_t n, int variant, void *out, void *stream) {
+  if (n < 0) return QSW_ERR_INVALID_ARG;
+  if (variant != QSW_MATCH && variant != QSW_F32) return QSW_ERR_INVALID_ARG;
+  if (n == 0) return QSW_OK;
+  if (!g || !u || !out) return QSW_ERR_INVALID_ARG;
+  if (!aligned(g, 16) || !aligned(u, 16) || !aligned(out, 16)) return QSW_ERR_UNSUPPORTED;
+  const qsw_status st = from_cuda(qsw::launch_silu_mul(g, u, n, variant, out, static_cast<cudaStream_t>(stream)));
+  if (st == QSW_OK) g_counters[QSW_CNT_SILU_MUL].fetch_add(1, std::memory_order_relaxed);
+  return st;
+}
+
+qsw_status qsw_check_device_errors(void *stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QSW_ERR_CUDA;
+  unsigned int bits = 0;
+  if (qsw::prefill_take_errors(&bits) != cudaSuccess) return QSW_ERR_CUDA;
+  return bits ? QSW_ERR_TIMEOUT : QSW_OK;
+}
+
+void qsw_set_gemv_max_m(int m) {
+  if (m < 0) m = 0;
+  if (m > qsw::kGemvMaxM) m = static_cast<int>(qsw::kGemvMaxM);
+  g_gemv_max_m.store(m);
+}
+
+int qsw_get_gemv_max_m(void) { return gemv_max_m(); }
+
+void qsw_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+void qsw_get_counters(uint64_t *out, int n) {
+  if (!out) return;
+  for (int i = 0; i < n && i < QSW_NUM_COUNTERS; ++i) out[i] = g_counters[i].load();
+}
+
+void qsw_reset_counters(void) {
+  for (auto &c : g_counters) c.store(0);
+}
+
+const char *qsw_status_string(qsw_status s) {
+  switch (s) {
+    case QSW_OK: return "ok";
+    case QSW_ERR_INVALID_ARG: return "invalid argument";
+    case QSW_ERR_UNSUPPORTED: return "unsupported shape, spec or alignment";
+    case QSW_ERR_CUDA: return "CUDA error";
+    case QSW_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int qsw_version(void) { return 100; }
+
+}  // extern "C"

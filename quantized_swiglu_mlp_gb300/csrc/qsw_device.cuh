@@ -1,0 +1,338 @@
+// Device-side building blocks shared by the qswiglu kernels (sm_103a):
+// inline-PTX wrappers for mbarrier / TMA / tcgen05, bounded waits, the
+// packed-code -> bf16 dequantisation and the SwiGLU epilogues.
+//
+// Method source: mlx-bun pages, src/model/fused-swiglu-kernel.ts
+//   - dequantised weights are staged as the activation dtype (bf16) before the
+//     block MMA (the Wgs/Wus threadgroup tiles), i.e. w = bf16(scale*q + bias);
+//   - MATCH epilogue: gate and up rounded to bf16 out of the float accumulator,
+//     then sigma = bf16(1/(1+exp(-g))), silu = bf16(g*sigma), h = bf16(silu*u);
+//   - F32 epilogue: no rounding before the final store.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qsw {
+
+// ------------------------------------------------------------------ errors --
+
+// Device error word bits, set by kernels that gave up on a wait.
+enum : unsigned { DEVERR_TIMEOUT = 1u };
+
+// ----------------------------------------------------------------- helpers --
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// ---------------------------------------------------------------- mbarrier --
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the barrier's phase with the given parity has completed.  Never
+// spins forever: gives up after `timeout_ns`, or as soon as another role of the
+// CTA has raised `abort`.  Returns false when it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint64_t timeout_ns, unsigned int *err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        *abort = 1;
+        atomicOr(err, DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait used while tearing down after an abort: ignores the abort flag (it is
+// already raised) and gives up silently after `timeout_ns`.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+  return true;
+}
+
+// --------------------------------------------------------------------- TMA --
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// Make generic-proxy writes to shared memory visible to the async proxy
+// (tensor-core operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- tcgen05 --
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] . B[smem]^T, bf16 inputs, f32 accumulator, one CTA.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns: thread t of the warp receives the
+// 16 columns of TMEM lane (lane_base + t).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major bf16 tile stored in the
+// 128-byte-swizzled canonical layout: rows of 64 bf16 (128 B), 8-row groups
+// 1024 B apart, tile base 1024-byte aligned.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);   // start address
+  d |= static_cast<uint64_t>(1) << 16;                       // leading byte offset (unused when swizzled)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;               // stride byte offset: 8 rows x 128 B
+  d |= static_cast<uint64_t>(1) << 46;                       // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                       // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16 with bf16 A/B, f32 D, both K-major.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n) {
+  return (1u << 4)                                   // D format f32
+         | (1u << 7)                                 // A format bf16
+         | (1u << 10)                                // B format bf16
+         | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
+}
+
+// ----------------------------------------------------------- bf16 helpers ---
+
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+// d = a*b + c with a single rounding to bf16 per lane.
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+// (a & mask) | c
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(c));
+  return d;
+}
+// Two f32 -> bf16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ uint32_t splat_bf16(uint16_t v) { return static_cast<uint32_t>(v) * 0x00010001u; }
+
+// bf16 value 128 in both halves; (0x4300 | q) is the bf16 value 128 + q for q < 128.
+constexpr uint32_t kBf16x2_128 = 0x43004300u;
+
+// Exact integer code -> bf16 value for 8-bit codes: the byte is placed in the
+// mantissa of the f32 2^23 and 2^23 is subtracted (exact), then narrowed
+// (exact: every integer 0..255 is a bf16).
+__device__ __forceinline__ float code8_to_f32(uint32_t word, uint32_t byte_sel) {
+  const uint32_t bits = prmt(word, 0x4B000000u, 0x7650u | byte_sel);
+  return __uint_as_float(bits) - 8388608.0f;
+}
+
+// ----------------------------------------------------- dequantisation -------
+// Eight consecutive codes of one row -> eight bf16 weights w = bf16(s*q + b),
+// returned as four bf16x2 words.  `s2`/`b2` hold the group's scale and bias in
+// both halves.  The natural order puts code 2j in the low half of word j and
+// code 2j+1 in the high half (k order, as the tensor-core tile needs).
+
+template <int BITS>
+struct Dequant8;
+
+template <>
+struct Dequant8<4> {
+  // `w` holds the eight codes (code j at bits 4j).
+  __device__ __forceinline__ static void natural(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
+    const uint32_t v = w >> 4;   // low nibble of byte j of v = code 2j+1
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      // byte j of w -> byte 0, byte j of v -> byte 2; keep the low nibbles
+      const uint32_t t = prmt(w, v, static_cast<uint32_t>(j) | (static_cast<uint32_t>(4 + j) << 8));
+      const uint32_t q = bf16x2_sub(and_or(t, 0x000F000Fu, kBf16x2_128), kBf16x2_128);
+      o[j] = bf16x2_fma(q, s2, b2);
+    }
+  }
+  // Interleaved order (codes j and j+4 in word j): cheaper, used where the K
+  // order inside an 8-code group is free.
+  __device__ __forceinline__ static void interleaved(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t q = bf16x2_sub(and_or(w >> (4 * j), 0x000F000Fu, kBf16x2_128), kBf16x2_128);
+      o[j] = bf16x2_fma(q, s2, b2);
+    }
+  }
+};
+
+template <>
+struct Dequant8<8> {
+  // `w0` holds codes 0..3, `w1` codes 4..7 (one byte each).
+  __device__ __forceinline__ static void natural(uint32_t w0, uint32_t w1, uint32_t s2, uint32_t b2,
+                                                 uint32_t (&o)[4]) {
+    o[0] = bf16x2_fma(pack_bf16x2(code8_to_f32(w0, 0), code8_to_f32(w0, 1)), s2, b2);
+    o[1] = bf16x2_fma(pack_bf16x2(code8_to_f32(w0, 2), code8_to_f32(w0, 3)), s2, b2);
+    o[2] = bf16x2_fma(pack_bf16x2(code8_to_f32(w1, 0), code8_to_f32(w1, 1)), s2, b2);
+    o[3] = bf16x2_fma(pack_bf16x2(code8_to_f32(w1, 2), code8_to_f32(w1, 3)), s2, b2);
+  }
+  __device__ __forceinline__ static void interleaved(uint32_t w0, uint32_t w1, uint32_t s2, uint32_t b2,
+                                                     uint32_t (&o)[4]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = bf16x2_fma(pack_bf16x2(code8_to_f32(w0, j), code8_to_f32(w1, j)), s2, b2);
+  }
+};
+
+template <>
+struct Dequant8<2> {
+  // `h` holds the eight codes in its low 16 bits (code j at bits 2j).
+  __device__ __forceinline__ static void natural(uint32_t h, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
+    const uint32_t v2 = h >> 2, v4 = h >> 4, v6 = h >> 6;
+    // byte B of h carries codes 4B..4B+3; the low 2 bits of byte B of h, v2,
+    // v4, v6 are codes 4B, 4B+1, 4B+2, 4B+3.
+    const uint32_t t0 = prmt(h, v2, 0x0400u);    // codes 0, 1
+    const uint32_t t1 = prmt(v4, v6, 0x0400u);   // codes 2, 3
+    const uint32_t t2 = prmt(h, v2, 0x0501u);    // codes 4, 5
+    const uint32_t t3 = prmt(v4, v6, 0x0501u);   // codes 6, 7
+    const uint32_t t[4] = {t0, t1, t2, t3};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t q = bf16x2_sub(and_or(t[j], 0x00030003u, kBf16x2_128), kBf16x2_128);
+      o[j] = bf16x2_fma(q, s2, b2);
+    }
+  }
+  __device__ __forceinline__ static void interleaved(uint32_t h, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
+    // codes j and j+4 sit in bytes 0 and 1 at bit 2j
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t t = prmt(h >> (2 * j), 0u, 0x0100u);
+      const uint32_t q = bf16x2_sub(and_or(t, 0x00030003u, kBf16x2_128), kBf16x2_128);
+      o[j] = bf16x2_fma(q, s2, b2);
+    }
+  }
+};
+
+// ---------------------------------------------------------------- epilogue --
+
+enum : int { VAR_MATCH = 0, VAR_F32 = 1, VAR_DEBUG_GATE = 2, VAR_DEBUG_UP = 3 };
+
+__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
+// hidden = silu(g) * u for one element, from the f32 projections.
+__device__ __forceinline__ float swiglu_epilogue(int variant, float g, float u) {
+  if (variant == VAR_MATCH) {
+    const float gb = round_bf16(g), ub = round_bf16(u);
+    const float sig = round_bf16(1.0f / (1.0f + expf(-gb)));
+    const float silu = round_bf16(gb * sig);
+    return silu * ub;   // exact product of two bf16; rounded once by the caller's store
+  }
+  if (variant == VAR_F32) {
+    const float sig = 1.0f / (1.0f + expf(-g));
+    return (g * sig) * u;
+  }
+  return variant == VAR_DEBUG_GATE ? g : u;
+}
+
+}  // namespace qsw

@@ -1,0 +1,36 @@
+// Host-side declarations shared by the qswiglu translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qsw {
+
+// One affine-quantised operand: packed codes [rows, K*bits/32], bf16
+// scales/biases [rows, K/gs].
+struct QuantOperand {
+  const uint32_t *w;
+  const uint16_t *s;
+  const uint16_t *b;
+  int gs;
+  int bits;
+};
+
+// Small-M kernel: rows of x up to 32.  `dual` selects the fused SwiGLU
+// (gate + up, epilogue `variant`) or a single quantised linear (y = bf16(x.W^T)).
+cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
+                        const QuantOperand *op1, int variant, void *out, cudaStream_t stream);
+
+// Tensor-core kernel (tcgen05 + TMA), any M.
+cudaError_t launch_prefill(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
+                           const QuantOperand *op1, int variant, void *out, cudaStream_t stream,
+                           uint64_t timeout_ns, int num_sms);
+
+cudaError_t launch_silu_mul(const void *g, const void *u, int64_t n, int variant, void *out,
+                            cudaStream_t stream);
+
+// Largest M the small-M kernel accepts.
+constexpr int64_t kGemvMaxM = 32;
+
+}  // namespace qsw

@@ -122,6 +122,25 @@ def make_case(M: int, H: int, I: int, *, bits_g: int = 4, gs_g: int = 64,
                           gs_u=gs_u, x_std=x_std, scale_range=tuple(scale_range), seed=seed))
 
 
+def _bits_to_bf16(a: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def _words_to_dev(a: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(dev)
+
+
+def operand_to_device(qm: QuantMatrix, dev):
+    """(packed int32, scales bf16, biases bf16, gs, bits) on `dev`."""
+    return (_words_to_dev(qm.packed, dev), _bits_to_bf16(qm.scales, dev), _bits_to_bf16(qm.biases, dev),
+            qm.gs, qm.bits)
+
+
+def device_args(case: Case, dev):
+    """(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u) as torch tensors on `dev`."""
+    return (_bits_to_bf16(case.x, dev), *operand_to_device(case.gate, dev), *operand_to_device(case.up, dev))
+
+
 def make_x(M: int, H: int, *, x_std: float = 1.0, seed: int = 0) -> np.ndarray:
     gen = torch.Generator(device="cpu").manual_seed(seed)
     return f32_to_bf16_bits(torch.randn((M, H), generator=gen, dtype=torch.float32) * x_std)

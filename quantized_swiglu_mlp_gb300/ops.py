@@ -1,0 +1,220 @@
+"""Python binding of libqswiglu.so (the C ABI in include/qswiglu.h).
+
+Argument marshalling only: tensors are checked for device, dtype and
+contiguity, and their data pointers, sizes and the current CUDA stream are
+passed to the C entry points, which enqueue the CUDA kernels.  There is no
+fallback: if the library is missing or a call fails, these functions raise.
+
+Tensor conventions (torch, all on one CUDA device, contiguous):
+  x            bfloat16 [M, H]           (leading dims are flattened into M)
+  w            int32 or uint32 [rows, H*bits/32]  packed codes, little-endian
+  scales/biases bfloat16 [rows, H/gs]
+  result       bfloat16 [M, rows]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libqswiglu.so")
+
+MATCH, F32, DEBUG_GATE, DEBUG_UP = 0, 1, 2, 3
+VARIANTS = {"match": MATCH, "f32": F32, "debug_gate": DEBUG_GATE, "debug_up": DEBUG_UP}
+CNT_FUSED_TC, CNT_FUSED_GEMV, CNT_QMM_TC, CNT_QMM_GEMV, CNT_SILU_MUL = range(5)
+NUM_COUNTERS = 5
+STATUS = {0: "QSW_OK", 1: "QSW_ERR_INVALID_ARG", 2: "QSW_ERR_UNSUPPORTED", 3: "QSW_ERR_CUDA",
+          4: "QSW_ERR_TIMEOUT"}
+EXPORTED = ("qswiglu_forward", "affine_qmm", "qsw_silu_mul", "qsw_check_device_errors",
+            "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_wait_timeout_ns",
+            "qsw_get_counters", "qsw_reset_counters", "qsw_status_string", "qsw_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QswError(RuntimeError):
+    def __init__(self, fn: str, code: int, message: str):
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} ({message})")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libqswiglu.so and declare its signatures.  Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built; run quantized_swiglu_mlp_gb300.build.build() "
+                               "(or __graft_entry__.build())")
+        lib = ctypes.CDLL(path)
+        p, i64, i32, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+        lib.qswiglu_forward.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, p, p]
+        lib.qswiglu_forward.restype = i32
+        lib.affine_qmm.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p]
+        lib.affine_qmm.restype = i32
+        lib.qsw_silu_mul.argtypes = [p, p, i64, i32, p, p]
+        lib.qsw_silu_mul.restype = i32
+        lib.qsw_check_device_errors.argtypes = [p]
+        lib.qsw_check_device_errors.restype = i32
+        lib.qsw_set_gemv_max_m.argtypes = [i32]
+        lib.qsw_get_gemv_max_m.restype = i32
+        lib.qsw_set_wait_timeout_ns.argtypes = [u64]
+        lib.qsw_get_counters.argtypes = [ctypes.POINTER(u64), i32]
+        lib.qsw_status_string.argtypes = [i32]
+        lib.qsw_status_string.restype = ctypes.c_char_p
+        lib.qsw_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        msg = load_library().qsw_status_string(code).decode()
+        raise QswError(fn, code, msg)
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtypes, device=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+_PACKED = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+_BF16 = (torch.bfloat16,)
+
+
+def _operand(w, s, b, name, device, K, bits, gs):
+    _need(w, f"{name} packed weights", _PACKED, device)
+    _need(s, f"{name} scales", _BF16, device)
+    _need(b, f"{name} biases", _BF16, device)
+    rows = w.shape[0]
+    if w.dim() != 2 or w.shape[1] * 32 != K * bits:
+        raise ValueError(f"{name} packed weights must be [rows, K*bits/32], got {tuple(w.shape)}")
+    if s.shape != (rows, K // gs) or b.shape != s.shape:
+        raise ValueError(f"{name} scales/biases must be [rows, K/gs] = {(rows, K // gs)}")
+    return rows
+
+
+def qswiglu_forward(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant=MATCH,
+                    out=None, stream=None) -> torch.Tensor:
+    """hidden = silu(x . Wg^T) * (x . Wu^T) on the GPU; returns bf16 [..., I]."""
+    lib = load_library()
+    _need(x, "x", _BF16)
+    H = x.shape[-1]
+    x2 = x.reshape(-1, H)
+    M = x2.shape[0]
+    I = _operand(wg, sg, bg, "gate", x.device, H, bits_g, gs_g)
+    if _operand(wu, su, bu, "up", x.device, H, bits_u, gs_u) != I:
+        raise ValueError("gate and up must have the same number of rows")
+    if out is None:
+        out = torch.empty((M, I), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(out, "out", _BF16, x.device)
+        if out.numel() != M * I:
+            raise ValueError("out has the wrong size")
+    code = lib.qswiglu_forward(x2.data_ptr(), M, H, I, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(),
+                               int(gs_g), int(bits_g), wu.data_ptr(), su.data_ptr(), bu.data_ptr(),
+                               int(gs_u), int(bits_u), int(variant), out.data_ptr(), _stream_ptr(stream))
+    _check("qswiglu_forward", code)
+    return out.view(*x.shape[:-1], I)
+
+
+def affine_qmm(x, w, s, b, gs, bits, y=None, stream=None) -> torch.Tensor:
+    """y = bf16(x . W^T) with W affine-quantised; returns bf16 [..., N]."""
+    lib = load_library()
+    _need(x, "x", _BF16)
+    K = x.shape[-1]
+    x2 = x.reshape(-1, K)
+    M = x2.shape[0]
+    N = _operand(w, s, b, "w", x.device, K, bits, gs)
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(y, "y", _BF16, x.device)
+        if y.numel() != M * N:
+            raise ValueError("y has the wrong size")
+    code = lib.affine_qmm(x2.data_ptr(), M, K, N, w.data_ptr(), s.data_ptr(), b.data_ptr(),
+                          int(gs), int(bits), y.data_ptr(), _stream_ptr(stream))
+    _check("affine_qmm", code)
+    return y.view(*x.shape[:-1], N)
+
+
+def qsw_silu_mul(g, u, variant=MATCH, out=None, stream=None) -> torch.Tensor:
+    """out = silu(g) * u elementwise over bf16 tensors of equal shape."""
+    lib = load_library()
+    _need(g, "g", _BF16)
+    _need(u, "u", _BF16, g.device)
+    if g.shape != u.shape:
+        raise ValueError("g and u must have the same shape")
+    if out is None:
+        out = torch.empty_like(g)
+    else:
+        _need(out, "out", _BF16, g.device)
+        if out.numel() != g.numel():
+            raise ValueError("out has the wrong size")
+    _check("qsw_silu_mul", lib.qsw_silu_mul(g.data_ptr(), u.data_ptr(), g.numel(), int(variant),
+                                            out.data_ptr(), _stream_ptr(stream)))
+    return out
+
+
+def unfused_swiglu(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant=MATCH,
+                   stream=None) -> torch.Tensor:
+    """The unfused comparison path: two affine_qmm calls, then silu*mul."""
+    g = affine_qmm(x, wg, sg, bg, gs_g, bits_g, stream=stream)
+    u = affine_qmm(x, wu, su, bu, gs_u, bits_u, stream=stream)
+    return qsw_silu_mul(g, u, variant, out=g, stream=stream)
+
+
+def qsw_check_device_errors(stream=None) -> None:
+    _check("qsw_check_device_errors", load_library().qsw_check_device_errors(_stream_ptr(stream)))
+
+
+def qsw_set_gemv_max_m(m: int) -> None:
+    load_library().qsw_set_gemv_max_m(int(m))
+
+
+def qsw_get_gemv_max_m() -> int:
+    return int(load_library().qsw_get_gemv_max_m())
+
+
+def qsw_set_wait_timeout_ns(ns: int) -> None:
+    load_library().qsw_set_wait_timeout_ns(int(ns))
+
+
+def qsw_get_counters() -> list[int]:
+    arr = (ctypes.c_uint64 * NUM_COUNTERS)()
+    load_library().qsw_get_counters(arr, NUM_COUNTERS)
+    return list(arr)
+
+
+def qsw_reset_counters() -> None:
+    load_library().qsw_reset_counters()
+
+
+def qsw_status_string(code: int) -> str:
+    return load_library().qsw_status_string(int(code)).decode()
+
+
+def qsw_version() -> int:
+    return int(load_library().qsw_version())

@@ -1,0 +1,122 @@
+"""The C ABI on the CPU: the library loads, exports every symbol the header
+declares, and rejects bad arguments on the host before any CUDA call.
+No compute is launched here (no GPU in this environment)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from quantized_swiglu_mlp_gb300 import build as qbuild
+from quantized_swiglu_mlp_gb300 import ops
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "qswiglu.h")
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return ops.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"QSW_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    assert set(names) == set(ops.EXPORTED), names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+FAKE = 0x10000          # aligned, never dereferenced: validation fails or M == 0 first
+
+
+def fwd(lib, M=4, H=256, I=64, gs_g=64, bits_g=4, gs_u=64, bits_u=4, variant=0,
+        x=FAKE, wg=FAKE, sg=FAKE, bg=FAKE, wu=FAKE, su=FAKE, bu=FAKE, out=FAKE):
+    return lib.qswiglu_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u,
+                               variant, out, None)
+
+
+def test_m_zero_is_a_noop(lib):
+    assert fwd(lib, M=0) == OK
+    assert lib.affine_qmm(FAKE, 0, 256, 64, FAKE, FAKE, FAKE, 64, 4, FAKE, None) == OK
+    assert lib.qsw_silu_mul(FAKE, FAKE, 0, 0, FAKE, None) == OK
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), INVALID),
+    (dict(H=0), INVALID),
+    (dict(I=0), INVALID),
+    (dict(H=48), UNSUPPORTED),                 # H % 32 != 0
+    (dict(gs_g=48), UNSUPPORTED),              # group size not a multiple of 32
+    (dict(gs_u=96), UNSUPPORTED),              # does not divide H=256
+    (dict(bits_g=3), UNSUPPORTED),
+    (dict(bits_u=16), UNSUPPORTED),
+    (dict(bits_g=2, H=96, gs_g=32, gs_u=32), UNSUPPORTED),   # 2-bit needs H % 64 == 0
+    (dict(variant=7), INVALID),
+    (dict(x=0), INVALID),
+    (dict(wg=0), INVALID),
+    (dict(su=0), INVALID),
+    (dict(out=0), INVALID),
+    (dict(x=FAKE + 8), UNSUPPORTED),           # 16-byte alignment
+    (dict(wu=FAKE + 4), UNSUPPORTED),
+    (dict(out=FAKE + 2), UNSUPPORTED),
+    (dict(sg=FAKE + 1), UNSUPPORTED),
+])
+def test_forward_rejects(lib, kw, code):
+    assert fwd(lib, **kw) == code
+
+
+def test_affine_qmm_rejects(lib):
+    assert lib.affine_qmm(FAKE, 4, 100, 64, FAKE, FAKE, FAKE, 32, 4, FAKE, None) == UNSUPPORTED
+    assert lib.affine_qmm(FAKE, 4, 256, -1, FAKE, FAKE, FAKE, 64, 4, FAKE, None) == INVALID
+    assert lib.affine_qmm(0, 4, 256, 64, FAKE, FAKE, FAKE, 64, 4, FAKE, None) == INVALID
+    assert lib.affine_qmm(FAKE, 4, 256, 64, FAKE, FAKE, FAKE, 64, 5, FAKE, None) == UNSUPPORTED
+
+
+def test_silu_mul_rejects(lib):
+    assert lib.qsw_silu_mul(FAKE, FAKE, -1, 0, FAKE, None) == INVALID
+    assert lib.qsw_silu_mul(FAKE, FAKE, 8, 2, FAKE, None) == INVALID     # debug variants only fuse
+    assert lib.qsw_silu_mul(0, FAKE, 8, 0, FAKE, None) == INVALID
+    assert lib.qsw_silu_mul(FAKE + 2, FAKE, 8, 0, FAKE, None) == UNSUPPORTED
+
+
+def test_gemv_limit_is_clamped(lib):
+    saved = ops.qsw_get_gemv_max_m()
+    try:
+        ops.qsw_set_gemv_max_m(1000)
+        assert ops.qsw_get_gemv_max_m() == 32
+        ops.qsw_set_gemv_max_m(-5)
+        assert ops.qsw_get_gemv_max_m() == 0
+        ops.qsw_set_gemv_max_m(8)
+        assert ops.qsw_get_gemv_max_m() == 8
+    finally:
+        ops.qsw_set_gemv_max_m(saved)
+
+
+def test_counters_and_strings(lib):
+    ops.qsw_reset_counters()
+    assert ops.qsw_get_counters() == [0] * ops.NUM_COUNTERS
+    assert fwd(lib, M=0) == OK                       # a no-op launches nothing
+    assert ops.qsw_get_counters() == [0] * ops.NUM_COUNTERS
+    assert ops.qsw_status_string(0) == "ok"
+    assert "unsupported" in ops.qsw_status_string(2)
+    assert ops.qsw_status_string(99) == "unknown status"
+    assert ops.qsw_version() >= 100
+
+
+def test_python_binding_rejects_host_tensors(lib):
+    import torch
+    x = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ops.qswiglu_forward(x, x, x, x, 64, 4, x, x, x, 64, 4)

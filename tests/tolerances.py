@@ -1,0 +1,68 @@
+"""Acceptance bounds of the GPU path against the oracle.
+
+MATCH:  |gpu - oracle| <= 2 bf16 ulps of the oracle value + 1e-3, elementwise;
+        the stored gate/up projections (debug variants) equal the oracle's on
+        at least 99.9 % of elements.
+F32:    |gpu - oracle| <= 1e-3 + 8e-3 * |oracle|, elementwise.
+Integer and byte results are compared bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+MATCH_ULPS = 2
+ABS_TOL = 1e-3
+F32_RTOL = 8e-3
+EXACT_FRACTION = 0.999
+
+
+def bf16_to_f64(h) -> np.ndarray:
+    h = np.asarray(h, dtype=np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 numbers at |v| (8 significant bits, subnormal floor)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -126.0)
+    return np.where(a > 0, np.exp2(e - 7.0), 2.0 ** -133)
+
+
+def _summary(gpu, ref, bound):
+    err = np.abs(gpu - ref)
+    bad = ~(err <= bound)
+    n_bad = int(bad.sum())
+    info = {"n": int(gpu.size), "n_bad": n_bad, "max_err": float(err.max()) if err.size else 0.0}
+    if n_bad:
+        idx = np.argwhere(bad.reshape(np.shape(gpu)) if np.ndim(gpu) else bad)[:5]
+        info["first_bad"] = [(tuple(int(t) for t in i), float(np.asarray(gpu).reshape(np.shape(gpu))[tuple(i)]),
+                              float(np.asarray(ref).reshape(np.shape(ref))[tuple(i)])) for i in idx]
+    return n_bad == 0, info
+
+
+def check_match(gpu_bits, oracle_bits):
+    gpu, ref = bf16_to_f64(gpu_bits), bf16_to_f64(oracle_bits)
+    return _summary(gpu, ref, MATCH_ULPS * bf16_ulp(ref) + ABS_TOL)
+
+
+def check_f32(gpu_bits, oracle_bits):
+    gpu, ref = bf16_to_f64(gpu_bits), bf16_to_f64(oracle_bits)
+    return _summary(gpu, ref, ABS_TOL + F32_RTOL * np.abs(ref))
+
+
+def exact_fraction(gpu_bits, oracle_bits) -> float:
+    a = np.asarray(gpu_bits, dtype=np.uint16)
+    b = np.asarray(oracle_bits, dtype=np.uint16)
+    return float((a == b).mean()) if a.size else 1.0
+
+
+def check_projection(gpu_bits, oracle_bits):
+    """Stored gate/up projection: >= 99.9 % bit-identical, the rest within
+    1 ulp + 1e-3 (the absolute term covers sums that cancel to near zero)."""
+    frac = exact_fraction(gpu_bits, oracle_bits)
+    gpu, ref = bf16_to_f64(gpu_bits), bf16_to_f64(oracle_bits)
+    ok_close, info = _summary(gpu, ref, bf16_ulp(ref) + ABS_TOL)
+    info["exact_fraction"] = frac
+    return (frac >= EXACT_FRACTION and ok_close), info
