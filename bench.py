@@ -222,7 +222,7 @@ def bench_decode(args, dev, stream, peaks, peak_src):
 
     # soak so that the clock sampler sees the GPU under this load
     sampler = ClockSampler(dev.index).start()
-    t_end = time.time() + 1.0
+    t_end = time.time() + args.soak_seconds
     while time.time() < t_end:
         for i in range(200):
             step(i)
@@ -269,6 +269,18 @@ def bench_prefill(args, dev, stream, peaks, peak_src):
     from quantized_swiglu_mlp_gb300 import inputs, ops
 
     res = {}
+    if args.only in ("all", "large"):
+        res.update(_bench_large(args, dev, stream, peaks, peak_src))
+    if args.only in ("all", "mid"):
+        res.update(_bench_mid(args, dev, stream))
+    return res
+
+
+def _bench_large(args, dev, stream, peaks, peak_src):
+    import torch
+    from quantized_swiglu_mlp_gb300 import inputs, ops
+
+    res = {}
     case = inputs.workload_case("large_prefill")
     a = to_device(case, dev)
     out = torch.empty((case.M, case.I), dtype=torch.bfloat16, device=dev)
@@ -288,7 +300,14 @@ def bench_prefill(args, dev, stream, peaks, peak_src):
                              "algorithmic_flops_per_launch": flops}
     del a, out
     torch.cuda.empty_cache()
+    return res
 
+
+def _bench_mid(args, dev, stream):
+    import torch
+    from quantized_swiglu_mlp_gb300 import inputs, ops
+
+    res = {}
     case = inputs.workload_case("mid_prefill")
     a = to_device(case, dev)
     out = torch.empty((case.M, case.I), dtype=torch.bfloat16, device=dev)
@@ -346,8 +365,15 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
 
     with torch.cuda.stream(stream):
-        d = bench_decode(args, dev, stream, peaks, peak_src)
-        prefill = bench_prefill(args, dev, stream, peaks, peak_src) if not args.no_prefill else None
+        d = bench_decode(args, dev, stream, peaks, peak_src) if args.only in ("all", "decode") else None
+        prefill = None
+        if not args.no_prefill and args.only != "decode":
+            prefill = bench_prefill(args, dev, stream, peaks, peak_src)
+
+    if d is None:   # a profiling run of one prefill workload: report only what ran
+        if rank == 0:
+            print(json.dumps({"only": args.only, "prefill": prefill}), flush=True)
+        return
 
     value = d["total_bytes"] / (d["ms"] / 1e3) / 1e9
     e2e = d["e2e_bytes"] / (d["e2e_ms"] / 1e3) / 1e9
@@ -463,6 +489,10 @@ def main(argv=None):
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--only", choices=["all", "decode", "large", "mid"], default="all",
+                    help="run one workload only (profiling); the JSON line then carries what ran")
+    ap.add_argument("--soak-seconds", type=float, default=1.0,
+                    help="untimed load before the timed region, so the clock sampler sees it")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -9,11 +9,12 @@
 #include <cstdlib>
 #include <mutex>
 
-#include "../../include/qswiglu.h"
+#include "qswiglu.h"
 #include "qsw_internal.h"
 
 namespace qsw {
 cudaError_t prefill_take_errors(unsigned int *out);
+cudaError_t gemv_take_errors(unsigned int *out);
 }
 
 namespace {
@@ -89,15 +90,15 @@ qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const
   if (variant < QSW_MATCH || variant > QSW_DEBUG_UP) return QSW_ERR_INVALID_ARG;
   if ((st = check_operand(wg, sg, bg, H, gs_g, bits_g)) != QSW_OK) return st;
   if ((st = check_operand(wu, su, bu, H, gs_u, bits_u)) != QSW_OK) return st;
+  if (M == 0) return QSW_OK;   // nothing to read or write: x and out may be null
   if (!x || !out) return QSW_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(out, 16)) return QSW_ERR_UNSUPPORTED;
-  if (M == 0) return QSW_OK;
 
   const qsw::QuantOperand g{wg, static_cast<const uint16_t *>(sg), static_cast<const uint16_t *>(bg), gs_g, bits_g};
   const qsw::QuantOperand u{wu, static_cast<const uint16_t *>(su), static_cast<const uint16_t *>(bu), gs_u, bits_u};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (M <= gemv_max_m()) {
-    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, out, s));
+  if (M <= gemv_max_m() && qsw::gemv_fits(M, H, I, g, &u, sm_count())) {
+    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count()));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
     st = from_cuda(qsw::launch_prefill(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count()));
@@ -111,14 +112,14 @@ qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N, const uint
   qsw_status st = check_shape(M, K, N);
   if (st != QSW_OK) return st;
   if ((st = check_operand(w, s, b, K, gs, bits)) != QSW_OK) return st;
+  if (M == 0) return QSW_OK;   // nothing to read or write: x and y may be null
   if (!x || !y) return QSW_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(y, 16)) return QSW_ERR_UNSUPPORTED;
-  if (M == 0) return QSW_OK;
 
   const qsw::QuantOperand op{w, static_cast<const uint16_t *>(s), static_cast<const uint16_t *>(b), gs, bits};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (M <= gemv_max_m()) {
-    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs));
+  if (M <= gemv_max_m() && qsw::gemv_fits(M, K, N, op, nullptr, sm_count())) {
+    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs, g_timeout_ns.load(), sm_count()));
     if (st == QSW_OK) g_counters[QSW_CNT_QMM_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
     st = from_cuda(qsw::launch_prefill(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs, g_timeout_ns.load(),
@@ -141,9 +142,10 @@ qsw_status qsw_silu_mul(const void *g, const void *u, int64_t n, int variant, vo
 
 qsw_status qsw_check_device_errors(void *stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QSW_ERR_CUDA;
-  unsigned int bits = 0;
-  if (qsw::prefill_take_errors(&bits) != cudaSuccess) return QSW_ERR_CUDA;
-  return bits ? QSW_ERR_TIMEOUT : QSW_OK;
+  unsigned int a = 0, b = 0;
+  if (qsw::prefill_take_errors(&a) != cudaSuccess) return QSW_ERR_CUDA;
+  if (qsw::gemv_take_errors(&b) != cudaSuccess) return QSW_ERR_CUDA;
+  return (a | b) ? QSW_ERR_TIMEOUT : QSW_OK;
 }
 
 void qsw_set_gemv_max_m(int m) {

@@ -67,6 +67,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended by the hardware for up to
+// `hint_ns` until the phase completes, instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the barrier's phase with the given parity has completed.  Never
 // spins forever: gives up after `timeout_ns`, or as soon as another role of the
 // CTA has raised `abort`.  Returns false when it gave up.
@@ -85,6 +99,35 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
       }
     }
   }
+}
+
+// Warp-collective wait for waits that may be long: lane 0 waits with the
+// hardware suspend hint (the thread sleeps until the phase completes, so an
+// idle warp takes no issue slots from the warps doing work), then every lane
+// observes the completed phase itself (immediate).  The result is
+// warp-uniform; false means "give up".
+__device__ __forceinline__ bool warp_wait_lazy(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                               uint64_t timeout_ns, unsigned int *err, uint32_t suspend_ns) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0 && !mbar_try_wait(bar, parity)) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      if (mbar_try_wait_suspend(bar, parity, suspend_ns)) break;
+      if (*abort) {
+        ok = 0;
+        break;
+      }
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        *abort = 1;
+        atomicOr(err, DEVERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return false;
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, timeout_ns, err));
 }
 
 // Wait used while tearing down after an abort: ignores the abort flag (it is
@@ -168,6 +211,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Inverse of tmem_ld16: thread t writes 16 consecutive columns of TMEM lane
+// (lane_base + t).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a K-major bf16 tile stored in the
 // 128-byte-swizzled canonical layout: rows of 64 bf16 (128 B), 8-row groups
@@ -311,6 +366,26 @@ struct Dequant8<2> {
       const uint32_t q = bf16x2_sub(and_or(t, 0x00030003u, kBf16x2_128), kBf16x2_128);
       o[j] = bf16x2_fma(q, s2, b2);
     }
+  }
+};
+
+// ------------------------------------------------------------- group index --
+
+// k / gs for the scale/bias group of code k without a runtime division when gs
+// is a power of two (shift >= 0); otherwise a 32-bit division.
+struct GroupDiv {
+  int gs;
+  int shift;   // log2(gs) when gs is a power of two, else -1
+  __host__ __device__ static GroupDiv make(int g) {
+    int s = -1;
+    if (g > 0 && (g & (g - 1)) == 0) {
+      s = 0;
+      while ((1 << s) < g) ++s;
+    }
+    return GroupDiv{g, s};
+  }
+  __device__ __forceinline__ uint32_t operator()(uint32_t k) const {
+    return shift >= 0 ? (k >> shift) : k / static_cast<uint32_t>(gs);
   }
 };
 

@@ -2,35 +2,69 @@
 // the single quantised linear at small M.
 //
 // Method: mlx-bun pages, src/model/fused-swiglu-kernel.ts -- at decode the two
-// projections are memory-bound GEMVs and "reading Wg/Wu dominates".  Here the
-// packed rows are streamed once with 128-bit loads, dequantised in registers to
-// bf16 (w = bf16(s*q + b), one rounding) and reduced over K on the tensor
-// cores with mma.sync m16n8k16 (a cheap reduction engine for this HBM-bound
-// path; the contraction is not what bounds it).
+// projections are memory-bound GEMVs and "reading Wg/Wu dominates".  The design
+// streams the packed rows from HBM exactly once, as early and as deep as
+// possible, and keeps everything but the dequantisation off the critical path:
 //
-// Work split: one CTA owns 16 output rows (i); its 8 warps split K in blocks
-// of 128 codes.  Inside a block, lane (g = lane/4, c = lane%4) owns the
-// 32-code chunk c of rows g and g+8.  The order of K inside an 8-code group
-// is free as long as A (weights) and B (x) agree, so each lane dequantises
-// with the interleaved pairing (codes j, j+4) and permutes its own x values
-// the same way.  Partial sums meet in shared memory in a fixed order.
+//  * unit of work: 8 output rows (fused: rows r..r+7 of Wg AND of Wu) or 16
+//    rows (single linear).  One persistent CTA per SM takes units round-robin.
+//  * a unit's rows are contiguous in HBM: ONE 1-D bulk (TMA) copy per array
+//    (codes of each operand, each scale and bias array) lands it in a
+//    shared-memory ring slot, completing on the slot's mbarrier.  At kernel
+//    start every slot is in flight, so each SM requests its share at once.
+//  * the 16 warps form 4 groups of 4; group q takes the CTA's units q, q+4, ...
+//    and its 4 warps split K in 128-code blocks, so every warp does several
+//    blocks per unit and the per-unit bookkeeping stays small.  One warp of the
+//    group adds the 4 partial sums in a fixed order and applies the epilogue.
+//  * x is the same for every unit: it is staged once per CTA in shared memory,
+//    already permuted into MMA B-fragment order (bank-conflict-free reads).
+//  * a lane (g = lane/4, c = lane%4) dequantises 32 codes of gate row g and of
+//    up row g to bf16 in registers (w = bf16(s*q + b), one rounding) and feeds
+//    them as A rows g and g+8 of mma.sync m16n8k16 with x (8 rows, zero padded)
+//    as B: one MMA yields gate and up of the same outputs.  The K order inside
+//    each 8-code group is interleaved (codes j, j+4); x is permuted the same way.
+//  * each 128-code block accumulates in a fresh fragment that is then added to
+//    the warp's running f32 sum (short tensor-core accumulation chains).
+//
+// Every wait is bounded; on a timeout the CTA raises an abort flag, lets its
+// own copies land and returns, and the host reads the device error word.
+#include <atomic>
+
 #include "qsw_device.cuh"
 #include "qsw_internal.h"
 
 namespace qsw {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kBlockK = 128;   // codes per K block
-constexpr int kChunk = 32;     // codes per lane per block
+constexpr int kGroupWarps = 4;                  // warps sharing one unit
+constexpr int kGroups = kWarps / kGroupWarps;   // units in progress per CTA
+constexpr int kBlockK = 128;                    // codes per K block
+constexpr int kChunk = 32;                      // codes per lane per block
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kMaxSlots = 16;
+constexpr int kXBlockBytes = 4 * 32 * 16;       // B fragments of one block, one x row group (2 KB)
+
+__device__ unsigned int g_gemv_error;
 
 struct GemvParams {
   const uint16_t *x;
-  int64_t M, K, N;
-  QuantOperand op[2];
+  int M, K, N;
+  const uint32_t *w0, *w1;
+  const uint16_t *s0, *b0, *s1, *b1;
+  GroupDiv gd0, gd1;
+  uint32_t ng0, ng1;      // groups per row (K / gs)
   int variant;
   uint16_t *out;
+  int units, slots;
+  int pitch0, pitch1;     // packed bytes per row of operand 0 / 1
+  int sb_off;             // byte offset of the scale/bias rows inside a slot
+  int slot_bytes;
+  int x_off;              // byte offset of the staged x fragments
+  int red_off;            // byte offset of the partial sums
+  int bar_off;            // byte offset of the barriers
+  uint64_t timeout_ns;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -41,43 +75,53 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Packed words covering one lane's 32 codes of one row.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// 32 codes of one row (the lane's chunk of a 128-code block), from shared memory.
 template <int BITS>
-struct RowChunk {
+struct Chunk {
   static constexpr int kWords = kChunk * BITS / 32;   // 4, 8 or 2
   uint32_t w[kWords];
-  uint32_t s2, b2;   // group scale/bias splatted to bf16x2
-
-  __device__ __forceinline__ void load(const QuantOperand &op, int64_t row, int64_t k, int64_t K, bool valid) {
-    if (!valid) {
-#pragma unroll
-      for (int i = 0; i < kWords; ++i) w[i] = 0;
-      s2 = 0;
-      b2 = 0;
-      return;
-    }
-    const uint32_t *p = op.w + row * (K * BITS / 32) + k * BITS / 32;
+  __device__ __forceinline__ void load(uint32_t addr) {
     if constexpr (BITS == 2) {
-      const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+      const uint2 v = lds64(addr);
       w[0] = v.x;
       w[1] = v.y;
     } else {
 #pragma unroll
       for (int i = 0; i < kWords / 4; ++i) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p) + i);
+        const uint4 v = lds128(addr + 16 * i);
         w[4 * i + 0] = v.x;
         w[4 * i + 1] = v.y;
         w[4 * i + 2] = v.z;
         w[4 * i + 3] = v.w;
       }
     }
-    const int64_t gidx = row * (K / op.gs) + k / op.gs;
-    s2 = splat_bf16(__ldg(op.s + gidx));
-    b2 = splat_bf16(__ldg(op.b + gidx));
   }
-
-  // Eight dequantised codes (sub-chunk j), interleaved pairing.
-  __device__ __forceinline__ void dequant(int j, uint32_t (&o)[4]) const {
+  // eight codes (sub-chunk j), interleaved pairing (codes p, p+4 in word p)
+  __device__ __forceinline__ void dequant(int j, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) const {
     if constexpr (BITS == 4) {
       Dequant8<4>::interleaved(w[j], s2, b2, o);
     } else if constexpr (BITS == 8) {
@@ -88,193 +132,405 @@ struct RowChunk {
   }
 };
 
-template <int BITS0, int BITS1, bool DUAL, int NG>
-struct BlockData {
-  RowChunk<BITS0> a0[2];             // operand 0, rows g and g+8
-  RowChunk<BITS1> a1[DUAL ? 2 : 1];  // operand 1 (unused when single)
-  uint4 xv[NG][4];                   // x rows 8G+g, 32 values
-};
-
-template <int BITS0, int BITS1, bool DUAL, int NG>
-__device__ __forceinline__ void load_block(const GemvParams &p, int64_t kb, int64_t r0, int g, int c,
-                                           BlockData<BITS0, BITS1, DUAL, NG> &bd) {
-  const int64_t k = kb * kBlockK + c * kChunk;
-  const bool kvalid = k < p.K;
-  bd.a0[0].load(p.op[0], r0, k, p.K, kvalid && r0 < p.N);
-  bd.a0[1].load(p.op[0], r0 + 8, k, p.K, kvalid && r0 + 8 < p.N);
-  if constexpr (DUAL) {
-    bd.a1[0].load(p.op[1], r0, k, p.K, kvalid && r0 < p.N);
-    bd.a1[1].load(p.op[1], r0 + 8, k, p.K, kvalid && r0 + 8 < p.N);
+// Issue the bulk copies of unit u into a slot (lanes 0..5 of the calling warp).
+template <int BITS0, int BB, bool DUAL>
+__device__ __forceinline__ void issue_unit(const GemvParams &p, uint8_t *base, uint64_t *bar, unsigned int *issued,
+                                           int u, int lane) {
+  constexpr int R = DUAL ? 8 : 16;
+  const uint32_t r0 = static_cast<uint32_t>(u) * R;
+  const uint32_t rows = static_cast<uint32_t>(p.N) - r0 < static_cast<uint32_t>(R) ? static_cast<uint32_t>(p.N) - r0
+                                                                                     : static_cast<uint32_t>(R);
+  const uint32_t sb0 = R * p.ng0 * 2, sb1 = DUAL ? R * p.ng1 * 2 : 0;   // bytes of one s/b array region
+  if (lane == 0) {
+    const uint32_t bytes = rows * (p.pitch0 + (DUAL ? p.pitch1 : 0)) + rows * 4 * (p.ng0 + (DUAL ? p.ng1 : 0));
+    mbar_arrive_expect_tx(bar, bytes);
+    *issued += 1;   // fills of this slot so far (for draining after an abort)
   }
-#pragma unroll
-  for (int G = 0; G < NG; ++G) {
-    const int64_t m = 8 * G + g;
-    if (kvalid && m < p.M) {
-      const uint4 *xp = reinterpret_cast<const uint4 *>(p.x + m * p.K + k);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) bd.xv[G][i] = __ldg(xp + i);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) bd.xv[G][i] = make_uint4(0, 0, 0, 0);
-    }
+  __syncwarp();
+  if (lane == 0)
+    bulk_copy_g2s(base, p.w0 + static_cast<int64_t>(r0) * (p.pitch0 / 4), rows * p.pitch0, bar);
+  if (DUAL && lane == 1)
+    bulk_copy_g2s(base + R * p.pitch0, p.w1 + static_cast<int64_t>(r0) * (p.pitch1 / 4), rows * p.pitch1, bar);
+  if (lane >= 2 && lane < (DUAL ? 6 : 4)) {
+    const int arr = lane - 2;   // s0, b0, s1, b1
+    const uint16_t *src = arr == 0 ? p.s0 : arr == 1 ? p.b0 : arr == 2 ? p.s1 : p.b1;
+    const uint32_t ng = arr < 2 ? p.ng0 : p.ng1;
+    const uint32_t region = arr < 2 ? arr * sb0 : 2 * sb0 + (arr - 2) * sb1;
+    bulk_copy_g2s(base + p.sb_off + region, src + static_cast<int64_t>(r0) * ng, rows * ng * 2, bar);
   }
 }
 
 template <int BITS0, int BITS1, bool DUAL, int NG>
-__device__ __forceinline__ void compute_block(const BlockData<BITS0, BITS1, DUAL, NG> &bd,
-                                              float (&acc0)[NG][4], float (&acc1)[NG][4]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t p0r0[4], p0r1[4];
-    bd.a0[0].dequant(j, p0r0);
-    bd.a0[1].dequant(j, p0r1);
-    uint32_t p1r0[4], p1r1[4];
-    if constexpr (DUAL) {
-      bd.a1[0].dequant(j, p1r0);
-      bd.a1[1].dequant(j, p1r1);
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t a0[4] = {p0r0[2 * h], p0r1[2 * h], p0r0[2 * h + 1], p0r1[2 * h + 1]};
-      uint32_t a1[4] = {0, 0, 0, 0};
-      if constexpr (DUAL) {
-        a1[0] = p1r0[2 * h];
-        a1[1] = p1r1[2 * h];
-        a1[2] = p1r0[2 * h + 1];
-        a1[3] = p1r1[2 * h + 1];
-      }
-#pragma unroll
-      for (int G = 0; G < NG; ++G) {
-        // x values of sub-chunk j: q0=(x0,x1) q1=(x2,x3) q2=(x4,x5) q3=(x6,x7);
-        // the weights pair codes (p, p+4), so x is paired the same way.
-        const uint4 xs = bd.xv[G][j];
-        uint32_t b0, b1;
-        if (h == 0) {
-          b0 = prmt(xs.x, xs.z, 0x5410u);   // (x0, x4)
-          b1 = prmt(xs.x, xs.z, 0x7632u);   // (x1, x5)
-        } else {
-          b0 = prmt(xs.y, xs.w, 0x5410u);   // (x2, x6)
-          b1 = prmt(xs.y, xs.w, 0x7632u);   // (x3, x7)
-        }
-        mma_bf16_16816(acc0[G], a0, b0, b1);
-        if constexpr (DUAL) mma_bf16_16816(acc1[G], a1, b0, b1);
-      }
-    }
-  }
-}
-
-template <int BITS0, int BITS1, bool DUAL, int NG>
-__global__ void __launch_bounds__(kThreads) gemv_kernel(const GemvParams p) {
-  constexpr int NMAT = DUAL ? 2 : 1;
-  __shared__ float red[kWarps][NMAT][NG][32][4];
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
+  constexpr int R = DUAL ? 8 : 16;          // output rows per unit
+  constexpr int BB = DUAL ? BITS1 : BITS0;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);               // [kMaxSlots]
+  uint64_t *red_full = full + kMaxSlots;                                          // [kGroups][2]
+  uint64_t *red_free = red_full + 2 * kGroups;                                    // [kGroups][2]
+  unsigned int *done_cnt = reinterpret_cast<unsigned int *>(red_free + 2 * kGroups);   // [kMaxSlots]
+  unsigned int *issued_cnt = done_cnt + kMaxSlots;                                     // [kMaxSlots]
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(issued_cnt + kMaxSlots);
+  float *red = reinterpret_cast<float *>(smem + p.red_off);   // [kGroups][2][kGroupWarps][NG][32][4]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 16 + g;
-  const int64_t nkb = (p.K + kBlockK - 1) / kBlockK;
+  unsigned int *err = &g_gemv_error;
+  const uint32_t K = static_cast<uint32_t>(p.K);
+  const uint32_t nkb = (K + kBlockK - 1) / kBlockK;
+  const int my_units = (p.units - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                       static_cast<int>(gridDim.x);
+  auto unit_of = [&](int i) { return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x); };
 
-  float acc0[NG][4], acc1[NG][4];
-#pragma unroll
-  for (int G = 0; G < NG; ++G)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc0[G][i] = acc1[G][i] = 0.0f;
-
-  // Two blocks in flight per warp: the loads of both are issued before either
-  // is consumed.
-  int64_t kb = warp;
-  for (; kb + kWarps < nkb; kb += 2 * kWarps) {
-    BlockData<BITS0, BITS1, DUAL, NG> d0, d1;
-    load_block(p, kb, r0, g, c, d0);
-    load_block(p, kb + kWarps, r0, g, c, d1);
-    compute_block(d0, acc0, acc1);
-    compute_block(d1, acc0, acc1);
-  }
-  if (kb < nkb) {
-    BlockData<BITS0, BITS1, DUAL, NG> d0;
-    load_block(p, kb, r0, g, c, d0);
-    compute_block(d0, acc0, acc1);
-  }
-
-#pragma unroll
-  for (int G = 0; G < NG; ++G)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      red[warp][0][G][lane][i] = acc0[G][i];
-      if constexpr (DUAL) red[warp][NMAT - 1][G][lane][i] = acc1[G][i];
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.slots; ++s) {
+      mbar_init(&full[s], 1);
+      done_cnt[s] = 0;
+      issued_cnt[s] = 0;
     }
+    for (int b = 0; b < 2 * kGroups; ++b) {
+      mbar_init(&red_full[b], kGroupWarps);
+      mbar_init(&red_free[b], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // Each group owns `spg` slots and uses them in turn, so a slot only ever
+  // holds the units of one group, in order (a waiter is never more than one
+  // fill ahead of its slot).  Warp 0 puts the first units of every slot in
+  // flight; later fills are issued by the group's warp that finishes last.
+  const int spg = p.slots / kGroups;
+  if (warp == 0) {
+    for (int q = 0; q < kGroups; ++q)
+      for (int s = 0; s < spg; ++s) {
+        const int i = q + s * kGroups;
+        if (i < my_units)
+          issue_unit<BITS0, BB, DUAL>(p, smem + (q * spg + s) * p.slot_bytes, &full[q * spg + s],
+                                      &issued_cnt[q * spg + s], unit_of(i), lane);
+      }
+  }
+  // x -> shared memory in B-fragment order, once per CTA: for block kb, x row
+  // group G, fragment word q (0..15) of lane L = 4n + c sits at
+  // ((kb*NG + G)*4 + q/4)*512 + L*16 + (q%4)*4 bytes
+  {
+    const int total = static_cast<int>(nkb) * NG * 32;   // (kb, G, lane) triples
+    for (int e = threadIdx.x; e < total; e += kThreads) {
+      const int L = e & 31, G = (e >> 5) % NG, kb = (e >> 5) / NG;
+      const int n = L >> 2, c = L & 3, m = 8 * G + n;
+      const uint32_t k = static_cast<uint32_t>(kb) * kBlockK + c * kChunk;
+      uint4 xv[4];
+      if (k < K && m < p.M) {
+        const uint4 *xp = reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(m) * p.K + k);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xv[q] = __ldg(xp + q);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xv[q] = make_uint4(0, 0, 0, 0);
+      }
+      uint8_t *dst = smem + p.x_off + static_cast<size_t>(kb * NG + G) * kXBlockBytes + L * 16;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {   // x values 8j..8j+7: (x0,x1) (x2,x3) (x4,x5) (x6,x7)
+        const uint4 f = make_uint4(prmt(xv[j].x, xv[j].z, 0x5410u),    // h=0: (x0, x4)
+                                   prmt(xv[j].x, xv[j].z, 0x7632u),    //      (x1, x5)
+                                   prmt(xv[j].y, xv[j].w, 0x5410u),    // h=1: (x2, x6)
+                                   prmt(xv[j].y, xv[j].w, 0x7632u));   //      (x3, x7)
+        *reinterpret_cast<uint4 *>(dst + j * 512) = f;
+      }
+    }
+  }
   __syncthreads();
 
-  // Each element of the 16 x (8*NG) tile: fixed-order sum over the warps.
-  for (int e = threadIdx.x; e < NG * 128; e += kThreads) {
-    const int G = e >> 7, l = (e >> 2) & 31, q = e & 3;
-    const int row = (l >> 2) + ((q & 2) ? 8 : 0);
-    const int n = 2 * (l & 3) + (q & 1);
-    const int64_t m = 8 * G + n;
-    const int64_t i = static_cast<int64_t>(blockIdx.x) * 16 + row;
-    if (m >= p.M || i >= p.N) continue;
-    float s0 = 0.0f, s1 = 0.0f;
+  const int grp = warp / kGroupWarps, gw = warp % kGroupWarps;
+  const int g = lane >> 2, c = lane & 3;
+  const uint32_t sb0 = R * p.ng0 * 2, sb1 = DUAL ? R * p.ng1 * 2 : 0;
+  const uint32_t xbase = smem_u32(smem + p.x_off) + lane * 16;
+  for (int ig = 0;; ++ig) {
+    const int i = grp + ig * kGroups;
+    if (i >= my_units) break;
+    const int slot = grp * spg + ig % spg, round = ig / spg;
+    if (!warp_wait_lazy(&full[slot], round & 1, abort_flag, p.timeout_ns, err, 2000)) break;
+    const uint32_t base = smem_u32(smem + slot * p.slot_bytes);
+    const int ga = g, gb = DUAL ? g : g + 8;   // unit rows fed to A rows g and g+8
+    const uint32_t rowa = base + ga * p.pitch0 + c * (kChunk * BITS0 / 8);
+    const uint32_t rowb = (DUAL ? base + R * p.pitch0 + gb * p.pitch1 : base + gb * p.pitch0) + c * (kChunk * BB / 8);
+    const uint32_t sbase = base + p.sb_off;
+    const uint32_t s_a = sbase + ga * p.ng0 * 2, b_a = s_a + sb0;
+    const uint32_t s_b = DUAL ? sbase + 2 * sb0 + gb * p.ng1 * 2 : sbase + gb * p.ng0 * 2;
+    const uint32_t b_b = s_b + (DUAL ? sb1 : sb0);
+    float sum[NG][4];
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      s0 += red[w][0][G][l][q];
-      if constexpr (DUAL) s1 += red[w][NMAT - 1][G][l][q];
+    for (int G = 0; G < NG; ++G)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sum[G][q] = 0.0f;
+
+#pragma unroll 1
+    for (uint32_t kb = gw; kb < nkb; kb += kGroupWarps) {
+      // kb is warp-uniform; past K (only in the last block) the codes are
+      // replaced by zeros, and every lane runs the MMAs
+      const uint32_t k = kb * kBlockK + c * kChunk;
+      const bool kval = k < K;
+      Chunk<BITS0> ca;
+      Chunk<BB> cb;
+      uint32_t sa = 0, ba = 0, sb = 0, bb = 0;
+      if (kval) {
+        ca.load(rowa + kb * (kBlockK * BITS0 / 8));
+        cb.load(rowb + kb * (kBlockK * BB / 8));
+        const uint32_t ia = p.gd0(k) * 2, ib = (DUAL ? p.gd1 : p.gd0)(k) * 2;
+        sa = lds_u16(s_a + ia);
+        ba = lds_u16(b_a + ia);
+        sb = lds_u16(s_b + ib);
+        bb = lds_u16(b_b + ib);
+      } else {
+#pragma unroll
+        for (int q = 0; q < Chunk<BITS0>::kWords; ++q) ca.w[q] = 0;
+#pragma unroll
+        for (int q = 0; q < Chunk<BB>::kWords; ++q) cb.w[q] = 0;
+      }
+      __syncwarp();
+      const uint32_t sa2 = splat_bf16(static_cast<uint16_t>(sa)), ba2 = splat_bf16(static_cast<uint16_t>(ba));
+      const uint32_t sb2 = splat_bf16(static_cast<uint16_t>(sb)), bb2 = splat_bf16(static_cast<uint16_t>(bb));
+      float acc[NG][4];
+#pragma unroll
+      for (int G = 0; G < NG; ++G)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[G][q] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t pa[4], pb[4];
+        ca.dequant(j, sa2, ba2, pa);
+        cb.dequant(j, sb2, bb2, pb);
+#pragma unroll
+        for (int G = 0; G < NG; ++G) {
+          const uint4 xf = lds128(xbase + ((kb * NG + G) * 4 + j) * 512);
+          // A rows g (operand a) and g+8 (operand b); k_local 2c,2c+1 <- pair 2h,
+          // k_local 2c+8,2c+9 <- pair 2h+1
+          const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
+          const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
+          mma_bf16_16816(acc[G], a0, xf.x, xf.y);
+          mma_bf16_16816(acc[G], a1, xf.z, xf.w);
+        }
+      }
+#pragma unroll
+      for (int G = 0; G < NG; ++G)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sum[G][q] += acc[G][q];
     }
-    const float v = DUAL ? swiglu_epilogue(p.variant, s0, s1) : s0;
-    p.out[m * p.N + i] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+
+    // Done with the slot: the last of all warps of the group to get here
+    // refills it with the unit `slots` further on.  Every read of the slot is
+    // ordered before that warp's counter increment; its copies after it, behind
+    // a proxy fence (generic reads before async-proxy writes).
+    __syncwarp();
+    unsigned int prev = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      prev = atomicAdd(&done_cnt[slot], 1u);
+      __threadfence_block();
+    }
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev == kGroupWarps - 1) {
+      if (lane == 0) done_cnt[slot] = 0;
+      fence_proxy_async_smem();
+      const int i_next = i + spg * kGroups;   // this group's next unit for the slot
+      if (i_next < my_units)
+        issue_unit<BITS0, BB, DUAL>(p, smem + slot * p.slot_bytes, &full[slot], &issued_cnt[slot],
+                                    unit_of(i_next), lane);
+    }
+
+    // partial sums of the group -> one warp reduces them in a fixed order
+    const int buf = ig & 1;
+    const uint32_t use = static_cast<uint32_t>(ig >> 1);
+    uint64_t *rf = &red_full[grp * 2 + buf], *rfree = &red_free[grp * 2 + buf];
+    if (use > 0 && !warp_wait_lazy(rfree, (use - 1) & 1, abort_flag, p.timeout_ns, err, 2000)) break;
+    float *rb = red + ((grp * 2 + buf) * kGroupWarps) * NG * 128;
+#pragma unroll
+    for (int G = 0; G < NG; ++G)
+      *reinterpret_cast<float4 *>(rb + ((gw * NG + G) * 32 + lane) * 4) =
+          make_float4(sum[G][0], sum[G][1], sum[G][2], sum[G][3]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(rf);
+    if (gw == 0) {
+      if (!warp_wait_lazy(rf, use & 1, abort_flag, p.timeout_ns, err, 2000)) break;
+      const int64_t r0 = static_cast<int64_t>(unit_of(i)) * R;
+      for (int e = lane; e < R * NG * 8; e += 32) {
+        const int G = e / (R * 8), rem = e % (R * 8);
+        const int row = rem / 8, n = rem % 8;
+        const int m = 8 * G + n;
+        const int64_t i_out = r0 + row;
+        if (m >= p.M || i_out >= p.N) continue;
+        // accumulator element of (A row a, x col n): lane 4*(a % 8) + n/2,
+        // register (n & 1) + 2*(a >= 8).  Gate (or the single operand) is A
+        // row `row`; in the fused form up is A row row+8.
+        const int l = 4 * (row & 7) + (n >> 1);
+        const int qa = (n & 1) + ((row >= 8) ? 2 : 0);
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kGroupWarps; ++w) {
+          const float *rw = rb + ((w * NG + G) * 32 + l) * 4;
+          s0 += rw[qa];
+          if (DUAL) s1 += rw[(n & 1) + 2];
+        }
+        const float v = DUAL ? swiglu_epilogue(p.variant, s0, s1) : s0;
+        p.out[static_cast<int64_t>(m) * p.N + i_out] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(rfree);
+    }
+  }
+
+  // After an abort, let every copy this CTA issued land before it exits.
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) {
+    for (int s = 0; s < p.slots; ++s)
+      if (issued_cnt[s] > 0) mbar_wait_drain(&full[s], (issued_cnt[s] - 1) & 1, 100000000ull);
   }
 }
 
-template <int BITS0, int BITS1, bool DUAL>
-cudaError_t launch_ng(const GemvParams &p, cudaStream_t stream) {
-  const dim3 grid(static_cast<unsigned>((p.N + 15) / 16));
-  if (p.M <= 8) {
-    gemv_kernel<BITS0, BITS1, DUAL, 1><<<grid, kThreads, 0, stream>>>(p);
-  } else if (p.M <= 16) {
-    gemv_kernel<BITS0, BITS1, DUAL, 2><<<grid, kThreads, 0, stream>>>(p);
-  } else {
-    gemv_kernel<BITS0, BITS1, DUAL, 4><<<grid, kThreads, 0, stream>>>(p);
+struct Layout {
+  int slot_bytes, sb_off, x_off, red_off, bar_off, total, slots;
+};
+
+// Shared-memory layout for the given shape; slots == 0 when it does not fit.
+Layout plan(int64_t K, int64_t N, int M, int gs0, int gs1, int bits0, int bits1, bool dual, int num_sms) {
+  const int64_t R = dual ? 8 : 16;
+  const int NG = M <= 8 ? 1 : M <= 16 ? 2 : 4;
+  const int64_t pitch0 = K * bits0 / 8, pitch1 = dual ? K * bits1 / 8 : 0;
+  const int64_t ng = K / gs0 + (dual ? K / gs1 : 0);
+  Layout l{};
+  l.sb_off = static_cast<int>(R * (pitch0 + pitch1));
+  l.slot_bytes = static_cast<int>((l.sb_off + R * 4 * ng + 127) / 128 * 128);
+  const int64_t nkb = (K + kBlockK - 1) / kBlockK;
+  const int64_t x_bytes = nkb * NG * kXBlockBytes;
+  const int64_t red_bytes = static_cast<int64_t>(kGroups) * 2 * kGroupWarps * NG * 128 * 4;
+  const int64_t bar_bytes = (kMaxSlots + 4 * kGroups) * 8 + 2 * kMaxSlots * 4 + 16;
+  const int64_t fixed = x_bytes + red_bytes + bar_bytes;
+  const int64_t units = (N + R - 1) / R;
+  const int64_t grid = units < num_sms ? units : num_sms;
+  const int64_t per_cta = (units + grid - 1) / grid;
+  // slots per group: what fits, at most what one group can use
+  int64_t spg = (kSmemBudget - fixed) / l.slot_bytes / kGroups;
+  const int64_t per_group = (per_cta + kGroups - 1) / kGroups;
+  if (spg > kMaxSlots / kGroups) spg = kMaxSlots / kGroups;
+  if (spg > per_group) spg = per_group;
+  if (spg < 1) return Layout{};
+  const int64_t slots = spg * kGroups;
+  l.slots = static_cast<int>(slots);
+  l.x_off = static_cast<int>(slots * l.slot_bytes);
+  l.red_off = static_cast<int>(l.x_off + x_bytes);
+  l.bar_off = static_cast<int>(l.red_off + red_bytes);
+  l.total = static_cast<int>(l.bar_off + bar_bytes);
+  return l;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <int BITS0, int BITS1, bool DUAL, int NG>
+cudaError_t launch_cfg(GemvParams p, const Layout &l, cudaStream_t stream, int num_sms) {
+  constexpr int R = DUAL ? 8 : 16;
+  p.pitch0 = p.K * BITS0 / 8;
+  p.pitch1 = DUAL ? p.K * BITS1 / 8 : 0;
+  p.units = (p.N + R - 1) / R;
+  p.slots = l.slots;
+  p.slot_bytes = l.slot_bytes;
+  p.sb_off = l.sb_off;
+  p.x_off = l.x_off;
+  p.red_off = l.red_off;
+  p.bar_off = l.bar_off;
+  const int grid = p.units < num_sms ? p.units : num_sms;
+  static std::atomic<uint64_t> attr_done{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(attr_done.load() & (uint64_t(1) << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<BITS0, BITS1, DUAL, NG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(uint64_t(1) << dev);
   }
+  gemv_kernel<BITS0, BITS1, DUAL, NG><<<grid, kThreads, l.total, stream>>>(p);
   return cudaGetLastError();
 }
 
+template <int BITS0, int BITS1, bool DUAL>
+cudaError_t launch_ng(const GemvParams &p, const Layout &l, cudaStream_t stream, int num_sms) {
+  if (p.M <= 8) return launch_cfg<BITS0, BITS1, DUAL, 1>(p, l, stream, num_sms);
+  if (p.M <= 16) return launch_cfg<BITS0, BITS1, DUAL, 2>(p, l, stream, num_sms);
+  return launch_cfg<BITS0, BITS1, DUAL, 4>(p, l, stream, num_sms);
+}
+
 template <int BITS0>
-cudaError_t launch_dual_bits1(const GemvParams &p, int bits1, cudaStream_t stream) {
+cudaError_t launch_dual_bits1(const GemvParams &p, const Layout &l, int bits1, cudaStream_t stream, int num_sms) {
   switch (bits1) {
-    case 2: return launch_ng<BITS0, 2, true>(p, stream);
-    case 4: return launch_ng<BITS0, 4, true>(p, stream);
-    case 8: return launch_ng<BITS0, 8, true>(p, stream);
+    case 2: return launch_ng<BITS0, 2, true>(p, l, stream, num_sms);
+    case 4: return launch_ng<BITS0, 4, true>(p, l, stream, num_sms);
+    case 8: return launch_ng<BITS0, 8, true>(p, l, stream, num_sms);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
+bool gemv_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const QuantOperand *op1, int num_sms) {
+  const bool dual = op1 != nullptr;
+  const QuantOperand &o1 = dual ? *op1 : op0;
+  // scale/bias rows of a unit are staged by 16-byte bulk copies
+  if ((K / op0.gs) % 8 != 0 || (dual && (K / o1.gs) % 8 != 0)) return false;
+  if (!aligned16(op0.s) || !aligned16(op0.b) || (dual && (!aligned16(o1.s) || !aligned16(o1.b)))) return false;
+  if (M < 1 || M > kGemvMaxM || num_sms < 1) return false;
+  return plan(K, N, static_cast<int>(M), op0.gs, o1.gs, op0.bits, o1.bits, dual, num_sms).slots > 0;
+}
+
 cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                        const QuantOperand *op1, int variant, void *out, cudaStream_t stream) {
-  if (M < 1 || M > kGemvMaxM) return cudaErrorInvalidValue;
+                        const QuantOperand *op1, int variant, void *out, cudaStream_t stream,
+                        uint64_t timeout_ns, int num_sms) {
+  if (!gemv_fits(M, K, N, op0, op1, num_sms)) return cudaErrorInvalidValue;
+  const QuantOperand &o1 = op1 ? *op1 : op0;
+  const Layout l = plan(K, N, static_cast<int>(M), op0.gs, o1.gs, op0.bits, o1.bits, op1 != nullptr, num_sms);
   GemvParams p{};
   p.x = static_cast<const uint16_t *>(x);
-  p.M = M;
-  p.K = K;
-  p.N = N;
-  p.op[0] = op0;
-  p.op[1] = op1 ? *op1 : op0;
+  p.M = static_cast<int>(M);
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.w0 = op0.w;
+  p.s0 = op0.s;
+  p.b0 = op0.b;
+  p.gd0 = GroupDiv::make(op0.gs);
+  p.w1 = o1.w;
+  p.s1 = o1.s;
+  p.b1 = o1.b;
+  p.gd1 = GroupDiv::make(o1.gs);
+  p.ng0 = static_cast<uint32_t>(K / op0.gs);
+  p.ng1 = static_cast<uint32_t>(K / o1.gs);
   p.variant = variant;
   p.out = static_cast<uint16_t *>(out);
+  p.timeout_ns = timeout_ns;
   if (op1) {
     switch (op0.bits) {
-      case 2: return launch_dual_bits1<2>(p, op1->bits, stream);
-      case 4: return launch_dual_bits1<4>(p, op1->bits, stream);
-      case 8: return launch_dual_bits1<8>(p, op1->bits, stream);
+      case 2: return launch_dual_bits1<2>(p, l, op1->bits, stream, num_sms);
+      case 4: return launch_dual_bits1<4>(p, l, op1->bits, stream, num_sms);
+      case 8: return launch_dual_bits1<8>(p, l, op1->bits, stream, num_sms);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (op0.bits) {
-    case 2: return launch_ng<2, 2, false>(p, stream);
-    case 4: return launch_ng<4, 4, false>(p, stream);
-    case 8: return launch_ng<8, 8, false>(p, stream);
+    case 2: return launch_ng<2, 2, false>(p, l, stream, num_sms);
+    case 4: return launch_ng<4, 4, false>(p, l, stream, num_sms);
+    case 8: return launch_ng<8, 8, false>(p, l, stream, num_sms);
     default: return cudaErrorInvalidValue;
   }
+}
+
+// Read and clear the device error word of this translation unit's kernels.
+cudaError_t gemv_take_errors(unsigned int *out) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof v);
+  if (e != cudaSuccess) return e;
+  if (v) {
+    e = cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof zero);
+    if (e != cudaSuccess) return e;
+  }
+  *out = v;
+  return cudaSuccess;
 }
 
 }  // namespace qsw

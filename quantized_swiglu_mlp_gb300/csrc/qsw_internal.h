@@ -20,7 +20,12 @@ struct QuantOperand {
 // Small-M kernel: rows of x up to 32.  `dual` selects the fused SwiGLU
 // (gate + up, epilogue `variant`) or a single quantised linear (y = bf16(x.W^T)).
 cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                        const QuantOperand *op1, int variant, void *out, cudaStream_t stream);
+                        const QuantOperand *op1, int variant, void *out, cudaStream_t stream,
+                        uint64_t timeout_ns, int num_sms);
+
+// Whether the small-M kernel can stage rows of length K (else the tensor-core
+// kernel serves every M).
+bool gemv_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const QuantOperand *op1, int num_sms);
 
 // Tensor-core kernel (tcgen05 + TMA), any M.
 cudaError_t launch_prefill(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,

@@ -72,6 +72,7 @@ struct PrefillParams {
   const uint16_t *s0, *b0;
   const uint16_t *s1, *b1;
   int gs0, gs1;
+  GroupDiv gd0, gd1;
   int variant;
   uint16_t *out;
   int m_tiles, num_tiles, k_steps;
@@ -129,9 +130,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *full = bars;             // TMA bytes landed (x + packed codes)
   uint64_t *deq = bars + S;          // bf16 weights written by the dequantisers
   uint64_t *empty = bars + 2 * S;    // MMAs of the stage completed
-  uint64_t *acc_full = bars + 3 * S; // [2] accumulator ready for the epilogue
-  uint64_t *acc_empty = acc_full + 2;// [2] accumulator drained by the epilogue
-  uint64_t *mma_done = acc_empty + 2;
+  // Accumulation: each tile's K range is split in two halves that accumulate
+  // in the two TMEM buffers X (first half) and Y (second half); the epilogue
+  // adds Y into X with f32 adds.  Shorter tensor-core accumulation chains keep
+  // the rounding of the stored projections close to a correctly rounded sum.
+  // X of tile t is buffer t%2, Y the other one, so roles swap every tile.
+  uint64_t *acc_full = bars + 3 * S; // both chains of the tile are complete
+  uint64_t *y_free = acc_full + 1;   // Y has been added into X (Y reusable)
+  uint64_t *x_free = acc_full + 2;   // X has been read out (X reusable)
+  uint64_t *mma_done = acc_full + 3;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -150,10 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&deq[s], kDeqWarps);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], kEpiWarps);
-    }
+    mbar_init(acc_full, 1);
+    mbar_init(y_free, kEpiWarps);
+    mbar_init(x_free, kEpiWarps);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -213,17 +219,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
+      const int k_half = (p.k_steps + 1) / 2;   // first chain: K steps [0, k_half)
       int lt = 0;
       for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++lt) {
-        const int buf = lt & 1;
-        const uint32_t acc_parity = (lt >> 1) & 1;
-        if (!mbar_wait(&acc_empty[buf], acc_parity ^ 1u, abort_flag, p.timeout_ns, err)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+        const uint32_t x_tmem = tmem_base + static_cast<uint32_t>((lt & 1) * BN);
+        const uint32_t y_tmem = tmem_base + static_cast<uint32_t>(((lt + 1) & 1) * BN);
+        const uint32_t prev_parity = static_cast<uint32_t>((lt - 1) & 1);
         for (int kb = 0; kb < p.k_steps; ++kb) {
+          // X of this tile was Y of the previous one, and Y was its X
+          if (lt > 0 && (kb == 0 || kb == k_half)) {
+            if (!mbar_wait(kb == 0 ? y_free : x_free, prev_parity, abort_flag, p.timeout_ns, err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          const uint32_t d_tmem = kb < k_half ? x_tmem : y_tmem;
+          const bool chain_start = (kb == 0 || kb == k_half);
           if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns, err) ||
               !mbar_wait(&deq[stage], phase, abort_flag, p.timeout_ns, err)) {
             ok = false;
@@ -235,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // +32 bytes of K per step inside the 128-byte swizzle atom
-            umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+            umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (chain_start && kk == 0) ? 0u : 1u);
           }
           umma_commit(&empty[stage]);
           if (++stage == S) {
@@ -243,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             phase ^= 1u;
           }
         }
-        if (ok) umma_commit(&acc_full[buf]);
+        if (ok) umma_commit(acc_full);
       }
       if (!ok) {
         umma_commit(mma_done);
@@ -262,29 +274,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
       const int64_t n0 = static_cast<int64_t>(t / p.m_tiles) * C::kOutCols;
-      // global row (clamped into range) of each of this thread's 8 B rows
-      int64_t grow[8];
+      // offset of the scale row of each of this thread's 8 B rows (row clamped
+      // into range); 32-bit: rows * groups < 2^31 is checked on the host
+      uint32_t srow[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int n = r0 + 32 * j;
         const int64_t r = n0 + (DUAL ? (n & 127) : n);
-        grow[j] = r < p.N ? r : p.N - 1;
+        const uint32_t rc = static_cast<uint32_t>(r < p.N ? r : p.N - 1);
+        srow[j] = rc * static_cast<uint32_t>((!DUAL || j < 4) ? ng0 : ng1);
       }
       auto fetch_sb = [&](int kb, uint32_t (&sb)[8]) {
-        const int64_t k = static_cast<int64_t>(kb) * BK + 8 * c;
-        const int64_t kc = k < p.K ? k : p.K - 1;
+        const uint32_t k = static_cast<uint32_t>(kb) * BK + 8 * c;
+        const uint32_t kc = k < static_cast<uint32_t>(p.K) ? k : static_cast<uint32_t>(p.K) - 1;
+        const uint32_t grp0 = p.gd0(kc), grp1 = p.gd1(kc);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const bool first = !DUAL || j < 4;
-          sb[j] = first ? load_sb(p.s0, p.b0, grow[j] * ng0 + kc / p.gs0)
-                        : load_sb(p.s1, p.b1, grow[j] * ng1 + kc / p.gs1);
+          sb[j] = first ? load_sb(p.s0, p.b0, srow[j] + grp0) : load_sb(p.s1, p.b1, srow[j] + grp1);
         }
       };
-      uint32_t sb_cur[8], sb_next[8];
+      // scale/bias registers for steps kb, kb+1, kb+2: the global loads are
+      // issued two K steps before they are used, hiding their latency
+      uint32_t sb_cur[8], sb_next[8], sb_next2[8];
       fetch_sb(0, sb_cur);
+      if (1 < p.k_steps) fetch_sb(1, sb_next);
       for (int kb = 0; kb < p.k_steps; ++kb) {
-        if (kb + 1 < p.k_steps) fetch_sb(kb + 1, sb_next);
-        if (!warp_wait(&full[stage], phase, abort_flag, p.timeout_ns, err)) {
+        if (kb + 2 < p.k_steps) fetch_sb(kb + 2, sb_next2);
+        if (!warp_wait_lazy(&full[stage], phase, abort_flag, p.timeout_ns, err, 1000)) {
           ok = false;
           break;
         }
@@ -312,7 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&deq[stage]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) sb_cur[j] = sb_next[j];
+        for (int j = 0; j < 8; ++j) {
+          sb_cur[j] = sb_next[j];
+          sb_next[j] = sb_next2[j];
+        }
         if (++stage == S) {
           stage = 0;
           phase ^= 1u;
@@ -324,15 +344,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
     const bool vec_ok = (p.N % 8) == 0;
+    const bool two_chains = p.k_steps > 1;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     int lt = 0;
     for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
-      const int buf = lt & 1;
-      const uint32_t acc_parity = (lt >> 1) & 1;
-      if (!warp_wait(&acc_full[buf], acc_parity, abort_flag, p.timeout_ns, err)) break;
+      // the epilogue idles for a whole tile's main loop: wait without spinning
+      if (!warp_wait_lazy(acc_full, static_cast<uint32_t>(lt & 1), abort_flag, p.timeout_ns, err, 10000)) break;
       tc_fence_after();
+      const uint32_t tbase = lane_base + static_cast<uint32_t>((lt & 1) * BN);          // X
+      const uint32_t ybase = lane_base + static_cast<uint32_t>(((lt + 1) & 1) * BN);    // Y
+      if (two_chains) {
+        // X += Y over all columns, f32 adds rounded to nearest
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          uint32_t ra[16], rb[16];
+          __syncwarp();
+          tmem_ld16(tbase + c0, ra);
+          tmem_ld16(ybase + c0, rb);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ra[e] = __float_as_uint(__uint_as_float(ra[e]) + __uint_as_float(rb[e]));
+          tmem_st16(tbase + c0, ra);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(y_free);   // Y may take the next tile's first chain
       const int64_t m = static_cast<int64_t>(t % p.m_tiles) * BM + row;
       const int64_t n0 = static_cast<int64_t>(t / p.m_tiles) * C::kOutCols;
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(buf * BN);
       uint16_t *orow = p.out + m * p.N;
 #pragma unroll 1
       for (int c0 = 0; c0 < C::kOutCols; c0 += 16) {
@@ -368,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (lane == 0) mbar_arrive(x_free);   // X may take the next tile's second chain
     }
   }
 
@@ -441,6 +481,9 @@ cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   p.s1 = DUAL ? op1->s : op0.s;
   p.b1 = DUAL ? op1->b : op0.b;
   p.gs1 = DUAL ? op1->gs : op0.gs;
+  p.gd0 = GroupDiv::make(p.gs0);
+  p.gd1 = GroupDiv::make(p.gs1);
+  if (N * (K / (p.gs0 < p.gs1 ? p.gs0 : p.gs1)) >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   p.variant = variant;
   p.out = static_cast<uint16_t *>(out);
   p.m_tiles = static_cast<int>((M + BM - 1) / BM);

@@ -31,7 +31,12 @@ def bf16_ulp(v: np.ndarray) -> np.ndarray:
 
 
 def _summary(gpu, ref, bound):
-    err = np.abs(gpu - ref)
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    same = (gpu == ref) | (np.isnan(gpu) & np.isnan(ref))      # also equal infinities
+    with np.errstate(invalid="ignore"):
+        err = np.where(same, 0.0, np.abs(gpu - ref))
+    err = np.where(np.isnan(err), np.inf, err)
     bad = ~(err <= bound)
     n_bad = int(bad.sum())
     info = {"n": int(gpu.size), "n_bad": n_bad, "max_err": float(err.max()) if err.size else 0.0}
@@ -58,11 +63,43 @@ def exact_fraction(gpu_bits, oracle_bits) -> float:
     return float((a == b).mean()) if a.size else 1.0
 
 
+def check_match_with_projections(h_gpu, g_gpu, u_gpu, h_ref, g_ref, u_ref, epilogue):
+    """MATCH check that accounts for the projections' rounding.
+
+    The GPU accumulates in f32, in another order than the oracle's f64 sum, so
+    on a few elements the stored bf16 gate or up rounds to the neighbouring
+    value; both results are correct.  What is unique is checked:
+      * the stored projections (debug variants) equal the oracle's on >= 99.9 %
+        of elements and are within 1 ulp (+1e-3) elsewhere;
+      * where both projections equal the oracle's, hidden is within the MATCH
+        bound of the oracle's hidden;
+      * elsewhere hidden is within the MATCH bound of the oracle's MATCH
+        epilogue applied to the GPU's own projections (`epilogue(g, u)`)."""
+    h_gpu, g_gpu, u_gpu = (np.asarray(a, dtype=np.uint16) for a in (h_gpu, g_gpu, u_gpu))
+    h_ref, g_ref, u_ref = (np.asarray(a, dtype=np.uint16) for a in (h_ref, g_ref, u_ref))
+    ok_g, info_g = check_projection(g_gpu, g_ref)
+    ok_u, info_u = check_projection(u_gpu, u_ref)
+    same = (g_gpu == g_ref) & (u_gpu == u_ref)
+    ok_same, info_same = check_match(h_gpu[same], h_ref[same])
+    alt = epilogue(g_gpu[~same], u_gpu[~same]) if (~same).any() else np.zeros(0, np.uint16)
+    ok_alt, info_alt = check_match(h_gpu[~same], alt)
+    info = {"gate": info_g, "up": info_u, "agreeing": info_same, "flipped": info_alt,
+            "flipped_fraction": float((~same).mean()) if same.size else 0.0}
+    return ok_g and ok_u and ok_same and ok_alt, info
+
+
+MIN_RATE_SAMPLE = 10_000
+
+
 def check_projection(gpu_bits, oracle_bits):
-    """Stored gate/up projection: >= 99.9 % bit-identical, the rest within
-    1 ulp + 1e-3 (the absolute term covers sums that cancel to near zero)."""
+    """Stored gate/up projection: every element within 1 ulp + 1e-3 (the
+    absolute term covers sums that cancel to near zero), and bit-identical on
+    >= 99.9 % of elements.  The 99.9 % figure is a rate, so it is enforced on
+    samples of at least MIN_RATE_SAMPLE elements (a handful of elements cannot
+    resolve a 0.1 % rate); smaller samples report it."""
     frac = exact_fraction(gpu_bits, oracle_bits)
     gpu, ref = bf16_to_f64(gpu_bits), bf16_to_f64(oracle_bits)
     ok_close, info = _summary(gpu, ref, bf16_ulp(ref) + ABS_TOL)
     info["exact_fraction"] = frac
-    return (frac >= EXACT_FRACTION and ok_close), info
+    rate_ok = frac >= EXACT_FRACTION or np.size(gpu_bits) < MIN_RATE_SAMPLE
+    return (rate_ok and ok_close), info
