@@ -201,6 +201,32 @@ def time_calls(fn, steps: int, warmup: int, stream):
     return start.elapsed_time(end)
 
 
+def time_graph(fn, steps: int, warmup: int, stream):
+    """Warm up, capture `steps` calls in one CUDA graph, then time a replay with
+    CUDA events on `stream` (synchronised, with a barrier across ranks, on both
+    sides).  The graph removes host launch gaps, so the time is the GPU's."""
+    import torch
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(steps):
+            fn(i)
+    with torch.cuda.stream(stream):
+        graph.replay()   # untimed
+    torch.cuda.synchronize()
+    barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end)
+
+
 def bench_decode(args, dev, stream, peaks, peak_src):
     import torch
     from quantized_swiglu_mlp_gb300 import inputs, ops
@@ -228,7 +254,7 @@ def bench_decode(args, dev, stream, peaks, peak_src):
             step(i)
         torch.cuda.synchronize()
     ops.qsw_reset_counters()
-    ms = time_calls(step, args.steps, args.warmup, stream)
+    ms = time_graph(step, args.steps, args.warmup, stream)
     counters = ops.qsw_get_counters()
     clocks = sampler.stop()
     ops.qsw_check_device_errors(stream)
@@ -287,7 +313,7 @@ def _bench_large(args, dev, stream, peaks, peak_src):
     flops = 4.0 * case.M * case.H * case.I
     for vname in ("match", "f32"):
         v = ops.VARIANTS[vname]
-        ms = time_calls(lambda i: ops.qswiglu_forward(*a, variant=v, out=out, stream=stream),
+        ms = time_graph(lambda i: ops.qswiglu_forward(*a, variant=v, out=out, stream=stream),
                         args.prefill_steps, 3, stream)
         per = ms / 1e3 / args.prefill_steps
         tf = flops / per / 1e12
@@ -314,7 +340,7 @@ def _bench_mid(args, dev, stream):
     g = torch.empty_like(out)
     u = torch.empty_like(out)
     flops = 4.0 * case.M * case.H * case.I
-    ms_f = time_calls(lambda i: ops.qswiglu_forward(*a, variant=ops.MATCH, out=out, stream=stream),
+    ms_f = time_graph(lambda i: ops.qswiglu_forward(*a, variant=ops.MATCH, out=out, stream=stream),
                       args.prefill_steps, 3, stream)
     x, wg, sg, bg, gsg, btg, wu, su, bu, gsu, btu = a
 
@@ -323,7 +349,7 @@ def _bench_mid(args, dev, stream):
         ops.affine_qmm(x, wu, su, bu, gsu, btu, y=u, stream=stream)
         ops.qsw_silu_mul(g, u, ops.MATCH, out=out, stream=stream)
 
-    ms_u = time_calls(unfused, args.prefill_steps, 3, stream)
+    ms_u = time_graph(unfused, args.prefill_steps, 3, stream)
     ops.qsw_check_device_errors(stream)
     pf, pu = ms_f / 1e3 / args.prefill_steps, ms_u / 1e3 / args.prefill_steps
     res["mid_fused"] = {"tflops": round(flops / pf / 1e12, 1), "us_per_call": round(pf * 1e6, 1)}
