@@ -45,6 +45,7 @@ constexpr int kChunk = 32;                      // codes per lane per block
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kMaxSlots = 16;
 constexpr int kXBlockBytes = 4 * 32 * 16;       // B fragments of one block, one x row group (2 KB)
+constexpr int kXPre = 4;                        // x pieces per thread requested ahead of the weights
 
 __device__ unsigned int g_gemv_error;
 
@@ -168,7 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);               // [kMaxSlots]
   uint64_t *red_full = full + kMaxSlots;                                          // [kGroups][2]
   uint64_t *red_free = red_full + 2 * kGroups;                                    // [kGroups][2]
-  unsigned int *done_cnt = reinterpret_cast<unsigned int *>(red_free + 2 * kGroups);   // [kMaxSlots]
+  uint64_t *x_ready = red_free + 2 * kGroups;                                     // x staged
+  unsigned int *done_cnt = reinterpret_cast<unsigned int *>(x_ready + 1);         // [kMaxSlots]
   unsigned int *issued_cnt = done_cnt + kMaxSlots;                                     // [kMaxSlots]
   volatile int *abort_flag = reinterpret_cast<volatile int *>(issued_cnt + kMaxSlots);
   float *red = reinterpret_cast<float *>(smem + p.red_off);   // [kGroups][2][kGroupWarps][NG][32][4]
@@ -192,60 +194,85 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
       mbar_init(&red_full[b], kGroupWarps);
       mbar_init(&red_free[b], 1);
     }
+    mbar_init(x_ready, kWarps - 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // x -> shared memory in B-fragment order, once per CTA: for block kb, x row
+  // group G, fragment word q (0..15) of lane L = 4n + c sits at
+  // ((kb*NG + G)*4 + q/4)*512 + L*16 + (q%4)*4 bytes.  Every staging thread
+  // requests its first pieces of x BEFORE the weight copies are issued: behind
+  // the weight stream of all SMs, x would only arrive microseconds later.  The
+  // last warp issues the copies and stages no x: issuing stalls while the copy
+  // engine is saturated, and no other warp should wait for that.
+  const int x_total = static_cast<int>(nkb) * NG * 32;   // (kb, G, lane) triples
+  auto load_x = [&](int e, uint4 (&xv)[4]) {
+    const int L = e & 31, G = (e >> 5) % NG, kb = (e >> 5) / NG;
+    const int m = 8 * G + (L >> 2);
+    const uint32_t k = static_cast<uint32_t>(kb) * kBlockK + (L & 3) * kChunk;
+    if (k < K && m < p.M) {
+      const uint4 *xp = reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(m) * p.K + k);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xv[q] = __ldg(xp + q);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xv[q] = make_uint4(0, 0, 0, 0);
+    }
+  };
+  auto store_x = [&](int e, const uint4 (&xv)[4]) {
+    const int L = e & 31, G = (e >> 5) % NG, kb = (e >> 5) / NG;
+    uint8_t *dst = smem + p.x_off + static_cast<size_t>(kb * NG + G) * kXBlockBytes + L * 16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // x values 8j..8j+7: (x0,x1) (x2,x3) (x4,x5) (x6,x7)
+      const uint4 f = make_uint4(prmt(xv[j].x, xv[j].z, 0x5410u),    // h=0: (x0, x4)
+                                 prmt(xv[j].x, xv[j].z, 0x7632u),    //      (x1, x5)
+                                 prmt(xv[j].y, xv[j].w, 0x5410u),    // h=1: (x2, x6)
+                                 prmt(xv[j].y, xv[j].w, 0x7632u));   //      (x3, x7)
+      *reinterpret_cast<uint4 *>(dst + j * 512) = f;
+    }
+  };
+  constexpr int kStageThreads = kThreads - 32;
+  const bool stager = static_cast<int>(threadIdx.x) < kStageThreads;
+  uint4 x_pre[kXPre][4];
+#pragma unroll
+  for (int r = 0; r < kXPre; ++r)
+    if (stager && static_cast<int>(threadIdx.x) + r * kStageThreads < x_total)
+      load_x(threadIdx.x + r * kStageThreads, x_pre[r]);
   __syncthreads();
   // Each group owns `spg` slots and uses them in turn, so a slot only ever
   // holds the units of one group, in order (a waiter is never more than one
-  // fill ahead of its slot).  Warp 0 puts the first units of every slot in
-  // flight; later fills are issued by the group's warp that finishes last.
+  // fill ahead of its slot).  The last warp puts the first units of every slot in
+  // flight, every group's first unit first; later fills are issued by the
+  // group's warp that finishes last.
   const int spg = p.slots / kGroups;
-  if (warp == 0) {
-    for (int q = 0; q < kGroups; ++q)
-      for (int s = 0; s < spg; ++s) {
+  if (!stager) {
+    for (int s = 0; s < spg; ++s)
+      for (int q = 0; q < kGroups; ++q) {
         const int i = q + s * kGroups;
         if (i < my_units)
           issue_unit<BITS0, BB, DUAL>(p, smem + (q * spg + s) * p.slot_bytes, &full[q * spg + s],
                                       &issued_cnt[q * spg + s], unit_of(i), lane);
       }
-  }
-  // x -> shared memory in B-fragment order, once per CTA: for block kb, x row
-  // group G, fragment word q (0..15) of lane L = 4n + c sits at
-  // ((kb*NG + G)*4 + q/4)*512 + L*16 + (q%4)*4 bytes
-  {
-    const int total = static_cast<int>(nkb) * NG * 32;   // (kb, G, lane) triples
-    for (int e = threadIdx.x; e < total; e += kThreads) {
-      const int L = e & 31, G = (e >> 5) % NG, kb = (e >> 5) / NG;
-      const int n = L >> 2, c = L & 3, m = 8 * G + n;
-      const uint32_t k = static_cast<uint32_t>(kb) * kBlockK + c * kChunk;
+  } else {
+#pragma unroll
+    for (int r = 0; r < kXPre; ++r)
+      if (static_cast<int>(threadIdx.x) + r * kStageThreads < x_total)
+        store_x(threadIdx.x + r * kStageThreads, x_pre[r]);
+    for (int e = threadIdx.x + kXPre * kStageThreads; e < x_total; e += kStageThreads) {
       uint4 xv[4];
-      if (k < K && m < p.M) {
-        const uint4 *xp = reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(m) * p.K + k);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) xv[q] = __ldg(xp + q);
-      } else {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) xv[q] = make_uint4(0, 0, 0, 0);
-      }
-      uint8_t *dst = smem + p.x_off + static_cast<size_t>(kb * NG + G) * kXBlockBytes + L * 16;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {   // x values 8j..8j+7: (x0,x1) (x2,x3) (x4,x5) (x6,x7)
-        const uint4 f = make_uint4(prmt(xv[j].x, xv[j].z, 0x5410u),    // h=0: (x0, x4)
-                                   prmt(xv[j].x, xv[j].z, 0x7632u),    //      (x1, x5)
-                                   prmt(xv[j].y, xv[j].w, 0x5410u),    // h=1: (x2, x6)
-                                   prmt(xv[j].y, xv[j].w, 0x7632u));   //      (x3, x7)
-        *reinterpret_cast<uint4 *>(dst + j * 512) = f;
-      }
+      load_x(e, xv);
+      store_x(e, xv);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(x_ready);
   }
-  __syncthreads();
+  const bool x_ok = warp_wait_lazy(x_ready, 0, abort_flag, p.timeout_ns, err, 2000);
 
   const int grp = warp / kGroupWarps, gw = warp % kGroupWarps;
   const int g = lane >> 2, c = lane & 3;
   const uint32_t sb0 = R * p.ng0 * 2, sb1 = DUAL ? R * p.ng1 * 2 : 0;
   const uint32_t xbase = smem_u32(smem + p.x_off) + lane * 16;
-  for (int ig = 0;; ++ig) {
+  for (int ig = 0; x_ok; ++ig) {
     const int i = grp + ig * kGroups;
     if (i >= my_units) break;
     const int slot = grp * spg + ig % spg, round = ig / spg;
@@ -403,7 +430,7 @@ Layout plan(int64_t K, int64_t N, int M, int gs0, int gs1, int bits0, int bits1,
   const int64_t nkb = (K + kBlockK - 1) / kBlockK;
   const int64_t x_bytes = nkb * NG * kXBlockBytes;
   const int64_t red_bytes = static_cast<int64_t>(kGroups) * 2 * kGroupWarps * NG * 128 * 4;
-  const int64_t bar_bytes = (kMaxSlots + 4 * kGroups) * 8 + 2 * kMaxSlots * 4 + 16;
+  const int64_t bar_bytes = (kMaxSlots + 4 * kGroups + 1) * 8 + 2 * kMaxSlots * 4 + 16;
   const int64_t fixed = x_bytes + red_bytes + bar_bytes;
   const int64_t units = (N + R - 1) / R;
   const int64_t grid = units < num_sms ? units : num_sms;
