@@ -8,17 +8,23 @@
 // single-operand form follows src/model/steel-linear-kernel.ts (float
 // accumulator cast to bf16 at the store).
 //
-// GB300 design (sm_103a), one persistent CTA per SM, warp-specialised:
-//   warp 0      TMA producer: x tile [128 x 64] (128-byte swizzle) and the
-//               packed-code tiles of this stage, one mbarrier per stage;
+// GB300 design (sm_103a), one persistent CTA per SM, warp-specialised, three
+// shared-memory rings filled by TMA and one filled by the dequantisers:
+//   x ring      x tile [128 x 64] bf16, 128-byte swizzle     TMA    -> MMA
+//   codes ring  packed codes of the tile's 256 B rows          TMA    -> dequant
+//   scale ring  per operand: scales and biases of 8 groups     TMA    -> dequant
+//   B ring      dequantised bf16 B tile [256 x 64], swizzled   dequant -> MMA
+// Roles:
+//   warp 0      producer of the codes and scale rings;
 //   warp 1      TMEM owner and MMA issuer: per 64-wide K step, four
-//               tcgen05.mma kind::f16 M=128 N=256 K=16 into a TMEM accumulator
-//               (two accumulators of 256 columns, double-buffered);
-//   warps 2-9   dequantisers: packed codes (smem) + scale/bias (global) ->
-//               bf16 weights written straight into the 128-byte-swizzled
-//               K-major operand layout the tensor core reads;
-//   warps 10-13 epilogue: tcgen05.ld of the accumulator, the SwiGLU epilogue,
-//               128-bit stores of bf16 hidden.
+//               tcgen05.mma kind::f16 M=128 N=256 K=16 into a TMEM accumulator;
+//   warp 2      producer of the x ring (two producers, so that neither stream
+//               waits behind the other's ring);
+//   warps 3-18  dequantisers: each thread turns 32 codes of one B row into bf16
+//               per K step and writes them into the swizzled K-major layout the
+//               tensor core reads;
+//   warps 19-22 epilogue: tcgen05.ld of the accumulator, the SwiGLU epilogue,
+//               16-byte stores of bf16 hidden.
 // The B operand of one MMA stacks 128 gate rows over 128 up rows (N = 256),
 // so a single MMA stream computes both projections from one staged x tile.
 //
@@ -35,14 +41,18 @@ namespace qsw {
 namespace {
 
 constexpr int BM = 128;   // rows of x per tile = UMMA M
-constexpr int BK = 64;    // K per stage: one 128-byte swizzle atom of bf16
+constexpr int BK = 64;    // K per step: one 128-byte swizzle atom of bf16
 constexpr int BN = 256;   // UMMA N (B-tile rows)
-constexpr int kDeqWarps = 8;
+constexpr int kDeqWarps = 16;
 constexpr int kEpiWarps = 4;
-constexpr int kWarpTma = 0, kWarpMma = 1, kWarpDeq0 = 2, kWarpEpi0 = kWarpDeq0 + kDeqWarps;
-constexpr int kThreads = 32 * (kWarpEpi0 + kEpiWarps);   // 448
+constexpr int kWarpTma = 0, kWarpMma = 1, kWarpX = 2, kWarpDeq0 = 3, kWarpEpi0 = kWarpDeq0 + kDeqWarps;
+constexpr int kThreads = 32 * (kWarpEpi0 + kEpiWarps);   // 736
 constexpr uint32_t kTmemCols = 512;                       // two 256-column accumulators
 constexpr int kMaxSmem = 232448;                          // opt-in limit per block
+constexpr int kXBytes = BM * BK * 2;                      // 16 KB
+constexpr int kBBytes = BN * BK * 2;                      // 32 KB
+constexpr int kGroupsPerEntry = 8;                        // scale groups per ring entry (16 bytes)
+constexpr int kBarBytes = 512;
 
 __device__ unsigned int g_prefill_error;
 
@@ -51,123 +61,202 @@ struct Cfg {
   static constexpr int kRows0 = DUAL ? 128 : 256;   // B rows from operand 0
   static constexpr int kRows1 = DUAL ? 128 : 0;     // B rows from operand 1
   static constexpr int kOutCols = DUAL ? 128 : 256; // output columns per tile
-  static constexpr int kABytes = BM * BK * 2;
-  static constexpr int kBBytes = BN * BK * 2;
-  static constexpr int kP0Pitch = BK * BITS0 / 8;   // bytes per packed row per stage
-  static constexpr int kP1Pitch = BK * BITS1 / 8;
-  static constexpr int kP0Bytes = kRows0 * kP0Pitch;
-  static constexpr int kP1Bytes = kRows1 * kP1Pitch;
-  static constexpr int kStageBytes = kABytes + kBBytes + kP0Bytes + kP1Bytes;
-  static constexpr int kTxBytes = kABytes + kP0Bytes + kP1Bytes;
-  static constexpr int kBarBytes = 256;
-  static constexpr int kStages = (4 * kStageBytes + 1024 + kBarBytes <= kMaxSmem) ? 4 : 3;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + kBarBytes;
-  static_assert(kStageBytes % 1024 == 0, "stage must keep 1024-byte alignment");
+  static constexpr int kC0Pitch = BK * BITS0 / 8;   // packed bytes per row per K step
+  static constexpr int kC1Pitch = BK * BITS1 / 8;
+  static constexpr int kC0Bytes = kRows0 * kC0Pitch;
+  static constexpr int kCodesBytes = kC0Bytes + kRows1 * kC1Pitch;
+  // one scale-ring entry: [rows][8] scales then [rows][8] biases, per operand
+  static constexpr int kS0Bytes = kRows0 * 2 * kGroupsPerEntry;
+  static constexpr int kS1Bytes = kRows1 * 2 * kGroupsPerEntry;
+  static constexpr int kEntryBytes = 2 * kS0Bytes + 2 * kS1Bytes;
+  static constexpr int kSb = 3;   // B ring
+  static constexpr int kBudget = kMaxSmem - 1024 - kBarBytes;
+  // x ring: a fifth stage where it still leaves four codes stages
+  static constexpr int kSx = (kBudget - 5 * kXBytes - kSb * kBBytes - 2 * kEntryBytes) / kCodesBytes >= 4 ? 5 : 4;
+  static constexpr int kFixed = kSx * kXBytes + kSb * kBBytes + 2 * kEntryBytes;
+  static constexpr int kScFit = (kBudget - kFixed) / kCodesBytes;
+  static constexpr int kSc = kScFit > 4 ? 4 : kScFit;   // codes ring
+  static constexpr int kXOff = 0;
+  static constexpr int kBOff = kXOff + kSx * kXBytes;
+  static constexpr int kCOff = kBOff + kSb * kBBytes;
+  static constexpr int kSOff = kCOff + kSc * kCodesBytes;
+  static constexpr int kBarOff = kSOff + 2 * kEntryBytes;
+  static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
+  static_assert(kSc >= 2, "codes ring too small");
+  static_assert(kCodesBytes % 1024 == 0 && kC0Bytes % 128 == 0, "codes ring alignment");
+  static_assert(kEntryBytes % 128 == 0 && kS0Bytes % 128 == 0, "scale ring alignment");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
-  static_assert((3 * kStages + 5) * 8 + 8 <= kBarBytes, "barrier area");
 };
 
 struct PrefillParams {
   int64_t M, K, N;
-  const uint16_t *s0, *b0;
+  const uint16_t *s0, *b0;   // scales/biases (read directly only where they cannot be TMA-staged)
   const uint16_t *s1, *b1;
-  int gs0, gs1;
+  int ng0, ng1;              // groups per row
   GroupDiv gd0, gd1;
+  int sb_tma0, sb_tma1;      // scale ring filled by TMA (else by plain loads)
   int variant;
   uint16_t *out;
   int m_tiles, num_tiles, k_steps;
   uint64_t timeout_ns;
 };
 
-// Eight codes of one packed row (chunk c of a 64-code stage) -> 16 bytes of bf16.
-template <int BITS>
-__device__ __forceinline__ uint4 dequant_chunk(const uint8_t *prow, int c, uint32_t s2, uint32_t b2) {
-  uint32_t o[4];
-  if constexpr (BITS == 4) {
-    Dequant8<4>::natural(*reinterpret_cast<const uint32_t *>(prow + 4 * c), s2, b2, o);
-  } else if constexpr (BITS == 8) {
-    const uint2 v = *reinterpret_cast<const uint2 *>(prow + 8 * c);
-    Dequant8<8>::natural(v.x, v.y, s2, b2, o);
-  } else {
-    Dequant8<2>::natural(*reinterpret_cast<const uint16_t *>(prow + 2 * c), s2, b2, o);
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
-
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
 __device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
 
-// Wait executed by every lane of a warp; the outcome is made warp-uniform so
-// that the whole warp either proceeds (converged) or leaves together.
+// Wait executed by a whole warp: lane 0 polls, then every lane observes the
+// completed phase itself; the outcome is warp-uniform (false: give up).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns,
                                           unsigned int *err) {
-  const bool ok = mbar_wait(bar, parity, abort, timeout_ns, err);
-  return __all_sync(0xffffffffu, ok);
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, timeout_ns, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return false;
+  return __all_sync(0xffffffffu, mbar_try_wait(bar, parity));
 }
 
-// Scale and bias of one (row, group), packed as (bias << 16) | scale.
-__device__ __forceinline__ uint32_t load_sb(const uint16_t *s, const uint16_t *b, int64_t idx) {
-  return static_cast<uint32_t>(__ldg(s + idx)) | (static_cast<uint32_t>(__ldg(b + idx)) << 16);
+// 32 consecutive codes of one row (the calling thread's half of a K step) ->
+// four 16-byte chunks of bf16 weights, stored at the swizzled positions of
+// chunks 4h .. 4h+3 of B-tile row `row`.
+template <int BITS>
+__device__ __forceinline__ void dequant32(uint32_t codes_addr, uint32_t s2, uint32_t b2, uint32_t brow_addr, int row,
+                                          int h) {
+  uint32_t w[BITS];   // 32 codes = BITS words
+  if constexpr (BITS == 2) {
+    const uint2 v = ld_shared_v2(codes_addr);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < BITS / 4; ++i) {
+      const uint4 v = ld_shared_v4(codes_addr + 16 * i);
+      w[4 * i + 0] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {   // chunk i: codes 8i .. 8i+7 of the 32
+    uint32_t o[4];
+    if constexpr (BITS == 4) {
+      Dequant8<4>::natural(w[i], s2, b2, o);
+    } else if constexpr (BITS == 8) {
+      Dequant8<8>::natural(w[2 * i], w[2 * i + 1], s2, b2, o);
+    } else {
+      Dequant8<2>::natural(w[i >> 1] >> (16 * (i & 1)), s2, b2, o);
+    }
+    // 128-byte swizzle: 16-byte chunk c of row n lands at chunk c ^ (n mod 8)
+    const int c = 4 * h + i;
+    st_shared_v4(brow_addr + static_cast<uint32_t>((c ^ (row & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+  }
 }
 
 template <int BITS0, int BITS1, bool DUAL>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
-                   const __grid_constant__ CUtensorMap tm_w1, const PrefillParams p) {
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c0,
+                   const __grid_constant__ CUtensorMap tm_c1, const __grid_constant__ CUtensorMap tm_s0,
+                   const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_s1,
+                   const __grid_constant__ CUtensorMap tm_b1, const PrefillParams p) {
   using C = Cfg<BITS0, BITS1, DUAL>;
-  constexpr int S = C::kStages;
+  constexpr int Sx = C::kSx, Sb = C::kSb, Sc = C::kSc;
+  constexpr int kOps = DUAL ? 2 : 1;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + S * C::kStageBytes);
-  uint64_t *full = bars;             // TMA bytes landed (x + packed codes)
-  uint64_t *deq = bars + S;          // bf16 weights written by the dequantisers
-  uint64_t *empty = bars + 2 * S;    // MMAs of the stage completed
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+  uint64_t *x_full = bars;              // x tile landed (TMA bytes)
+  uint64_t *x_empty = x_full + Sx;      // MMAs reading the x tile completed
+  uint64_t *b_full = x_empty + Sx;      // B tile written by all dequantisers
+  uint64_t *b_empty = b_full + Sb;      // MMAs reading the B tile completed
+  uint64_t *c_full = b_empty + Sb;      // codes landed
+  uint64_t *c_empty = c_full + Sc;      // codes consumed by all dequantisers
+  uint64_t *s_full = c_empty + Sc;      // [op][2] scale entry landed
+  uint64_t *s_empty = s_full + 4;       // [op][2] scale entry consumed
   // Accumulation: each tile's K range is split in two halves that accumulate
   // in the two TMEM buffers X (first half) and Y (second half); the epilogue
   // adds Y into X with f32 adds.  Shorter tensor-core accumulation chains keep
   // the rounding of the stored projections close to a correctly rounded sum.
   // X of tile t is buffer t%2, Y the other one, so roles swap every tile.
-  uint64_t *acc_full = bars + 3 * S; // both chains of the tile are complete
-  uint64_t *y_free = acc_full + 1;   // Y has been added into X (Y reusable)
-  uint64_t *x_free = acc_full + 2;   // X has been read out (X reusable)
+  uint64_t *acc_full = s_empty + 4;     // both chains of the tile are complete
+  uint64_t *y_free = acc_full + 1;      // Y has been added into X (Y reusable)
+  uint64_t *xacc_free = acc_full + 2;   // X has been read out (X reusable)
   uint64_t *mma_done = acc_full + 3;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-  auto stage_a = [&](int s) { return smem + s * C::kStageBytes; };
-  auto stage_b = [&](int s) { return smem + s * C::kStageBytes + C::kABytes; };
-  auto stage_p0 = [&](int s) { return smem + s * C::kStageBytes + C::kABytes + C::kBBytes; };
-  auto stage_p1 = [&](int s) { return smem + s * C::kStageBytes + C::kABytes + C::kBBytes + C::kP0Bytes; };
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   unsigned int *err = &g_prefill_error;
+  const int my_tiles = (p.num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                       static_cast<int>(gridDim.x);
+  auto tile_of = [&](int i) { return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x); };
+  // K steps per scale-ring entry of each operand (8 groups of gs codes)
+  const int kpe0 = kGroupsPerEntry * p.gd0.gs / BK;
+  const int kpe1 = kGroupsPerEntry * p.gd1.gs / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&deq[s], kDeqWarps);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < Sx; ++s) {
+      mbar_init(&x_full[s], 1);
+      mbar_init(&x_empty[s], 1);
+    }
+    for (int s = 0; s < Sb; ++s) {
+      mbar_init(&b_full[s], kDeqWarps);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < Sc; ++s) {
+      mbar_init(&c_full[s], 1);
+      mbar_init(&c_empty[s], kDeqWarps);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], kDeqWarps / kOps);   // the warps that dequantise that operand
     }
     mbar_init(acc_full, 1);
     mbar_init(y_free, kEpiWarps);
-    mbar_init(x_free, kEpiWarps);
+    mbar_init(xacc_free, kEpiWarps);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == kWarpTma && lane == 0) {
     prefetch_tensormap(&tm_x);
-    prefetch_tensormap(&tm_w0);
-    if (DUAL) prefetch_tensormap(&tm_w1);
+    prefetch_tensormap(&tm_c0);
+    if (p.sb_tma0) {
+      prefetch_tensormap(&tm_s0);
+      prefetch_tensormap(&tm_b0);
+    }
+    if (DUAL) {
+      prefetch_tensormap(&tm_c1);
+      if (p.sb_tma1) {
+        prefetch_tensormap(&tm_s1);
+        prefetch_tensormap(&tm_b1);
+      }
+    }
   }
   if (warp == kWarpMma) {
     __syncwarp();
@@ -180,35 +269,118 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == kWarpTma) {
-    // ------------------------------------------------------------ producer --
+    // ------------------------------------------- codes and scale producer --
+    // Warp-wide loop; lane 0 issues the TMA copies.  Sequence index j runs
+    // over (tile, K step) pairs of this CTA; at step j the codes (and scale
+    // entries) of j are requested.
+    // Every step of this loop is on the critical path of the whole CTA, so it
+    // keeps running positions instead of dividing: (t_c, kb_c) for the codes
+    // stream, and per operand the entry index and position of the K step
+    // inside its scale entry.
+    const int steps = my_tiles * p.k_steps;
+    int n_c = 0;               // codes fills issued so far
+    int n_e[2] = {0, 0};       // scale entries issued per operand
+    int t_c = blockIdx.x, kb_c = 0, n0_c = (t_c / p.m_tiles) * C::kOutCols;
+    int epos[2] = {0, 0}, eidx[2] = {0, 0};
+    bool ok = true;
+    for (int j = 0; j < steps && ok; ++j) {
+      {
+        const int cs = n_c % Sc;
+        if (!(ok = warp_wait(&c_empty[cs], ((n_c / Sc) & 1) ^ 1u, abort_flag, p.timeout_ns, err))) break;
+        if (lane == 0) {
+          uint8_t *dst = smem + C::kCOff + cs * C::kCodesBytes;
+          mbar_arrive_expect_tx(&c_full[cs], C::kCodesBytes);
+          tma_load_2d(dst, &tm_c0, &c_full[cs], kb_c * BK * BITS0 / 32, n0_c);
+          if (DUAL) tma_load_2d(dst + C::kC0Bytes, &tm_c1, &c_full[cs], kb_c * BK * BITS1 / 32, n0_c);
+        }
+        ++n_c;
+#pragma unroll
+        for (int op = 0; op < kOps; ++op) {
+          const int kpe = op ? kpe1 : kpe0;
+          const bool start = epos[op] == 0;
+          if (++epos[op] == kpe) epos[op] = 0;
+          if (!start) continue;
+          const int es = n_e[op] & 1;
+          if (!(ok = warp_wait(&s_empty[op * 2 + es], ((n_e[op] >> 1) & 1) ^ 1u, abort_flag, p.timeout_ns,
+                               err)))
+            break;
+          const int rows = op ? C::kRows1 : C::kRows0;
+          uint8_t *sdst = smem + C::kSOff + es * C::kEntryBytes + (op ? 2 * C::kS0Bytes : 0);
+          uint8_t *bdst = sdst + (op ? C::kS1Bytes : C::kS0Bytes);
+          const int g0 = eidx[op]++ * kGroupsPerEntry;   // first group of the entry
+          if (op ? p.sb_tma1 : p.sb_tma0) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&s_full[op * 2 + es], 2 * rows * 2 * kGroupsPerEntry);
+              tma_load_2d(sdst, op ? &tm_s1 : &tm_s0, &s_full[op * 2 + es], g0, n0_c);
+              tma_load_2d(bdst, op ? &tm_b1 : &tm_b0, &s_full[op * 2 + es], g0, n0_c);
+            }
+          } else {
+            // rows whose scale rows cannot be TMA-staged: plain loads
+            const uint16_t *sg = op ? p.s1 : p.s0;
+            const uint16_t *bg = op ? p.b1 : p.b0;
+            const int ng = op ? p.ng1 : p.ng0;
+            for (int idx = lane; idx < rows * kGroupsPerEntry; idx += 32) {
+              const int r = idx / kGroupsPerEntry, gi = idx % kGroupsPerEntry;
+              const int64_t row = static_cast<int64_t>(n0_c) + r;
+              const int g = g0 + gi;
+              uint16_t sv = 0, bv = 0;
+              if (row < p.N && g < ng) {
+                sv = __ldg(sg + row * ng + g);
+                bv = __ldg(bg + row * ng + g);
+              }
+              st_shared_u16(smem_u32(sdst) + idx * 2, sv);
+              st_shared_u16(smem_u32(bdst) + idx * 2, bv);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_full[op * 2 + es]);
+          }
+          ++n_e[op];
+        }
+        if (!ok) break;
+        if (++kb_c == p.k_steps) {   // next tile of the codes stream
+          kb_c = 0;
+          t_c += gridDim.x;
+          n0_c = (t_c / p.m_tiles) * C::kOutCols;
+          epos[0] = epos[1] = 0;
+          eidx[0] = eidx[1] = 0;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // let the copies already issued land before the CTA's memory goes away
+      for (int s = 0; s < Sc && s < n_c; ++s) {
+        const int last = s + ((n_c - 1 - s) / Sc) * Sc;
+        mbar_wait_drain(&c_full[s], (last / Sc) & 1, 100000000ull);
+      }
+      for (int op = 0; op < kOps; ++op)
+        for (int e = n_e[op] - 2 < 0 ? 0 : n_e[op] - 2; e < n_e[op]; ++e)
+          mbar_wait_drain(&s_full[op * 2 + (e & 1)], (e >> 1) & 1, 100000000ull);
+    }
+    __syncwarp();
+  } else if (warp == kWarpX) {
+    // ------------------------------------------------------- x producer ----
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int last_parity[4] = {-1, -1, -1, -1};
+      int n_x = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        const int m0 = (t % p.m_tiles) * BM;
-        const int n0 = (t / p.m_tiles) * C::kOutCols;
+      for (int lt = 0; lt < my_tiles && ok; ++lt) {
+        const int m0 = (tile_of(lt) % p.m_tiles) * BM;
         for (int kb = 0; kb < p.k_steps; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.timeout_ns, err)) {
+          const int xs = n_x % Sx;
+          if (!mbar_wait(&x_empty[xs], ((n_x / Sx) & 1) ^ 1u, abort_flag, p.timeout_ns, err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], C::kTxBytes);
-          tma_load_2d(stage_a(stage), &tm_x, &full[stage], kb * BK, m0);
-          tma_load_2d(stage_p0(stage), &tm_w0, &full[stage], kb * BK * BITS0 / 32, n0);
-          if (DUAL) tma_load_2d(stage_p1(stage), &tm_w1, &full[stage], kb * BK * BITS1 / 32, n0);
-          last_parity[stage] = static_cast<int>(phase);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          mbar_arrive_expect_tx(&x_full[xs], kXBytes);
+          tma_load_2d(smem + C::kXOff + xs * kXBytes, &tm_x, &x_full[xs], kb * BK, m0);
+          ++n_x;
         }
       }
       if (!ok) {
         // let the copies already issued land before the CTA's memory goes away
-        for (int s = 0; s < S; ++s)
-          if (last_parity[s] >= 0) mbar_wait_drain(&full[s], static_cast<uint32_t>(last_parity[s]), 100000000ull);
+        for (int s = 0; s < Sx && s < n_x; ++s) {
+          const int last = s + ((n_x - 1 - s) / Sx) * Sx;
+          mbar_wait_drain(&x_full[s], (last / Sx) & 1, 100000000ull);
+        }
       }
     }
     __syncwarp();
@@ -216,19 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issue --
     if (lane == 0) {
       constexpr uint32_t kIdesc = umma_idesc_bf16(BM, BN);
-      int stage = 0;
-      uint32_t phase = 0;
+      int n_x = 0, n_b = 0;
       bool ok = true;
       const int k_half = (p.k_steps + 1) / 2;   // first chain: K steps [0, k_half)
-      int lt = 0;
-      for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x, ++lt) {
+      for (int lt = 0; lt < my_tiles && ok; ++lt) {
         const uint32_t x_tmem = tmem_base + static_cast<uint32_t>((lt & 1) * BN);
         const uint32_t y_tmem = tmem_base + static_cast<uint32_t>(((lt + 1) & 1) * BN);
         const uint32_t prev_parity = static_cast<uint32_t>((lt - 1) & 1);
         for (int kb = 0; kb < p.k_steps; ++kb) {
           // X of this tile was Y of the previous one, and Y was its X
           if (lt > 0 && (kb == 0 || kb == k_half)) {
-            if (!mbar_wait(kb == 0 ? y_free : x_free, prev_parity, abort_flag, p.timeout_ns, err)) {
+            if (!mbar_wait(kb == 0 ? y_free : xacc_free, prev_parity, abort_flag, p.timeout_ns, err)) {
               ok = false;
               break;
             }
@@ -236,24 +406,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t d_tmem = kb < k_half ? x_tmem : y_tmem;
           const bool chain_start = (kb == 0 || kb == k_half);
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.timeout_ns, err) ||
-              !mbar_wait(&deq[stage], phase, abort_flag, p.timeout_ns, err)) {
+          const int xs = n_x % Sx, bs = n_b % Sb;
+          if (!mbar_wait(&x_full[xs], (n_x / Sx) & 1, abort_flag, p.timeout_ns, err) ||
+              !mbar_wait(&b_full[bs], (n_b / Sb) & 1, abort_flag, p.timeout_ns, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = umma_desc_sw128(smem_u32(stage_a(stage)));
-          const uint64_t bdesc = umma_desc_sw128(smem_u32(stage_b(stage)));
+          const uint64_t adesc = umma_desc_sw128(smem_u32(smem + C::kXOff + xs * kXBytes));
+          const uint64_t bdesc = umma_desc_sw128(smem_u32(smem + C::kBOff + bs * kBBytes));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // +32 bytes of K per step inside the 128-byte swizzle atom
             umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (chain_start && kk == 0) ? 0u : 1u);
           }
-          umma_commit(&empty[stage]);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          umma_commit(&x_empty[xs]);
+          umma_commit(&b_empty[bs]);
+          ++n_x;
+          ++n_b;
         }
         if (ok) umma_commit(acc_full);
       }
@@ -265,77 +435,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kWarpEpi0) {
     // ---------------------------------------------------------- dequantise --
-    const int dt = threadIdx.x - kWarpDeq0 * 32;   // 0..255
-    const int c = dt & 7;                          // 8-code chunk within the stage
-    const int r0 = dt >> 3;                        // rows r0 + 32 j, j = 0..7
-    const int64_t ng0 = p.K / p.gs0, ng1 = DUAL ? p.K / p.gs1 : 1;
-    int stage = 0;
-    uint32_t phase = 0;
+    // Warp dw owns B rows 16 dw .. 16 dw + 15; lane = (row, half): lanes 0-15
+    // take codes 0-31 of the K step, lanes 16-31 codes 32-63.  In the fused
+    // form warps 0-7 hold the gate rows and warps 8-15 the up rows.
+    const int dw = warp - kWarpDeq0;
+    const int op = DUAL ? (dw >= kDeqWarps / 2) : 0;   // warp-uniform
+    const int row = dw * 16 + (lane & 15);               // B-tile row
+    const int h = lane >> 4;
+    const int r_op = DUAL ? (row & 127) : row;           // row within the operand's rows
+    const int kpe = op ? kpe1 : kpe0;
+    const GroupDiv gd = op ? p.gd1 : p.gd0;
+    const int bits = op ? BITS1 : BITS0;
+    const uint32_t c_row = static_cast<uint32_t>(C::kCOff + (op ? C::kC0Bytes : 0) +
+                                                 r_op * (op ? C::kC1Pitch : C::kC0Pitch) + h * 4 * bits);
+    const uint32_t s_row = static_cast<uint32_t>(C::kSOff + (op ? 2 * C::kS0Bytes : 0) + r_op * 16);
+    const uint32_t b_row = s_row + static_cast<uint32_t>(op ? C::kS1Bytes : C::kS0Bytes);
+    const uint32_t sbase = smem_u32(smem);
+    int n_c = 0, n_b = 0, n_e = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-      const int64_t n0 = static_cast<int64_t>(t / p.m_tiles) * C::kOutCols;
-      // offset of the scale row of each of this thread's 8 B rows (row clamped
-      // into range); 32-bit: rows * groups < 2^31 is checked on the host
-      uint32_t srow[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int n = r0 + 32 * j;
-        const int64_t r = n0 + (DUAL ? (n & 127) : n);
-        const uint32_t rc = static_cast<uint32_t>(r < p.N ? r : p.N - 1);
-        srow[j] = rc * static_cast<uint32_t>((!DUAL || j < 4) ? ng0 : ng1);
-      }
-      auto fetch_sb = [&](int kb, uint32_t (&sb)[8]) {
-        const uint32_t k = static_cast<uint32_t>(kb) * BK + 8 * c;
-        const uint32_t kc = k < static_cast<uint32_t>(p.K) ? k : static_cast<uint32_t>(p.K) - 1;
-        const uint32_t grp0 = p.gd0(kc), grp1 = p.gd1(kc);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const bool first = !DUAL || j < 4;
-          sb[j] = first ? load_sb(p.s0, p.b0, srow[j] + grp0) : load_sb(p.s1, p.b1, srow[j] + grp1);
-        }
-      };
-      // scale/bias registers for steps kb, kb+1, kb+2: the global loads are
-      // issued two K steps before they are used, hiding their latency
-      uint32_t sb_cur[8], sb_next[8], sb_next2[8];
-      fetch_sb(0, sb_cur);
-      if (1 < p.k_steps) fetch_sb(1, sb_next);
+    for (int lt = 0; lt < my_tiles && ok; ++lt) {
+      int epos = 0;   // K step within the current scale entry
       for (int kb = 0; kb < p.k_steps; ++kb) {
-        if (kb + 2 < p.k_steps) fetch_sb(kb + 2, sb_next2);
-        if (!warp_wait_lazy(&full[stage], phase, abort_flag, p.timeout_ns, err, 1000)) {
-          ok = false;
+        const int es = n_e & 1;
+        if (epos == 0 && !(ok = warp_wait(&s_full[op * 2 + es], (n_e >> 1) & 1, abort_flag, p.timeout_ns, err)))
           break;
-        }
-        const bool kvalid = static_cast<int64_t>(kb) * BK + 8 * c < p.K;
-        const uint32_t bbase = smem_u32(stage_b(stage));
-        const uint8_t *p0 = stage_p0(stage);
-        const uint8_t *p1 = stage_p1(stage);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int n = r0 + 32 * j;
-          const uint32_t s2 = prmt(sb_cur[j], 0, 0x1010u);   // scale in both halves
-          const uint32_t b2 = prmt(sb_cur[j], 0, 0x3232u);   // bias in both halves
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (kvalid) {
-            if (!DUAL || j < 4) {
-              v = dequant_chunk<BITS0>(p0 + (DUAL ? (n & 127) : n) * C::kP0Pitch, c, s2, b2);
-            } else {
-              v = dequant_chunk<BITS1>(p1 + (n & 127) * C::kP1Pitch, c, s2, b2);
-            }
-          }
-          // 128-byte swizzle: 16-byte chunk c of row n lands at chunk c ^ (n mod 8)
-          st_shared_v4(bbase + n * 128 + ((c ^ (n & 7)) << 4), v);
-        }
+        const int cs = n_c % Sc, bs = n_b % Sb;
+        if (!(ok = warp_wait(&c_full[cs], (n_c / Sc) & 1, abort_flag, p.timeout_ns, err))) break;
+        if (!(ok = warp_wait(&b_empty[bs], ((n_b / Sb) & 1) ^ 1u, abort_flag, p.timeout_ns, err))) break;
+        // scale and bias of this thread's 32 codes (one group: gs is a multiple of 32)
+        const uint32_t gi = gd(static_cast<uint32_t>(epos * BK + 32 * h));
+        const uint32_t eoff = static_cast<uint32_t>(es * C::kEntryBytes) + gi * 2;
+        const uint32_t s2 = splat_bf16(static_cast<uint16_t>(ld_shared_u16(sbase + s_row + eoff)));
+        const uint32_t b2 = splat_bf16(static_cast<uint16_t>(ld_shared_u16(sbase + b_row + eoff)));
+        const uint32_t caddr = sbase + c_row + static_cast<uint32_t>(cs * C::kCodesBytes);
+        const uint32_t baddr = sbase + static_cast<uint32_t>(C::kBOff + bs * kBBytes + row * 128);
+        if (op == 0)
+          dequant32<BITS0>(caddr, s2, b2, baddr, row, h);
+        else
+          dequant32<BITS1>(caddr, s2, b2, baddr, row, h);
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&deq[stage]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          sb_cur[j] = sb_next[j];
-          sb_next[j] = sb_next2[j];
+        if (lane == 0) {
+          mbar_arrive(&b_full[bs]);
+          mbar_arrive(&c_empty[cs]);
         }
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1u;
+        ++n_c;
+        ++n_b;
+        if (++epos == kpe || kb + 1 == p.k_steps) {
+          if (lane == 0) mbar_arrive(&s_empty[op * 2 + es]);
+          ++n_e;
+          epos = 0;
         }
       }
     }
@@ -346,8 +495,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool vec_ok = (p.N % 8) == 0;
     const bool two_chains = p.k_steps > 1;
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    int lt = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
+    for (int lt = 0; lt < my_tiles; ++lt) {
+      const int t = tile_of(lt);
       // the epilogue idles for a whole tile's main loop: wait without spinning
       if (!warp_wait_lazy(acc_full, static_cast<uint32_t>(lt & 1), abort_flag, p.timeout_ns, err, 10000)) break;
       tc_fence_after();
@@ -408,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(x_free);   // X may take the next tile's second chain
+      if (lane == 0) mbar_arrive(xacc_free);   // X may take the next tile's second chain
     }
   }
 
@@ -452,24 +601,37 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dtype, int elem_bytes, cons
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+// Scale/bias rows of an operand can be TMA-staged when their row stride and
+// base are 16-byte aligned (K/gs a multiple of 8).
+bool scales_tma_ok(const QuantOperand &op, int64_t K) {
+  return (K / op.gs) % kGroupsPerEntry == 0 && aligned16(op.s) && aligned16(op.b);
+}
+
+bool encode_scales(CUtensorMap *s, CUtensorMap *b, const QuantOperand &op, int64_t K, int64_t N, int rows) {
+  const uint64_t ng = static_cast<uint64_t>(K / op.gs);
+  return encode_2d(s, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, op.s, ng, N, kGroupsPerEntry, rows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
+         encode_2d(b, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, op.b, ng, N, kGroupsPerEntry, rows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 template <int BITS0, int BITS1, bool DUAL>
 cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                         const QuantOperand *op1, int variant, void *out, cudaStream_t stream, uint64_t timeout_ns,
                         int num_sms) {
   using C = Cfg<BITS0, BITS1, DUAL>;
-  CUtensorMap tm_x, tm_w0, tm_w1;
+  CUtensorMap tm_x, tm_c0, tm_c1, tm_s0, tm_b0, tm_s1, tm_b1;
   if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if (!encode_2d(&tm_w0, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, op0.w, K * BITS0 / 32, N, BK * BITS0 / 32, C::kRows0,
+  if (!encode_2d(&tm_c0, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, op0.w, K * BITS0 / 32, N, BK * BITS0 / 32, C::kRows0,
                  CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (DUAL) {
-    if (!encode_2d(&tm_w1, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, op1->w, K * BITS1 / 32, N, BK * BITS1 / 32, C::kRows1,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
-      return cudaErrorInvalidValue;
-  } else {
-    tm_w1 = tm_w0;
-  }
+  tm_c1 = tm_c0;
+  if (DUAL && !encode_2d(&tm_c1, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, op1->w, K * BITS1 / 32, N, BK * BITS1 / 32,
+                         C::kRows1, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
 
   PrefillParams p{};
   p.M = M;
@@ -477,13 +639,18 @@ cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   p.N = N;
   p.s0 = op0.s;
   p.b0 = op0.b;
-  p.gs0 = op0.gs;
   p.s1 = DUAL ? op1->s : op0.s;
   p.b1 = DUAL ? op1->b : op0.b;
-  p.gs1 = DUAL ? op1->gs : op0.gs;
-  p.gd0 = GroupDiv::make(p.gs0);
-  p.gd1 = GroupDiv::make(p.gs1);
-  if (N * (K / (p.gs0 < p.gs1 ? p.gs0 : p.gs1)) >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  p.ng0 = static_cast<int>(K / op0.gs);
+  p.ng1 = static_cast<int>(K / (DUAL ? op1->gs : op0.gs));
+  p.gd0 = GroupDiv::make(op0.gs);
+  p.gd1 = GroupDiv::make(DUAL ? op1->gs : op0.gs);
+  if (N * (K / (op0.gs < p.gd1.gs ? op0.gs : p.gd1.gs)) >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+  p.sb_tma0 = scales_tma_ok(op0, K) ? 1 : 0;
+  p.sb_tma1 = DUAL ? (scales_tma_ok(*op1, K) ? 1 : 0) : 0;
+  tm_s0 = tm_b0 = tm_s1 = tm_b1 = tm_c0;   // placeholders where no scale map is used
+  if (p.sb_tma0 && !encode_scales(&tm_s0, &tm_b0, op0, K, N, C::kRows0)) return cudaErrorInvalidValue;
+  if (p.sb_tma1 && !encode_scales(&tm_s1, &tm_b1, *op1, K, N, C::kRows1)) return cudaErrorInvalidValue;
   p.variant = variant;
   p.out = static_cast<uint16_t *>(out);
   p.m_tiles = static_cast<int>((M + BM - 1) / BM);
@@ -505,7 +672,8 @@ cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const Qu
     attr_done.fetch_or(uint64_t(1) << dev);
   }
   const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
-  prefill_kernel<BITS0, BITS1, DUAL><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_x, tm_w0, tm_w1, p);
+  prefill_kernel<BITS0, BITS1, DUAL><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_x, tm_c0, tm_c1, tm_s0, tm_b0,
+                                                                                 tm_s1, tm_b1, p);
   return cudaGetLastError();
 }
 
