@@ -130,6 +130,18 @@ __device__ __forceinline__ bool warp_wait_lazy(uint64_t *bar, uint32_t parity, v
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, timeout_ns, err));
 }
 
+// Wait executed by a whole warp for waits that are usually short: lane 0
+// polls, then every lane observes the completed phase itself; the outcome is
+// warp-uniform (false: give up).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns,
+                                          unsigned int *err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, timeout_ns, err) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (!ok) return false;
+  return __all_sync(0xffffffffu, mbar_try_wait(bar, parity));
+}
+
 // Wait used while tearing down after an abort: ignores the abort flag (it is
 // already raised) and gives up silently after `timeout_ns`.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {

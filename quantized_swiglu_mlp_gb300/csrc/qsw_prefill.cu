@@ -128,17 +128,6 @@ __device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
                : "memory");
 }
 
-// Wait executed by a whole warp: lane 0 polls, then every lane observes the
-// completed phase itself; the outcome is warp-uniform (false: give up).
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort, uint64_t timeout_ns,
-                                          unsigned int *err) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, timeout_ns, err) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  if (!ok) return false;
-  return __all_sync(0xffffffffu, mbar_try_wait(bar, parity));
-}
-
 // 32 consecutive codes of one row (the calling thread's half of a K step) ->
 // four 16-byte chunks of bf16 weights, stored at the swizzled positions of
 // chunks 4h .. 4h+3 of B-tile row `row`.
