@@ -487,22 +487,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int lt = 0; lt < my_tiles; ++lt) {
       const int t = tile_of(lt);
       // the epilogue idles for a whole tile's main loop: wait without spinning
-      if (!warp_wait_lazy(acc_full, static_cast<uint32_t>(lt & 1), abort_flag, p.timeout_ns, err, 10000)) break;
+      if (!warp_wait_lazy(acc_full, static_cast<uint32_t>(lt & 1), abort_flag, p.timeout_ns, err, 500)) break;
       tc_fence_after();
       const uint32_t tbase = lane_base + static_cast<uint32_t>((lt & 1) * BN);          // X
       const uint32_t ybase = lane_base + static_cast<uint32_t>(((lt + 1) & 1) * BN);    // Y
       if (two_chains) {
-        // X += Y over all columns, f32 adds rounded to nearest
+        // X += Y over all columns, f32 adds rounded to nearest.  The next tile's
+        // first chain waits for this pass, so it keeps four loads in flight
+        // per wait (32 columns).
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          uint32_t ra[16], rb[16];
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t ra[16], rb[16], rc[16], rd[16];
           __syncwarp();
           tmem_ld16(tbase + c0, ra);
           tmem_ld16(ybase + c0, rb);
+          tmem_ld16(tbase + c0 + 16, rc);
+          tmem_ld16(ybase + c0 + 16, rd);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ra[e] = __float_as_uint(__uint_as_float(ra[e]) + __uint_as_float(rb[e]));
+          for (int e = 0; e < 16; ++e) {
+            ra[e] = __float_as_uint(__uint_as_float(ra[e]) + __uint_as_float(rb[e]));
+            rc[e] = __float_as_uint(__uint_as_float(rc[e]) + __uint_as_float(rd[e]));
+          }
           tmem_st16(tbase + c0, ra);
+          tmem_st16(tbase + c0 + 16, rc);
         }
         tmem_st_wait();
       }
