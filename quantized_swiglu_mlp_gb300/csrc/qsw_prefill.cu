@@ -53,6 +53,7 @@ constexpr int kXBytes = BM * BK * 2;                      // 16 KB
 constexpr int kBBytes = BN * BK * 2;                      // 32 KB
 constexpr int kGroupsPerEntry = 8;                        // scale groups per ring entry (16 bytes)
 constexpr int kBarBytes = 512;
+constexpr int kChainSteps = 20;                          // K steps per accumulation chain, at most
 
 __device__ unsigned int g_prefill_error;
 
@@ -186,12 +187,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *c_empty = c_full + Sc;      // codes consumed by all dequantisers
   uint64_t *s_full = c_empty + Sc;      // [op][2] scale entry landed
   uint64_t *s_empty = s_full + 4;       // [op][2] scale entry consumed
-  // Accumulation: each tile's K range is split in two halves that accumulate
-  // in the two TMEM buffers X (first half) and Y (second half); the epilogue
-  // adds Y into X with f32 adds.  Shorter tensor-core accumulation chains keep
-  // the rounding of the stored projections close to a correctly rounded sum.
-  // X of tile t is buffer t%2, Y the other one, so roles swap every tile.
-  uint64_t *acc_full = s_empty + 4;     // both chains of the tile are complete
+  // Accumulation: each tile's K range is split into chains of at most
+  // kChainSteps K steps.  Chain 0 accumulates in TMEM buffer X, every later
+  // chain in buffer Y, and the epilogue adds Y into X with f32 adds after each
+  // of them.  Short tensor-core accumulation chains keep the rounding of the
+  // stored projections close to a correctly rounded sum.  X of tile t is
+  // buffer t%2, Y the other one, so roles swap every tile.
+  uint64_t *acc_full = s_empty + 4;     // a chain that ends in Y (or a single-chain tile) is complete
   uint64_t *y_free = acc_full + 1;      // Y has been added into X (Y reusable)
   uint64_t *xacc_free = acc_full + 2;   // X has been read out (X reusable)
   uint64_t *mma_done = acc_full + 3;
@@ -379,22 +381,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdesc = umma_idesc_bf16(BM, BN);
       int n_x = 0, n_b = 0;
       bool ok = true;
-      const int k_half = (p.k_steps + 1) / 2;   // first chain: K steps [0, k_half)
+      // Chains of at most kChainSteps K steps (see the accumulation note at the
+      // barriers): chain 0 accumulates in X, chains 1.. in Y, and the epilogue
+      // adds Y into X after each of them.  Completions counted per barrier:
+      // y_free P per tile, xacc_free 1 per tile, acc_full P per tile.
+      const int nc = (p.k_steps + kChainSteps - 1) / kChainSteps;
+      const int clen = (p.k_steps + nc - 1) / nc;   // K steps per chain (the last may be shorter)
+      const int P = nc > 1 ? nc - 1 : 1;
       for (int lt = 0; lt < my_tiles && ok; ++lt) {
         const uint32_t x_tmem = tmem_base + static_cast<uint32_t>((lt & 1) * BN);
         const uint32_t y_tmem = tmem_base + static_cast<uint32_t>(((lt + 1) & 1) * BN);
-        const uint32_t prev_parity = static_cast<uint32_t>((lt - 1) & 1);
+        int c = 0, cpos = 0;   // chain and K step within it
         for (int kb = 0; kb < p.k_steps; ++kb) {
-          // X of this tile was Y of the previous one, and Y was its X
-          if (lt > 0 && (kb == 0 || kb == k_half)) {
-            if (!mbar_wait(kb == 0 ? y_free : xacc_free, prev_parity, abort_flag, p.timeout_ns, err)) {
-              ok = false;
-              break;
+          if (cpos == 0) {
+            // X of this tile was Y of the previous one, and Y was its X:
+            // chain 0 needs the previous tile's last X += Y done, chain 1 the
+            // previous tile's X read out, chain c >= 2 the X += Y of chain c-1
+            uint64_t *bar = nullptr;
+            int n = 0;
+            if (c == 0 && lt > 0) {
+              bar = y_free;
+              n = lt * P - 1;
+            } else if (c == 1 && lt > 0) {
+              bar = xacc_free;
+              n = lt - 1;
+            } else if (c >= 2) {
+              bar = y_free;
+              n = lt * P + c - 2;
             }
-            tc_fence_after();
+            if (bar != nullptr) {
+              if (!mbar_wait(bar, static_cast<uint32_t>(n & 1), abort_flag, p.timeout_ns, err)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
           }
-          const uint32_t d_tmem = kb < k_half ? x_tmem : y_tmem;
-          const bool chain_start = (kb == 0 || kb == k_half);
+          const uint32_t d_tmem = c == 0 ? x_tmem : y_tmem;
+          const bool chain_start = cpos == 0;
           const int xs = n_x % Sx, bs = n_b % Sb;
           if (!mbar_wait(&x_full[xs], (n_x / Sx) & 1, abort_flag, p.timeout_ns, err) ||
               !mbar_wait(&b_full[bs], (n_b / Sb) & 1, abort_flag, p.timeout_ns, err)) {
@@ -413,8 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&b_empty[bs]);
           ++n_x;
           ++n_b;
+          if (++cpos == clen || kb + 1 == p.k_steps) {   // chain c complete
+            if (c >= 1 || nc == 1) umma_commit(acc_full);
+            ++c;
+            cpos = 0;
+          }
         }
-        if (ok) umma_commit(acc_full);
       }
       if (!ok) {
         umma_commit(mma_done);
@@ -482,41 +510,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
     const bool vec_ok = (p.N % 8) == 0;
-    const bool two_chains = p.k_steps > 1;
+    const int nc = (p.k_steps + kChainSteps - 1) / kChainSteps;
+    const int P = nc > 1 ? nc - 1 : 1;   // acc_full completions per tile
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    for (int lt = 0; lt < my_tiles; ++lt) {
+    bool ok = true;
+    for (int lt = 0; lt < my_tiles && ok; ++lt) {
       const int t = tile_of(lt);
-      // the epilogue idles for a whole tile's main loop: wait without spinning
-      if (!warp_wait_lazy(acc_full, static_cast<uint32_t>(lt & 1), abort_flag, p.timeout_ns, err, 500)) break;
-      tc_fence_after();
       const uint32_t tbase = lane_base + static_cast<uint32_t>((lt & 1) * BN);          // X
       const uint32_t ybase = lane_base + static_cast<uint32_t>(((lt + 1) & 1) * BN);    // Y
-      if (two_chains) {
-        // X += Y over all columns, f32 adds rounded to nearest.  The next tile's
-        // first chain waits for this pass, so it keeps four loads in flight
-        // per wait (32 columns).
+      for (int q = 0; q < P; ++q) {
+        // the epilogue idles for most of a chain: wait without spinning
+        if (!(ok = warp_wait_lazy(acc_full, static_cast<uint32_t>((lt * P + q) & 1), abort_flag, p.timeout_ns, err,
+                                  500)))
+          break;
+        tc_fence_after();
+        if (nc > 1) {
+          // X += Y over all columns, f32 adds rounded to nearest.  The next
+          // chain waits for this pass, so it keeps four loads in flight per
+          // wait (32 columns).
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t ra[16], rb[16], rc[16], rd[16];
-          __syncwarp();
-          tmem_ld16(tbase + c0, ra);
-          tmem_ld16(ybase + c0, rb);
-          tmem_ld16(tbase + c0 + 16, rc);
-          tmem_ld16(ybase + c0 + 16, rd);
-          tmem_ld_wait();
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t ra[16], rb[16], rc[16], rd[16];
+            __syncwarp();
+            tmem_ld16(tbase + c0, ra);
+            tmem_ld16(ybase + c0, rb);
+            tmem_ld16(tbase + c0 + 16, rc);
+            tmem_ld16(ybase + c0 + 16, rd);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            ra[e] = __float_as_uint(__uint_as_float(ra[e]) + __uint_as_float(rb[e]));
-            rc[e] = __float_as_uint(__uint_as_float(rc[e]) + __uint_as_float(rd[e]));
+            for (int e = 0; e < 16; ++e) {
+              ra[e] = __float_as_uint(__uint_as_float(ra[e]) + __uint_as_float(rb[e]));
+              rc[e] = __float_as_uint(__uint_as_float(rc[e]) + __uint_as_float(rd[e]));
+            }
+            tmem_st16(tbase + c0, ra);
+            tmem_st16(tbase + c0 + 16, rc);
           }
-          tmem_st16(tbase + c0, ra);
-          tmem_st16(tbase + c0 + 16, rc);
+          tmem_st_wait();
         }
-        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(y_free);   // Y may take the next chain
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(y_free);   // Y may take the next tile's first chain
+      if (!ok) break;
       const int64_t m = static_cast<int64_t>(t % p.m_tiles) * BM + row;
       const int64_t n0 = static_cast<int64_t>(t / p.m_tiles) * C::kOutCols;
       uint16_t *orow = p.out + m * p.N;
@@ -554,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(xacc_free);   // X may take the next tile's second chain
+      if (lane == 0) mbar_arrive(xacc_free);   // X may take the next tile's chains 1..
     }
   }
 
