@@ -53,7 +53,7 @@ constexpr int kXBytes = BM * BK * 2;                      // 16 KB
 constexpr int kBBytes = BN * BK * 2;                      // 32 KB
 constexpr int kGroupsPerEntry = 8;                        // scale groups per ring entry (16 bytes)
 constexpr int kBarBytes = 512;
-constexpr int kChainSteps = 20;                          // K steps per accumulation chain, at most
+constexpr int kChainSteps = 22;                          // K steps per accumulation chain, at most
 
 __device__ unsigned int g_prefill_error;
 
