@@ -243,6 +243,10 @@ def bench_decode(args, dev, stream, peaks, peak_src):
     algo_bytes = wbytes + case.x.nbytes + 2 * case.I
     variant = ops.VARIANTS[args.variant]
 
+    # weights are constant across the decode loop: let each call stream its
+    # weights while the previous call finishes (it still reads x only after)
+    ops.qsw_set_early_weight_stream(args.early_weights)
+
     def step(i):
         ops.qswiglu_forward(x, *reps[i % replicas], variant=variant, out=out, stream=stream)
 
@@ -420,6 +424,7 @@ def run_ours(args):
                                f"{args.variant.upper()}",
                    "M": 1, "H": 2048, "I": 8192, "bits": 4, "gs": 64, "variant": args.variant,
                    "weight_bytes_per_step": d["wbytes"],
+                   "early_weight_stream": bool(args.early_weights),
                    "l2": f"weights rotated over {d['replicas']} replicas "
                          f"({d['replicas'] * d['wbytes'] / 1e6:.0f} MB > 3x L2 {d['l2_bytes'] / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}"},
@@ -513,6 +518,8 @@ def main(argv=None):
     ap.add_argument("--variant", choices=["match", "f32"], default="match")
     ap.add_argument("--prefill-steps", type=int, default=10)
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--early-weights", type=int, choices=[0, 1], default=1,
+                    help="decode calls stream their weights while the previous call finishes (library switch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--only", choices=["all", "decode", "large", "mid"], default="all",

@@ -129,6 +129,17 @@ QSW_API qsw_status qsw_check_device_errors(void *stream);
 QSW_API void qsw_set_gemv_max_m(int m);
 QSW_API int qsw_get_gemv_max_m(void);
 
+/* Early weight stream (default off).  When on, the small-M kernel is launched
+ * as a programmatic dependent of the work before it on the stream: it may start
+ * while the previous kernel is still running and streams the packed weights,
+ * scales and biases of its first units into shared memory at once; it reads x
+ * and writes hidden only after all earlier work on the stream has completed
+ * (griddepcontrol.wait).  Turn it on only when no earlier work on the stream
+ * writes the weight, scale or bias arrays of the call -- the usual decode loop,
+ * where weights are constant.  Process-wide. */
+QSW_API void qsw_set_early_weight_stream(int on);
+QSW_API int qsw_get_early_weight_stream(void);
+
 /* Per-wait limit for device-side waits, in nanoseconds (default 4e9). */
 QSW_API void qsw_set_wait_timeout_ns(uint64_t ns);
 

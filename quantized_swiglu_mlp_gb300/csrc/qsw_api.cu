@@ -22,6 +22,7 @@ namespace {
 std::atomic<uint64_t> g_counters[QSW_NUM_COUNTERS];
 std::atomic<int> g_gemv_max_m{-1};   // -1: not yet initialised
 std::atomic<uint64_t> g_timeout_ns{4000000000ull};
+std::atomic<int> g_early_weights{0};
 
 int gemv_max_m() {
   int v = g_gemv_max_m.load(std::memory_order_relaxed);
@@ -98,7 +99,8 @@ qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const
   const qsw::QuantOperand u{wu, static_cast<const uint16_t *>(su), static_cast<const uint16_t *>(bu), gs_u, bits_u};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M <= gemv_max_m() && qsw::gemv_fits(M, H, I, g, &u, sm_count())) {
-    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count()));
+    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count(),
+                                    g_early_weights.load(std::memory_order_relaxed) != 0));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
     st = from_cuda(qsw::launch_prefill(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count()));
@@ -119,7 +121,8 @@ qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N, const uint
   const qsw::QuantOperand op{w, static_cast<const uint16_t *>(s), static_cast<const uint16_t *>(b), gs, bits};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (M <= gemv_max_m() && qsw::gemv_fits(M, K, N, op, nullptr, sm_count())) {
-    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs, g_timeout_ns.load(), sm_count()));
+    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs, g_timeout_ns.load(), sm_count(),
+                                    g_early_weights.load(std::memory_order_relaxed) != 0));
     if (st == QSW_OK) g_counters[QSW_CNT_QMM_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
     st = from_cuda(qsw::launch_prefill(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs, g_timeout_ns.load(),
@@ -158,6 +161,10 @@ int qsw_get_gemv_max_m(void) { return gemv_max_m(); }
 
 void qsw_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
 
+void qsw_set_early_weight_stream(int on) { g_early_weights.store(on ? 1 : 0); }
+
+int qsw_get_early_weight_stream(void) { return g_early_weights.load(); }
+
 void qsw_get_counters(uint64_t *out, int n) {
   if (!out) return;
   for (int i = 0; i < n && i < QSW_NUM_COUNTERS; ++i) out[i] = g_counters[i].load();
@@ -178,6 +185,6 @@ const char *qsw_status_string(qsw_status s) {
   }
 }
 
-int qsw_version(void) { return 100; }
+int qsw_version(void) { return 101; }
 
 }  // extern "C"

@@ -152,6 +152,16 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity, 
   return true;
 }
 
+// ------------------------------------------------ programmatic dependents --
+
+// Let the next grid on the stream (launched as a programmatic dependent) be
+// scheduled; wait until every grid this one depends on has completed and its
+// memory is visible.  Both are no-ops without a programmatic dependency.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // --------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int c0, int c1) {

@@ -65,6 +65,7 @@ struct GemvParams {
   int x_off;              // byte offset of the staged x fragments
   int red_off;            // byte offset of the partial sums
   int bar_off;            // byte offset of the barriers
+  int early;              // launched as a programmatic dependent (early weight stream)
   uint64_t timeout_ns;
 };
 
@@ -170,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
   uint64_t *red_full = full + kMaxSlots;                                          // [kGroups][2]
   uint64_t *red_free = red_full + 2 * kGroups;                                    // [kGroups][2]
   uint64_t *x_ready = red_free + 2 * kGroups;                                     // x staged
-  unsigned int *done_cnt = reinterpret_cast<unsigned int *>(x_ready + 1);         // [kMaxSlots]
+  uint64_t *x_requested = x_ready + 1;                                            // x loads issued
+  unsigned int *done_cnt = reinterpret_cast<unsigned int *>(x_requested + 1);     // [kMaxSlots]
   unsigned int *issued_cnt = done_cnt + kMaxSlots;                                     // [kMaxSlots]
   volatile int *abort_flag = reinterpret_cast<volatile int *>(issued_cnt + kMaxSlots);
   float *red = reinterpret_cast<float *>(smem + p.red_off);   // [kGroups][2][kGroupWarps][NG][32][4]
@@ -195,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
       mbar_init(&red_free[b], 1);
     }
     mbar_init(x_ready, kWarps - 1);
+    mbar_init(x_requested, kWarps - 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -233,26 +236,51 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
   };
   constexpr int kStageThreads = kThreads - 32;
   const bool stager = static_cast<int>(threadIdx.x) < kStageThreads;
-  uint4 x_pre[kXPre][4];
-#pragma unroll
-  for (int r = 0; r < kXPre; ++r)
-    if (stager && static_cast<int>(threadIdx.x) + r * kStageThreads < x_total)
-      load_x(threadIdx.x + r * kStageThreads, x_pre[r]);
-  __syncthreads();
   // Each group owns `spg` slots and uses them in turn, so a slot only ever
   // holds the units of one group, in order (a waiter is never more than one
-  // fill ahead of its slot).  The last warp puts the first units of every slot in
-  // flight, every group's first unit first; later fills are issued by the
+  // fill ahead of its slot).  The last warp puts the first units of every slot
+  // in flight, every group's first unit first; later fills are issued by the
   // group's warp that finishes last.
   const int spg = p.slots / kGroups;
+  auto issue_round = [&](int s) {
+    for (int q = 0; q < kGroups; ++q) {
+      const int i = q + s * kGroups;
+      if (i < my_units)
+        issue_unit<BITS0, BB, DUAL>(p, smem + (q * spg + s) * p.slot_bytes, &full[q * spg + s],
+                                    &issued_cnt[q * spg + s], unit_of(i), lane);
+    }
+  };
+  uint4 x_pre[kXPre][4];
+  auto preload_x = [&]() {
+#pragma unroll
+    for (int r = 0; r < kXPre; ++r)
+      if (stager && static_cast<int>(threadIdx.x) + r * kStageThreads < x_total)
+        load_x(threadIdx.x + r * kStageThreads, x_pre[r]);
+  };
+  int first_round = 0;
+  if (p.early) {
+    // Programmatic dependent launch: the next call may be scheduled as soon as
+    // every CTA of this one has got here.  Weights are not written by earlier
+    // work on the stream (caller's guarantee), so the first unit of every group
+    // is requested before waiting for that work; x is read only after it.
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    __syncthreads();
+    if (!stager) issue_round(0);
+    first_round = 1;
+    griddep_wait();
+    preload_x();
+    if (stager) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(x_requested);   // this warp's x loads are in flight
+    } else if (!warp_wait(x_requested, 0, abort_flag, p.timeout_ns, err)) {
+      first_round = spg;   // give up issuing; the waits below time out the same way
+    }
+  } else {
+    preload_x();
+    __syncthreads();
+  }
   if (!stager) {
-    for (int s = 0; s < spg; ++s)
-      for (int q = 0; q < kGroups; ++q) {
-        const int i = q + s * kGroups;
-        if (i < my_units)
-          issue_unit<BITS0, BB, DUAL>(p, smem + (q * spg + s) * p.slot_bytes, &full[q * spg + s],
-                                      &issued_cnt[q * spg + s], unit_of(i), lane);
-      }
+    for (int s = first_round; s < spg; ++s) issue_round(s);
   } else {
 #pragma unroll
     for (int r = 0; r < kXPre; ++r)
@@ -430,7 +458,7 @@ Layout plan(int64_t K, int64_t N, int M, int gs0, int gs1, int bits0, int bits1,
   const int64_t nkb = (K + kBlockK - 1) / kBlockK;
   const int64_t x_bytes = nkb * NG * kXBlockBytes;
   const int64_t red_bytes = static_cast<int64_t>(kGroups) * 2 * kGroupWarps * NG * 128 * 4;
-  const int64_t bar_bytes = (kMaxSlots + 4 * kGroups + 1) * 8 + 2 * kMaxSlots * 4 + 16;
+  const int64_t bar_bytes = (kMaxSlots + 4 * kGroups + 2) * 8 + 2 * kMaxSlots * 4 + 16;
   const int64_t fixed = x_bytes + red_bytes + bar_bytes;
   const int64_t units = (N + R - 1) / R;
   const int64_t grid = units < num_sms ? units : num_sms;
@@ -474,8 +502,18 @@ cudaError_t launch_cfg(GemvParams p, const Layout &l, cudaStream_t stream, int n
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(uint64_t(1) << dev);
   }
-  gemv_kernel<BITS0, BITS1, DUAL, NG><<<grid, kThreads, l.total, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = l.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.early ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_kernel<BITS0, BITS1, DUAL, NG>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int BITS0, int BITS1, bool DUAL>
@@ -509,7 +547,7 @@ bool gemv_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const Q
 
 cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                         const QuantOperand *op1, int variant, void *out, cudaStream_t stream,
-                        uint64_t timeout_ns, int num_sms) {
+                        uint64_t timeout_ns, int num_sms, bool early_weights) {
   if (!gemv_fits(M, K, N, op0, op1, num_sms)) return cudaErrorInvalidValue;
   const QuantOperand &o1 = op1 ? *op1 : op0;
   const Layout l = plan(K, N, static_cast<int>(M), op0.gs, o1.gs, op0.bits, o1.bits, op1 != nullptr, num_sms);
@@ -531,6 +569,7 @@ cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   p.variant = variant;
   p.out = static_cast<uint16_t *>(out);
   p.timeout_ns = timeout_ns;
+  p.early = early_weights ? 1 : 0;
   if (op1) {
     switch (op0.bits) {
       case 2: return launch_dual_bits1<2>(p, l, op1->bits, stream, num_sms);

@@ -19,9 +19,12 @@ struct QuantOperand {
 
 // Small-M kernel: rows of x up to 32.  `dual` selects the fused SwiGLU
 // (gate + up, epilogue `variant`) or a single quantised linear (y = bf16(x.W^T)).
+// `early_weights`: launch as a programmatic dependent and stream weights
+// before waiting for the preceding work (the caller guarantees that no earlier
+// work on the stream writes the weight arrays).
 cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                         const QuantOperand *op1, int variant, void *out, cudaStream_t stream,
-                        uint64_t timeout_ns, int num_sms);
+                        uint64_t timeout_ns, int num_sms, bool early_weights);
 
 // Whether the small-M kernel can stage rows of length K (else the tensor-core
 // kernel serves every M).

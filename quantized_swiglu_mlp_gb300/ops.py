@@ -29,7 +29,8 @@ NUM_COUNTERS = 5
 STATUS = {0: "QSW_OK", 1: "QSW_ERR_INVALID_ARG", 2: "QSW_ERR_UNSUPPORTED", 3: "QSW_ERR_CUDA",
           4: "QSW_ERR_TIMEOUT"}
 EXPORTED = ("qswiglu_forward", "affine_qmm", "qsw_silu_mul", "qsw_check_device_errors",
-            "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_wait_timeout_ns",
+            "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_early_weight_stream",
+            "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns",
             "qsw_get_counters", "qsw_reset_counters", "qsw_status_string", "qsw_version")
 
 _lock = threading.Lock()
@@ -63,6 +64,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.qsw_check_device_errors.restype = i32
         lib.qsw_set_gemv_max_m.argtypes = [i32]
         lib.qsw_get_gemv_max_m.restype = i32
+        lib.qsw_set_early_weight_stream.argtypes = [i32]
+        lib.qsw_get_early_weight_stream.restype = i32
         lib.qsw_set_wait_timeout_ns.argtypes = [u64]
         lib.qsw_get_counters.argtypes = [ctypes.POINTER(u64), i32]
         lib.qsw_status_string.argtypes = [i32]
@@ -214,6 +217,14 @@ def qsw_reset_counters() -> None:
 
 def qsw_status_string(code: int) -> str:
     return load_library().qsw_status_string(int(code)).decode()
+
+
+def qsw_set_early_weight_stream(on: bool) -> None:
+    load_library().qsw_set_early_weight_stream(1 if on else 0)
+
+
+def qsw_get_early_weight_stream() -> bool:
+    return bool(load_library().qsw_get_early_weight_stream())
 
 
 def qsw_version() -> int:

@@ -120,3 +120,18 @@ def test_python_binding_rejects_host_tensors(lib):
     x = torch.zeros(2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         ops.qswiglu_forward(x, x, x, x, 64, 4, x, x, x, 64, 4)
+
+
+def test_early_weight_stream_switch():
+    """The early weight stream is off by default and toggles process-wide."""
+    from quantized_swiglu_mlp_gb300 import ops
+    ops.load_library()
+    saved = ops.qsw_get_early_weight_stream()
+    try:
+        ops.qsw_set_early_weight_stream(True)
+        assert ops.qsw_get_early_weight_stream() is True
+        ops.qsw_set_early_weight_stream(False)
+        assert ops.qsw_get_early_weight_stream() is False
+    finally:
+        ops.qsw_set_early_weight_stream(saved)
+

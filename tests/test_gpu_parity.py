@@ -306,3 +306,54 @@ def test_full_mixed_sweep(dev, gemv_limit, M):
         # the other kernel at the same M meets the same bound
         gemv_limit(0 if M <= 16 else 32)
         check_fused(case, dev, ops.MATCH, rows=rows)
+
+
+@pytest.fixture
+def early_weights():
+    saved = ops.qsw_get_early_weight_stream()
+    yield ops.qsw_set_early_weight_stream
+    ops.qsw_set_early_weight_stream(saved)
+
+
+@pytest.mark.parametrize("graph", [False, True], ids=["stream", "graph"])
+def test_early_weight_stream_reads_previous_output(dev, gemv_limit, early_weights, graph):
+    """With the early weight stream on, a small-M call may start while the call
+    before it runs; it must still read x only after that call wrote it.  Three
+    fused calls are chained (I == H, each call's hidden is the next call's x),
+    on a stream and captured in a CUDA graph, and every output is checked
+    against the oracle fed the GPU's own previous output."""
+    gemv_limit(16)
+    early_weights(True)
+    cases = [inputs.make_case(2, 1024, 1024, seed=s, scale_range=(0.01, 0.03)) for s in (11, 12, 13)]
+    args = [device_args(c, dev) for c in cases]
+    x0 = args[0][0]
+    outs = [torch.empty((2, 1024), dtype=torch.bfloat16, device=dev) for _ in cases]
+    stream = torch.cuda.Stream(device=dev)
+
+    def chain():
+        x = x0
+        for a, o in zip(args, outs):
+            ops.qswiglu_forward(x, *a[1:], variant=ops.MATCH, out=o, stream=stream)
+            x = o
+
+    torch.cuda.synchronize()
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            chain()
+        for o in outs:
+            o.fill_(0)
+        torch.cuda.synchronize()
+        g.replay()
+    else:
+        with torch.cuda.stream(stream):
+            chain()
+    ops.qsw_check_device_errors(stream)
+    x_bits = to_bits(x0)
+    for c, o in zip(cases, outs):
+        step = inputs.Case(x=x_bits, gate=c.gate, up=c.up)
+        want = oracle.qswiglu(*step.oracle_args(), variant=oracle.MATCH)
+        got = to_bits(o)
+        ok, info = check_match(got, want)
+        assert ok, info
+        x_bits = got
