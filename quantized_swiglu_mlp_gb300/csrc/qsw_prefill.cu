@@ -10,23 +10,25 @@
 //
 // GB300 design (sm_103a), one persistent CTA per SM, warp-specialised, three
 // shared-memory rings filled by TMA and one filled by the dequantisers:
-//   x ring      x tile [128 x 64] bf16, 128-byte swizzle     TMA    -> MMA
-//   codes ring  packed codes of the tile's 256 B rows          TMA    -> dequant
+//   x ring      x tile [256 x 64] bf16, 128-byte swizzle     TMA    -> MMA
+//   codes ring  packed codes of the tile's 128 B rows          TMA    -> dequant
 //   scale ring  per operand: scales and biases of 8 groups     TMA    -> dequant
-//   B ring      dequantised bf16 B tile [256 x 64], swizzled   dequant -> MMA
+//   B ring      dequantised bf16 B tile [128 x 64], swizzled   dequant -> MMA
 // Roles:
 //   warp 0      producer of the codes and scale rings;
-//   warp 1      TMEM owner and MMA issuer: per 64-wide K step, four
-//               tcgen05.mma kind::f16 M=128 N=256 K=16 into a TMEM accumulator;
+//   warp 1      TMEM owner and MMA issuer: per 64-wide K step, 2 x 4
+//               tcgen05.mma kind::f16 M=128 N=128 K=16, one per 128-row half of
+//               the x tile, both against the same B tile (every dequantised
+//               weight serves 256 rows of x);
 //   warp 2      producer of the x ring (two producers, so that neither stream
 //               waits behind the other's ring);
-//   warps 3-18  dequantisers: each thread turns 32 codes of one B row into bf16
+//   warps 3-18  dequantisers: each thread turns 16 codes of one B row into bf16
 //               per K step and writes them into the swizzled K-major layout the
 //               tensor core reads;
 //   warps 19-22 epilogue: tcgen05.ld of the accumulator, the SwiGLU epilogue,
 //               16-byte stores of bf16 hidden.
-// The B operand of one MMA stacks 128 gate rows over 128 up rows (N = 256),
-// so a single MMA stream computes both projections from one staged x tile.
+// The B operand stacks 64 gate rows over 64 up rows (N = 128), so one MMA
+// stream computes both projections from one staged x tile.
 //
 // Every mbarrier wait is bounded; a CTA that gives up raises a shared abort
 // flag so its other roles exit too, waits (bounded) for its own copies and
@@ -40,17 +42,19 @@
 namespace qsw {
 namespace {
 
-constexpr int BM = 128;   // rows of x per tile = UMMA M
+constexpr int BM = 256;   // rows of x per tile: two UMMAs (M = 128 each) share every B tile
+constexpr int UM = 128;   // UMMA M
 constexpr int BK = 64;    // K per step: one 128-byte swizzle atom of bf16
-constexpr int BN = 256;   // UMMA N (B-tile rows)
+constexpr int BN = 128;   // UMMA N (B-tile rows)
 constexpr int kDeqWarps = 16;
 constexpr int kEpiWarps = 4;
 constexpr int kWarpTma = 0, kWarpMma = 1, kWarpX = 2, kWarpDeq0 = 3, kWarpEpi0 = kWarpDeq0 + kDeqWarps;
 constexpr int kThreads = 32 * (kWarpEpi0 + kEpiWarps);   // 736
-constexpr uint32_t kTmemCols = 512;                       // two 256-column accumulators
+constexpr uint32_t kTmemCols = 512;                       // X and Y, each two 128-column accumulators
 constexpr int kMaxSmem = 232448;                          // opt-in limit per block
-constexpr int kXBytes = BM * BK * 2;                      // 16 KB
-constexpr int kBBytes = BN * BK * 2;                      // 32 KB
+constexpr int kAccCols = 2 * BN;                          // TMEM columns of X (or Y): one accumulator per x half
+constexpr int kXBytes = BM * BK * 2;                      // 32 KB
+constexpr int kBBytes = BN * BK * 2;                      // 16 KB
 constexpr int kGroupsPerEntry = 8;                        // scale groups per ring entry (16 bytes)
 constexpr int kBarBytes = 512;
 constexpr int kChainSteps = 22;                          // K steps per accumulation chain, at most
@@ -59,9 +63,9 @@ __device__ unsigned int g_prefill_error;
 
 template <int BITS0, int BITS1, bool DUAL>
 struct Cfg {
-  static constexpr int kRows0 = DUAL ? 128 : 256;   // B rows from operand 0
-  static constexpr int kRows1 = DUAL ? 128 : 0;     // B rows from operand 1
-  static constexpr int kOutCols = DUAL ? 128 : 256; // output columns per tile
+  static constexpr int kRows0 = DUAL ? 64 : 128;    // B rows from operand 0
+  static constexpr int kRows1 = DUAL ? 64 : 0;      // B rows from operand 1
+  static constexpr int kOutCols = DUAL ? 64 : 128;  // output columns per tile
   static constexpr int kC0Pitch = BK * BITS0 / 8;   // packed bytes per row per K step
   static constexpr int kC1Pitch = BK * BITS1 / 8;
   static constexpr int kC0Bytes = kRows0 * kC0Pitch;
@@ -70,10 +74,9 @@ struct Cfg {
   static constexpr int kS0Bytes = kRows0 * 2 * kGroupsPerEntry;
   static constexpr int kS1Bytes = kRows1 * 2 * kGroupsPerEntry;
   static constexpr int kEntryBytes = 2 * kS0Bytes + 2 * kS1Bytes;
-  static constexpr int kSb = 3;   // B ring
+  static constexpr int kSb = 4;   // B ring
+  static constexpr int kSx = 4;   // x ring
   static constexpr int kBudget = kMaxSmem - 1024 - kBarBytes;
-  // x ring: a fifth stage where it still leaves four codes stages
-  static constexpr int kSx = (kBudget - 5 * kXBytes - kSb * kBBytes - 2 * kEntryBytes) / kCodesBytes >= 4 ? 5 : 4;
   static constexpr int kFixed = kSx * kXBytes + kSb * kBBytes + 2 * kEntryBytes;
   static constexpr int kScFit = (kBudget - kFixed) / kCodesBytes;
   static constexpr int kSc = kScFit > 4 ? 4 : kScFit;   // codes ring
@@ -116,6 +119,11 @@ __device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
   asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
   uint16_t v;
   asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
@@ -129,39 +137,38 @@ __device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
                : "memory");
 }
 
-// 32 consecutive codes of one row (the calling thread's half of a K step) ->
-// four 16-byte chunks of bf16 weights, stored at the swizzled positions of
-// chunks 4h .. 4h+3 of B-tile row `row`.
+// 16 consecutive codes of one row (quarter q of a K step) -> two 16-byte
+// chunks of bf16 weights, stored at the swizzled positions of chunks 2q and
+// 2q+1 of B-tile row `row`.
 template <int BITS>
-__device__ __forceinline__ void dequant32(uint32_t codes_addr, uint32_t s2, uint32_t b2, uint32_t brow_addr, int row,
-                                          int h) {
-  uint32_t w[BITS];   // 32 codes = BITS words
+__device__ __forceinline__ void dequant16(uint32_t codes_addr, uint32_t s2, uint32_t b2, uint32_t brow_addr, int row,
+                                          int q) {
+  uint32_t w[BITS / 2 > 0 ? BITS / 2 : 1];   // 16 codes = BITS/2 words
   if constexpr (BITS == 2) {
+    w[0] = ld_shared_u32(codes_addr);
+  } else if constexpr (BITS == 4) {
     const uint2 v = ld_shared_v2(codes_addr);
     w[0] = v.x;
     w[1] = v.y;
   } else {
-#pragma unroll
-    for (int i = 0; i < BITS / 4; ++i) {
-      const uint4 v = ld_shared_v4(codes_addr + 16 * i);
-      w[4 * i + 0] = v.x;
-      w[4 * i + 1] = v.y;
-      w[4 * i + 2] = v.z;
-      w[4 * i + 3] = v.w;
-    }
+    const uint4 v = ld_shared_v4(codes_addr);
+    w[0] = v.x;
+    w[1] = v.y;
+    w[2] = v.z;
+    w[3] = v.w;
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {   // chunk i: codes 8i .. 8i+7 of the 32
+  for (int i = 0; i < 2; ++i) {   // chunk i: codes 8i .. 8i+7 of the 16
     uint32_t o[4];
     if constexpr (BITS == 4) {
       Dequant8<4>::natural(w[i], s2, b2, o);
     } else if constexpr (BITS == 8) {
       Dequant8<8>::natural(w[2 * i], w[2 * i + 1], s2, b2, o);
     } else {
-      Dequant8<2>::natural(w[i >> 1] >> (16 * (i & 1)), s2, b2, o);
+      Dequant8<2>::natural(w[0] >> (16 * i), s2, b2, o);
     }
     // 128-byte swizzle: 16-byte chunk c of row n lands at chunk c ^ (n mod 8)
-    const int c = 4 * h + i;
+    const int c = 2 * q + i;
     st_shared_v4(brow_addr + static_cast<uint32_t>((c ^ (row & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
   }
 }
@@ -378,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue --
     if (lane == 0) {
-      constexpr uint32_t kIdesc = umma_idesc_bf16(BM, BN);
+      constexpr uint32_t kIdesc = umma_idesc_bf16(UM, BN);
       int n_x = 0, n_b = 0;
       bool ok = true;
       // Chains of at most kChainSteps K steps (see the accumulation note at the
@@ -389,8 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int clen = (p.k_steps + nc - 1) / nc;   // K steps per chain (the last may be shorter)
       const int P = nc > 1 ? nc - 1 : 1;
       for (int lt = 0; lt < my_tiles && ok; ++lt) {
-        const uint32_t x_tmem = tmem_base + static_cast<uint32_t>((lt & 1) * BN);
-        const uint32_t y_tmem = tmem_base + static_cast<uint32_t>(((lt + 1) & 1) * BN);
+        const uint32_t x_tmem = tmem_base + static_cast<uint32_t>((lt & 1) * kAccCols);
+        const uint32_t y_tmem = tmem_base + static_cast<uint32_t>(((lt + 1) & 1) * kAccCols);
         int c = 0, cpos = 0;   // chain and K step within it
         for (int kb = 0; kb < p.k_steps; ++kb) {
           if (cpos == 0) {
@@ -426,12 +433,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = umma_desc_sw128(smem_u32(smem + C::kXOff + xs * kXBytes));
+          // the x tile's two 128-row halves (16 KB apart) against the same B tile
+          const uint64_t adesc0 = umma_desc_sw128(smem_u32(smem + C::kXOff + xs * kXBytes));
+          const uint64_t adesc1 = umma_desc_sw128(smem_u32(smem + C::kXOff + xs * kXBytes + UM * 128));
           const uint64_t bdesc = umma_desc_sw128(smem_u32(smem + C::kBOff + bs * kBBytes));
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             // +32 bytes of K per step inside the 128-byte swizzle atom
-            umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, (chain_start && kk == 0) ? 0u : 1u);
+            const uint32_t acc = (chain_start && kk == 0) ? 0u : 1u;
+            umma_bf16(d_tmem, adesc0 + 2 * kk, bdesc + 2 * kk, kIdesc, acc);
+            umma_bf16(d_tmem + BN, adesc1 + 2 * kk, bdesc + 2 * kk, kIdesc, acc);
           }
           umma_commit(&x_empty[xs]);
           umma_commit(&b_empty[bs]);
@@ -452,19 +463,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kWarpEpi0) {
     // ---------------------------------------------------------- dequantise --
-    // Warp dw owns B rows 16 dw .. 16 dw + 15; lane = (row, half): lanes 0-15
-    // take codes 0-31 of the K step, lanes 16-31 codes 32-63.  In the fused
-    // form warps 0-7 hold the gate rows and warps 8-15 the up rows.
+    // Warp dw owns B rows 8 dw .. 8 dw + 7; lane = (row, quarter): lane / 4 is
+    // the row, lane % 4 picks codes 16 q .. 16 q + 15 of the K step.  In the
+    // fused form warps 0-7 hold the gate rows and warps 8-15 the up rows.
     const int dw = warp - kWarpDeq0;
     const int op = DUAL ? (dw >= kDeqWarps / 2) : 0;   // warp-uniform
-    const int row = dw * 16 + (lane & 15);               // B-tile row
-    const int h = lane >> 4;
-    const int r_op = DUAL ? (row & 127) : row;           // row within the operand's rows
+    const int row = dw * 8 + (lane >> 2);                // B-tile row
+    const int q = lane & 3;
+    const int r_op = DUAL ? (row & (BN / 2 - 1)) : row;  // row within the operand's rows
     const int kpe = op ? kpe1 : kpe0;
     const GroupDiv gd = op ? p.gd1 : p.gd0;
     const int bits = op ? BITS1 : BITS0;
     const uint32_t c_row = static_cast<uint32_t>(C::kCOff + (op ? C::kC0Bytes : 0) +
-                                                 r_op * (op ? C::kC1Pitch : C::kC0Pitch) + h * 4 * bits);
+                                                 r_op * (op ? C::kC1Pitch : C::kC0Pitch) + q * 2 * bits);
     const uint32_t s_row = static_cast<uint32_t>(C::kSOff + (op ? 2 * C::kS0Bytes : 0) + r_op * 16);
     const uint32_t b_row = s_row + static_cast<uint32_t>(op ? C::kS1Bytes : C::kS0Bytes);
     const uint32_t sbase = smem_u32(smem);
@@ -479,17 +490,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int cs = n_c % Sc, bs = n_b % Sb;
         if (!(ok = warp_wait(&c_full[cs], (n_c / Sc) & 1, abort_flag, p.timeout_ns, err))) break;
         if (!(ok = warp_wait(&b_empty[bs], ((n_b / Sb) & 1) ^ 1u, abort_flag, p.timeout_ns, err))) break;
-        // scale and bias of this thread's 32 codes (one group: gs is a multiple of 32)
-        const uint32_t gi = gd(static_cast<uint32_t>(epos * BK + 32 * h));
+        // scale and bias of this thread's 16 codes (one group: gs is a multiple of 32)
+        const uint32_t gi = gd(static_cast<uint32_t>(epos * BK + 16 * q));
         const uint32_t eoff = static_cast<uint32_t>(es * C::kEntryBytes) + gi * 2;
         const uint32_t s2 = splat_bf16(static_cast<uint16_t>(ld_shared_u16(sbase + s_row + eoff)));
         const uint32_t b2 = splat_bf16(static_cast<uint16_t>(ld_shared_u16(sbase + b_row + eoff)));
         const uint32_t caddr = sbase + c_row + static_cast<uint32_t>(cs * C::kCodesBytes);
         const uint32_t baddr = sbase + static_cast<uint32_t>(C::kBOff + bs * kBBytes + row * 128);
         if (op == 0)
-          dequant32<BITS0>(caddr, s2, b2, baddr, row, h);
+          dequant16<BITS0>(caddr, s2, b2, baddr, row, q);
         else
-          dequant32<BITS1>(caddr, s2, b2, baddr, row, h);
+          dequant16<BITS1>(caddr, s2, b2, baddr, row, q);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -516,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int lt = 0; lt < my_tiles && ok; ++lt) {
       const int t = tile_of(lt);
-      const uint32_t tbase = lane_base + static_cast<uint32_t>((lt & 1) * BN);          // X
-      const uint32_t ybase = lane_base + static_cast<uint32_t>(((lt + 1) & 1) * BN);    // Y
+      const uint32_t tbase = lane_base + static_cast<uint32_t>((lt & 1) * kAccCols);          // X
+      const uint32_t ybase = lane_base + static_cast<uint32_t>(((lt + 1) & 1) * kAccCols);    // Y
       for (int q = 0; q < P; ++q) {
         // the epilogue idles for most of a chain: wait without spinning
         if (!(ok = warp_wait_lazy(acc_full, static_cast<uint32_t>((lt * P + q) & 1), abort_flag, p.timeout_ns, err,
@@ -529,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // chain waits for this pass, so it keeps four loads in flight per
           // wait (32 columns).
 #pragma unroll 1
-          for (int c0 = 0; c0 < BN; c0 += 32) {
+          for (int c0 = 0; c0 < kAccCols; c0 += 32) {   // both x halves' accumulators
             uint32_t ra[16], rb[16], rc[16], rd[16];
             __syncwarp();
             tmem_ld16(tbase + c0, ra);
@@ -552,38 +563,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(y_free);   // Y may take the next chain
       }
       if (!ok) break;
-      const int64_t m = static_cast<int64_t>(t % p.m_tiles) * BM + row;
       const int64_t n0 = static_cast<int64_t>(t / p.m_tiles) * C::kOutCols;
-      uint16_t *orow = p.out + m * p.N;
+      // accumulator h holds x rows m0 + 128 h + (TMEM lane); in the fused form
+      // columns 0-63 are gate, 64-127 up
 #pragma unroll 1
-      for (int c0 = 0; c0 < C::kOutCols; c0 += 16) {
-        uint32_t ra[16], rb[16];
-        __syncwarp();   // tcgen05.ld is warp-collective
-        tmem_ld16(tbase + c0, ra);
-        if (DUAL) tmem_ld16(tbase + 128 + c0, rb);
-        tmem_ld_wait();
-        if (m < p.M) {
-          uint32_t packed[8];
+      for (int h = 0; h < 2; ++h) {
+        const int64_t m = static_cast<int64_t>(t % p.m_tiles) * BM + h * UM + row;
+        uint16_t *orow = p.out + m * p.N;
+        const uint32_t hbase = tbase + static_cast<uint32_t>(h * BN);
+#pragma unroll 1
+        for (int c0 = 0; c0 < C::kOutCols; c0 += 16) {
+          uint32_t ra[16], rb[16];
+          __syncwarp();   // tcgen05.ld is warp-collective
+          tmem_ld16(hbase + c0, ra);
+          if (DUAL) tmem_ld16(hbase + BN / 2 + c0, rb);
+          tmem_ld_wait();
+          if (m < p.M) {
+            uint32_t packed[8];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            float v0, v1;
-            if (DUAL) {
-              v0 = swiglu_epilogue(p.variant, __uint_as_float(ra[e]), __uint_as_float(rb[e]));
-              v1 = swiglu_epilogue(p.variant, __uint_as_float(ra[e + 1]), __uint_as_float(rb[e + 1]));
-            } else {
-              v0 = __uint_as_float(ra[e]);
-              v1 = __uint_as_float(ra[e + 1]);
+            for (int e = 0; e < 16; e += 2) {
+              float v0, v1;
+              if (DUAL) {
+                v0 = swiglu_epilogue(p.variant, __uint_as_float(ra[e]), __uint_as_float(rb[e]));
+                v1 = swiglu_epilogue(p.variant, __uint_as_float(ra[e + 1]), __uint_as_float(rb[e + 1]));
+              } else {
+                v0 = __uint_as_float(ra[e]);
+                v1 = __uint_as_float(ra[e + 1]);
+              }
+              packed[e / 2] = pack_bf16x2(v0, v1);
             }
-            packed[e / 2] = pack_bf16x2(v0, v1);
-          }
-          const int64_t col = n0 + c0;
-          if (vec_ok && col + 16 <= p.N) {
-            st_global_v4(orow + col, make_uint4(packed[0], packed[1], packed[2], packed[3]));
-            st_global_v4(orow + col + 8, make_uint4(packed[4], packed[5], packed[6], packed[7]));
-          } else {
+            const int64_t col = n0 + c0;
+            if (vec_ok && col + 16 <= p.N) {
+              st_global_v4(orow + col, make_uint4(packed[0], packed[1], packed[2], packed[3]));
+              st_global_v4(orow + col + 8, make_uint4(packed[4], packed[5], packed[6], packed[7]));
+            } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              if (col + e < p.N) orow[col + e] = static_cast<uint16_t>(packed[e / 2] >> (16 * (e & 1)));
+              for (int e = 0; e < 16; ++e)
+                if (col + e < p.N) orow[col + e] = static_cast<uint16_t>(packed[e / 2] >> (16 * (e & 1)));
+            }
           }
         }
       }
