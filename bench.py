@@ -303,6 +303,8 @@ def bench_prefill(args, dev, stream, peaks, peak_src):
         res.update(_bench_large(args, dev, stream, peaks, peak_src))
     if args.only in ("all", "mid"):
         res.update(_bench_mid(args, dev, stream))
+    if args.only in ("all", "sweep"):
+        res.update(_bench_mixed_sweep(args, dev, stream))
     return res
 
 
@@ -360,6 +362,49 @@ def _bench_mid(args, dev, stream):
     res["mid_unfused"] = {"tflops": round(flops / pu / 1e12, 1), "us_per_call": round(pu * 1e6, 1)}
     res["mid_speedup_vs_unfused"] = round(pu / pf, 3)
     return res
+
+
+def _bench_mixed_sweep(args, dev, stream):
+    """Mixed specs (gate 4-bit gs 64, up 8-bit gs 32, H=2560, I=10240) over the M
+    sweep: both kernels where both apply, to locate the small-M / tensor-core
+    cut-over.  Weights rotate over replicas larger than L2 at small M."""
+    import torch
+    from quantized_swiglu_mlp_gb300 import inputs, ops
+
+    saved = ops.qsw_get_gemv_max_m()
+    rows = []
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    try:
+        for M in inputs.MIXED_M_SWEEP:
+            case = inputs.workload_case("mixed", M=M)
+            base = to_device(case, dev)
+            wbytes = weight_bytes(case)
+            reps = max(1, int(np.ceil(3.2 * l2 / wbytes))) if M <= 64 else 1
+            sets = [base[1:]] + [tuple(t.clone() if isinstance(t, torch.Tensor) else t for t in base[1:])
+                                 for _ in range(reps - 1)]
+            out = torch.empty((M, case.I), dtype=torch.bfloat16, device=dev)
+            entry = {"M": M}
+            for name, limit in (("small_m", 32), ("tensor_core", 0)):
+                if name == "small_m" and M > 32:
+                    continue
+                ops.qsw_set_gemv_max_m(limit)
+                steps = 200 if M <= 64 else 10
+                ms = time_graph(lambda i: ops.qswiglu_forward(base[0], *sets[i % len(sets)], variant=ops.MATCH,
+                                                              out=out, stream=stream), steps, 3, stream)
+                us = ms * 1e3 / steps
+                entry[name] = {"us": round(us, 2), "weight_GBps": round(wbytes / us / 1e3, 1),
+                               "tflops": round(4.0 * M * case.H * case.I / us / 1e6, 1)}
+            if "small_m" in entry:
+                entry["faster"] = "small_m" if entry["small_m"]["us"] < entry["tensor_core"]["us"] else "tensor_core"
+            rows.append(entry)
+            del base, sets, out
+            torch.cuda.empty_cache()
+    finally:
+        ops.qsw_set_gemv_max_m(saved)
+    ops.qsw_check_device_errors(stream)
+    small = [r["M"] for r in rows if r.get("faster") == "small_m"]
+    return {"mixed_sweep": rows, "mixed_small_m_faster_up_to": max(small) if small else 0,
+            "default_small_m_limit": saved}
 
 
 def cpu_baseline_decode(budget_s: float):
@@ -522,7 +567,7 @@ def main(argv=None):
                     help="decode calls stream their weights while the previous call finishes (library switch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--only", choices=["all", "decode", "large", "mid"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "large", "mid", "sweep"], default="all",
                     help="run one workload only (profiling); the JSON line then carries what ran")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="untimed load before the timed region, so the clock sampler sees it")
