@@ -298,7 +298,9 @@ def bench_prefill(args, dev, stream, peaks, peak_src):
     import torch
     from quantized_swiglu_mlp_gb300 import inputs, ops
 
-    res = {}
+    ops.qsw_set_stream_k({"off": ops.STREAM_K_OFF, "auto": ops.STREAM_K_AUTO,
+                          "always": ops.STREAM_K_ALWAYS}[args.stream_k])
+    res = {"stream_k": args.stream_k}
     if args.only in ("all", "large"):
         res.update(_bench_large(args, dev, stream, peaks, peak_src))
     if args.only in ("all", "mid"):
@@ -348,6 +350,9 @@ def _bench_mid(args, dev, stream):
     flops = 4.0 * case.M * case.H * case.I
     ms_f = time_graph(lambda i: ops.qswiglu_forward(*a, variant=ops.MATCH, out=out, stream=stream),
                       args.prefill_steps, 3, stream)
+    # the same call scheduled as whole tiles (no stream-K workspace)
+    ms_w = time_graph(lambda i: ops.qswiglu_forward(*a, variant=ops.MATCH, out=out, stream=stream,
+                                                    workspace=None), args.prefill_steps, 3, stream)
     x, wg, sg, bg, gsg, btg, wu, su, bu, gsu, btu = a
 
     def unfused(i):
@@ -359,6 +364,8 @@ def _bench_mid(args, dev, stream):
     ops.qsw_check_device_errors(stream)
     pf, pu = ms_f / 1e3 / args.prefill_steps, ms_u / 1e3 / args.prefill_steps
     res["mid_fused"] = {"tflops": round(flops / pf / 1e12, 1), "us_per_call": round(pf * 1e6, 1)}
+    pw = ms_w / 1e3 / args.prefill_steps
+    res["mid_fused_whole_tiles"] = {"tflops": round(flops / pw / 1e12, 1), "us_per_call": round(pw * 1e6, 1)}
     res["mid_unfused"] = {"tflops": round(flops / pu / 1e12, 1), "us_per_call": round(pu * 1e6, 1)}
     res["mid_speedup_vs_unfused"] = round(pu / pf, 3)
     return res
@@ -565,6 +572,8 @@ def main(argv=None):
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--early-weights", type=int, choices=[0, 1], default=1,
                     help="decode calls stream their weights while the previous call finishes (library switch)")
+    ap.add_argument("--stream-k", choices=["off", "auto", "always"], default="auto",
+                    help="stream-K scheduling of the tensor-core kernel (library switch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--only", choices=["all", "decode", "large", "mid", "sweep"], default="all",

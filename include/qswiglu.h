@@ -41,6 +41,7 @@
 #ifndef QSWIGLU_H_
 #define QSWIGLU_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #if defined(__GNUC__)
@@ -109,6 +110,55 @@ QSW_API qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t 
 QSW_API qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N,
                       const uint32_t *w, const void *s, const void *b,
                       int gs, int bits, void *y, void *stream);
+
+/* Stream-K scheduling of the tensor-core kernel (qsw_set_stream_k). */
+typedef enum {
+    QSW_STREAM_K_OFF = 0,     /* whole output tiles, round-robin over the SMs */
+    QSW_STREAM_K_AUTO = 1,    /* split K ranges where whole tiles would leave SMs idle (default) */
+    QSW_STREAM_K_ALWAYS = 2   /* split whenever the tile count is not a multiple of the SM count */
+} qsw_stream_k_mode;
+
+/*
+ * Bytes of workspace the *_ws entry points need on the current device
+ * (a 1 KB header plus a 128 KB f32 partial accumulator per SM; 0 when no
+ * device is current).
+ */
+QSW_API size_t qsw_workspace_bytes(void);
+
+/*
+ * qswiglu_forward / affine_qmm with a caller-owned device workspace that lets
+ * the tensor-core kernel split the K range of output tiles between SMs
+ * (stream-K) when whole tiles would fill the SMs unevenly -- e.g. 256 tiles on
+ * 152 SMs.  A split tile is finished by the CTA holding its first K steps,
+ * which adds the f32 partial accumulators that the others publish in the
+ * workspace before the epilogue; results are the same function as the plain
+ * entry points (f32 sums in a different order).
+ *   workspace        device pointer, 256-byte aligned, zero-filled before its
+ *                    first use (e.g. cudaMemsetAsync); the library keeps a
+ *                    launch counter in it, so reuse it as is afterwards.  It
+ *                    may be shared by the calls of one stream, not by calls
+ *                    that can run concurrently.  NULL: whole tiles only.
+ *   workspace_bytes  its size; less than qsw_workspace_bytes() returns
+ *                    QSW_ERR_INVALID_ARG.
+ * The small-M kernel does not use the workspace.  Other arguments, return
+ * values and error behaviour as for the plain entry points.
+ */
+QSW_API qsw_status qswiglu_forward_ws(const void *x, int64_t M, int64_t H, int64_t I,
+                           const uint32_t *wg, const void *sg, const void *bg,
+                           int gs_g, int bits_g,
+                           const uint32_t *wu, const void *su, const void *bu,
+                           int gs_u, int bits_u,
+                           int variant, void *out, void *workspace, size_t workspace_bytes,
+                           void *stream);
+QSW_API qsw_status affine_qmm_ws(const void *x, int64_t M, int64_t K, int64_t N,
+                      const uint32_t *w, const void *s, const void *b,
+                      int gs, int bits, void *y, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/* Stream-K mode of the *_ws entry points (qsw_stream_k_mode, default
+ * QSW_STREAM_K_AUTO; other values are ignored).  Process-wide. */
+QSW_API void qsw_set_stream_k(int mode);
+QSW_API int qsw_get_stream_k(void);
 
 /*
  * Elementwise out[i] = silu(g[i]) * u[i] over n bf16 values, the last step of

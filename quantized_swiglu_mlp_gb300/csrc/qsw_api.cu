@@ -23,6 +23,7 @@ std::atomic<uint64_t> g_counters[QSW_NUM_COUNTERS];
 std::atomic<int> g_gemv_max_m{-1};   // -1: not yet initialised
 std::atomic<uint64_t> g_timeout_ns{4000000000ull};
 std::atomic<int> g_early_weights{0};
+std::atomic<int> g_stream_k{QSW_STREAM_K_AUTO};
 
 int gemv_max_m() {
   int v = g_gemv_max_m.load(std::memory_order_relaxed);
@@ -79,15 +80,31 @@ qsw_status check_shape(int64_t M, int64_t K, int64_t N) {
 
 qsw_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QSW_OK : QSW_ERR_CUDA; }
 
+// A workspace is optional; if given it must be aligned and large enough.
+qsw_status check_workspace(const void *ws, size_t bytes, qsw::SplitWorkspace *out) {
+  out->ptr = nullptr;
+  out->bytes = 0;
+  out->mode = g_stream_k.load(std::memory_order_relaxed);
+  if (!ws) return QSW_OK;
+  if (!aligned(ws, 256)) return QSW_ERR_UNSUPPORTED;
+  if (bytes < qsw::prefill_workspace_bytes(sm_count())) return QSW_ERR_INVALID_ARG;
+  out->ptr = const_cast<void *>(ws);
+  out->bytes = bytes;
+  return QSW_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
-qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
-                           const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su, const void *bu,
-                           int gs_u, int bits_u, int variant, void *out, void *stream) {
+qsw_status qswiglu_forward_ws(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
+                              const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su,
+                              const void *bu, int gs_u, int bits_u, int variant, void *out, void *workspace,
+                              size_t workspace_bytes, void *stream) {
   qsw_status st = check_shape(M, H, I);
   if (st != QSW_OK) return st;
+  qsw::SplitWorkspace ws;
+  if ((st = check_workspace(workspace, workspace_bytes, &ws)) != QSW_OK) return st;
   if (variant < QSW_MATCH || variant > QSW_DEBUG_UP) return QSW_ERR_INVALID_ARG;
   if ((st = check_operand(wg, sg, bg, H, gs_g, bits_g)) != QSW_OK) return st;
   if ((st = check_operand(wu, su, bu, H, gs_u, bits_u)) != QSW_OK) return st;
@@ -103,16 +120,26 @@ qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const
                                     g_early_weights.load(std::memory_order_relaxed) != 0));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
-    st = from_cuda(qsw::launch_prefill(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count()));
+    st = from_cuda(qsw::launch_prefill(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count(), ws));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_TC].fetch_add(1, std::memory_order_relaxed);
   }
   return st;
 }
 
-qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
-                      const void *b, int gs, int bits, void *y, void *stream) {
+qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
+                           const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su, const void *bu,
+                           int gs_u, int bits_u, int variant, void *out, void *stream) {
+  return qswiglu_forward_ws(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, out, nullptr, 0,
+                            stream);
+}
+
+qsw_status affine_qmm_ws(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
+                         const void *b, int gs, int bits, void *y, void *workspace, size_t workspace_bytes,
+                         void *stream) {
   qsw_status st = check_shape(M, K, N);
   if (st != QSW_OK) return st;
+  qsw::SplitWorkspace ws;
+  if ((st = check_workspace(workspace, workspace_bytes, &ws)) != QSW_OK) return st;
   if ((st = check_operand(w, s, b, K, gs, bits)) != QSW_OK) return st;
   if (M == 0) return QSW_OK;   // nothing to read or write: x and y may be null
   if (!x || !y) return QSW_ERR_INVALID_ARG;
@@ -126,11 +153,24 @@ qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N, const uint
     if (st == QSW_OK) g_counters[QSW_CNT_QMM_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
     st = from_cuda(qsw::launch_prefill(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs, g_timeout_ns.load(),
-                                       sm_count()));
+                                       sm_count(), ws));
     if (st == QSW_OK) g_counters[QSW_CNT_QMM_TC].fetch_add(1, std::memory_order_relaxed);
   }
   return st;
 }
+
+qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
+                      const void *b, int gs, int bits, void *y, void *stream) {
+  return affine_qmm_ws(x, M, K, N, w, s, b, gs, bits, y, nullptr, 0, stream);
+}
+
+size_t qsw_workspace_bytes(void) { return qsw::prefill_workspace_bytes(sm_count()); }
+
+void qsw_set_stream_k(int mode) {
+  if (mode >= QSW_STREAM_K_OFF && mode <= QSW_STREAM_K_ALWAYS) g_stream_k.store(mode);
+}
+
+int qsw_get_stream_k(void) { return g_stream_k.load(); }
 
 qsw_status qsw_silu_mul(const void *g, const void *u, int64_t n, int variant, void *out, void *stream) {
   if (n < 0) return QSW_ERR_INVALID_ARG;
@@ -185,6 +225,6 @@ const char *qsw_status_string(qsw_status s) {
   }
 }
 
-int qsw_version(void) { return 101; }
+int qsw_version(void) { return 102; }
 
 }  // extern "C"

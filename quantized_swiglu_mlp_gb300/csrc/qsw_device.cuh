@@ -299,6 +299,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return d;
 }
 __device__ __forceinline__ uint32_t splat_bf16(uint16_t v) { return static_cast<uint32_t>(v) * 0x00010001u; }
+// Lane-wise bf16 product, correctly rounded (nearest even).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float bf16x2_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16x2_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
 // bf16 value 128 in both halves; (0x4300 | q) is the bf16 value 128 + q for q < 128.
 constexpr uint32_t kBf16x2_128 = 0x43004300u;
@@ -417,19 +425,35 @@ enum : int { VAR_MATCH = 0, VAR_F32 = 1, VAR_DEBUG_GATE = 2, VAR_DEBUG_UP = 3 };
 
 __device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
+// sigma(v) = 1 / (1 + e^-v) with the hardware exponential and reciprocal
+// approximations: branch-free, so an epilogue thread overlaps the 16 elements
+// it holds.  Their few-ulp f32 error is far below the bf16 rounding that
+// follows; for v < -88 the denominator overflows and sigma is 0 (the true value
+// is below 2^-126).
+__device__ __forceinline__ float sigmoid_fast(float v) { return __fdividef(1.0f, 1.0f + __expf(-v)); }
+
 // hidden = silu(g) * u for one element, from the f32 projections.
 __device__ __forceinline__ float swiglu_epilogue(int variant, float g, float u) {
   if (variant == VAR_MATCH) {
     const float gb = round_bf16(g), ub = round_bf16(u);
-    const float sig = round_bf16(1.0f / (1.0f + expf(-gb)));
+    const float sig = round_bf16(sigmoid_fast(gb));
     const float silu = round_bf16(gb * sig);
     return silu * ub;   // exact product of two bf16; rounded once by the caller's store
   }
-  if (variant == VAR_F32) {
-    const float sig = 1.0f / (1.0f + expf(-g));
-    return (g * sig) * u;
-  }
+  if (variant == VAR_F32) return (g * sigmoid_fast(g)) * u;
   return variant == VAR_DEBUG_GATE ? g : u;
+}
+
+// The MATCH epilogue of two elements at once, (g0, u0) in the low half of the
+// result and (g1, u1) in the high half: the same roundings as
+// swiglu_epilogue(VAR_MATCH) followed by the store's rounding, since a product
+// of two bf16 values is exact in f32 and mul.rn.bf16x2 rounds that exact
+// product to nearest even.  Bit-identical to the scalar form, in about half
+// the instructions.
+__device__ __forceinline__ uint32_t swiglu_match2(float g0, float g1, float u0, float u1) {
+  const uint32_t gb = pack_bf16x2(g0, g1), ub = pack_bf16x2(u0, u1);
+  const uint32_t sig = pack_bf16x2(sigmoid_fast(bf16x2_lo(gb)), sigmoid_fast(bf16x2_hi(gb)));
+  return bf16x2_mul(bf16x2_mul(gb, sig), ub);
 }
 
 }  // namespace qsw

@@ -11,7 +11,10 @@ namespace {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// Two elements; MATCH takes the paired form the tensor-core epilogue uses, the
+// tail kernel below the scalar form (the two are bit-identical).
 __device__ __forceinline__ uint32_t silu_mul_pair(int variant, uint32_t g, uint32_t u) {
+  if (variant == VAR_MATCH) return swiglu_match2(bf16_lo(g), bf16_hi(g), bf16_lo(u), bf16_hi(u));
   return pack_bf16x2(swiglu_epilogue(variant, bf16_lo(g), bf16_lo(u)),
                      swiglu_epilogue(variant, bf16_hi(g), bf16_hi(u)));
 }

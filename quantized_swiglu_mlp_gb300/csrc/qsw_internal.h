@@ -3,7 +3,10 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
+
+#include "qswiglu.h"
 
 namespace qsw {
 
@@ -30,10 +33,20 @@ cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const Qu
 // kernel serves every M).
 bool gemv_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const QuantOperand *op1, int num_sms);
 
+// Stream-K workspace of the tensor-core kernel: null ptr (or fewer than
+// prefill_workspace_bytes() bytes) means whole tiles only.
+struct SplitWorkspace {
+  void *ptr;
+  size_t bytes;
+  int mode;   // qsw_stream_k_mode
+};
+
+size_t prefill_workspace_bytes(int num_sms);
+
 // Tensor-core kernel (tcgen05 + TMA), any M.
 cudaError_t launch_prefill(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                            const QuantOperand *op1, int variant, void *out, cudaStream_t stream,
-                           uint64_t timeout_ns, int num_sms);
+                           uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws);
 
 cudaError_t launch_silu_mul(const void *g, const void *u, int64_t n, int variant, void *out,
                             cudaStream_t stream);

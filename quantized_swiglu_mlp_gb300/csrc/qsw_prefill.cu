@@ -58,6 +58,7 @@ constexpr int kBBytes = BN * BK * 2;                      // 16 KB
 constexpr int kGroupsPerEntry = 8;                        // scale groups per ring entry (16 bytes)
 constexpr int kBarBytes = 512;
 constexpr int kChainSteps = 22;                          // K steps per accumulation chain, at most
+constexpr int kPartFloats = 2 * UM * BN;                  // f32 partial accumulator of one split tile (128 KB)
 
 __device__ unsigned int g_prefill_error;
 
@@ -102,8 +103,100 @@ struct PrefillParams {
   int variant;
   uint16_t *out;
   int m_tiles, num_tiles, k_steps;
+  int sk_tiles;              // tiles [0, sk_tiles) are shared out stream-K style (0: none)
+  float *ws_part;            // [grid][kPartFloats] partial accumulators of split tiles
+  unsigned int *ws_ctrl;     // [0] launch epoch, [1] CTAs done in this launch
+  unsigned int *ws_flags;    // [grid][4] epoch tag per epilogue warp: that warp's partial rows are written
   uint64_t timeout_ns;
 };
+
+// Work list of one CTA: segments, each a K range [kb0, kb1) of one output tile.
+// Tiles [0, sk_tiles) are shared out stream-K style: their (tile, K step)
+// units are cut into one contiguous, equal range per CTA, so a tile can be
+// split between CTAs with neighbouring ranges; the other tiles go round-robin,
+// whole, after them.  Ranges are handed out in reverse block order: the CTA
+// that finishes a split tile (the one holding its K steps from 0, which it
+// reaches last) waits only for CTAs with lower block indices, which start
+// first.  A CTA's first segment may start inside a tile (it then contributes a
+// partial accumulator); only its last stream-K segment may end inside one (it
+// then finishes the tile).
+struct Seg {
+  int tile, kb0, kb1;
+};
+
+struct Sched {
+  int64_t u1;        // end of this CTA's stream-K units
+  int tile0, kbf;    // tile and K step of its first unit
+  int n_sk, n_seg;   // stream-K segments, all segments
+  __device__ __forceinline__ void init(const PrefillParams &p) {
+    const int64_t G = gridDim.x, rev = G - 1 - blockIdx.x;
+    const int64_t U = static_cast<int64_t>(p.sk_tiles) * p.k_steps;
+    const int64_t u0 = U * rev / G;
+    u1 = U * (rev + 1) / G;
+    tile0 = static_cast<int>(u0 / p.k_steps);
+    kbf = static_cast<int>(u0 - static_cast<int64_t>(tile0) * p.k_steps);
+    n_sk = u1 > u0 ? static_cast<int>((u1 - 1) / p.k_steps) - tile0 + 1 : 0;
+    const int dp = p.num_tiles - p.sk_tiles;   // whole tiles, round-robin
+    n_seg = n_sk + (dp - static_cast<int>(blockIdx.x) + static_cast<int>(G) - 1) / static_cast<int>(G);
+  }
+  __device__ __forceinline__ Seg seg(int ls, const PrefillParams &p) const {
+    if (ls < n_sk) {
+      const int t = tile0 + ls;
+      const int64_t hi = u1 - static_cast<int64_t>(t) * p.k_steps;
+      return {t, ls == 0 ? kbf : 0, hi < p.k_steps ? static_cast<int>(hi) : p.k_steps};
+    }
+    return {p.sk_tiles + static_cast<int>(blockIdx.x) + (ls - n_sk) * static_cast<int>(gridDim.x), 0, p.k_steps};
+  }
+};
+
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned int *p, unsigned int v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned int atom_add_acq_rel_gpu(unsigned int *p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ uint4 ld_global_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+// Wait (every lane of the warp) until another CTA has published `tag` in
+// `flag`.  Bounded like the mbarrier waits; the result is warp-uniform.
+__device__ __forceinline__ bool flag_wait(const unsigned int *flag, unsigned int tag, volatile int *abort,
+                                          uint64_t timeout_ns, unsigned int *err) {
+  bool ok = true;
+  if (ld_acquire_gpu(flag) != tag) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+      __nanosleep(128);
+      if (ld_acquire_gpu(flag) == tag) break;
+      if ((it & 15u) == 0) {
+        if (*abort) {
+          ok = false;
+          break;
+        }
+        if (globaltimer_ns() - t0 > timeout_ns) {
+          *abort = 1;
+          atomicOr(err, DEVERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -173,6 +266,20 @@ __device__ __forceinline__ void dequant16(uint32_t codes_addr, uint32_t s2, uint
   }
 }
 
+// SwiGLU epilogue of 16 (gate, up) accumulator pairs -> 8 packed bf16 pairs.
+template <int VARIANT>
+__device__ __forceinline__ void epilogue16(const uint32_t (&g)[16], const uint32_t (&u)[16], uint32_t (&out)[8]) {
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    if (VARIANT == VAR_MATCH)
+      out[e / 2] = swiglu_match2(__uint_as_float(g[e]), __uint_as_float(g[e + 1]), __uint_as_float(u[e]),
+                                 __uint_as_float(u[e + 1]));
+    else
+      out[e / 2] = pack_bf16x2(swiglu_epilogue(VARIANT, __uint_as_float(g[e]), __uint_as_float(u[e])),
+                               swiglu_epilogue(VARIANT, __uint_as_float(g[e + 1]), __uint_as_float(u[e + 1])));
+  }
+}
+
 template <int BITS0, int BITS1, bool DUAL>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c0,
@@ -206,13 +313,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t *mma_done = acc_full + 3;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  unsigned int *sk_tag_slot = reinterpret_cast<unsigned int *>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   unsigned int *err = &g_prefill_error;
-  const int my_tiles = (p.num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                       static_cast<int>(gridDim.x);
-  auto tile_of = [&](int i) { return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x); };
+  Sched S;
+  S.init(p);
   // K steps per scale-ring entry of each operand (8 groups of gs codes)
   const int kpe0 = kGroupsPerEntry * p.gd0.gs / BK;
   const int kpe1 = kGroupsPerEntry * p.gd1.gs / BK;
@@ -239,6 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(xacc_free, kEpiWarps);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
+    // this launch's tag for the split-tile flags: one more than the last
+    // launch's (set by that launch's last CTA; never 0, the zero-filled state)
+    unsigned int tag = 0;
+    if (p.sk_tiles > 0) {
+      tag = ld_acquire_gpu(p.ws_ctrl) + 1u;
+      if (tag == 0) tag = 1;
+    }
+    *sk_tag_slot = tag;
     fence_mbar_init();
   }
   if (warp == kWarpTma && lane == 0) {
@@ -265,37 +380,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const unsigned int sk_tag = *sk_tag_slot;
 
   if (warp == kWarpTma) {
     // ------------------------------------------- codes and scale producer --
-    // Warp-wide loop; lane 0 issues the TMA copies.  Sequence index j runs
-    // over (tile, K step) pairs of this CTA; at step j the codes (and scale
-    // entries) of j are requested.
-    // Every step of this loop is on the critical path of the whole CTA, so it
-    // keeps running positions instead of dividing: (t_c, kb_c) for the codes
-    // stream, and per operand the entry index and position of the K step
-    // inside its scale entry.
-    const int steps = my_tiles * p.k_steps;
+    // Warp-wide loop over this CTA's segments and their K steps; lane 0 issues
+    // the TMA copies: the codes of every K step, and a scale entry (8 groups
+    // per operand) wherever one starts -- at an entry boundary or at the
+    // first K step of a segment.  Every step of this loop is on the critical
+    // path of the whole CTA, so it keeps running positions instead of
+    // dividing per K step.
     int n_c = 0;               // codes fills issued so far
     int n_e[2] = {0, 0};       // scale entries issued per operand
-    int t_c = blockIdx.x, kb_c = 0, n0_c = (t_c / p.m_tiles) * C::kOutCols;
-    int epos[2] = {0, 0}, eidx[2] = {0, 0};
     bool ok = true;
-    for (int j = 0; j < steps && ok; ++j) {
-      {
+    for (int ls = 0; ls < S.n_seg && ok; ++ls) {
+      const Seg sg = S.seg(ls, p);
+      const int n0_c = (sg.tile / p.m_tiles) * C::kOutCols;
+      int epos[2], eidx[2];    // K step within the current entry, next entry index
+      epos[0] = sg.kb0 % kpe0;
+      eidx[0] = sg.kb0 / kpe0;
+      epos[1] = DUAL ? sg.kb0 % kpe1 : 0;
+      eidx[1] = DUAL ? sg.kb0 / kpe1 : 0;
+      for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
         const int cs = n_c % Sc;
         if (!(ok = warp_wait(&c_empty[cs], ((n_c / Sc) & 1) ^ 1u, abort_flag, p.timeout_ns, err))) break;
         if (lane == 0) {
           uint8_t *dst = smem + C::kCOff + cs * C::kCodesBytes;
           mbar_arrive_expect_tx(&c_full[cs], C::kCodesBytes);
-          tma_load_2d(dst, &tm_c0, &c_full[cs], kb_c * BK * BITS0 / 32, n0_c);
-          if (DUAL) tma_load_2d(dst + C::kC0Bytes, &tm_c1, &c_full[cs], kb_c * BK * BITS1 / 32, n0_c);
+          tma_load_2d(dst, &tm_c0, &c_full[cs], kb * BK * BITS0 / 32, n0_c);
+          if (DUAL) tma_load_2d(dst + C::kC0Bytes, &tm_c1, &c_full[cs], kb * BK * BITS1 / 32, n0_c);
         }
         ++n_c;
 #pragma unroll
         for (int op = 0; op < kOps; ++op) {
           const int kpe = op ? kpe1 : kpe0;
-          const bool start = epos[op] == 0;
+          const bool start = epos[op] == 0 || kb == sg.kb0;
           if (++epos[op] == kpe) epos[op] = 0;
           if (!start) continue;
           const int es = n_e[op] & 1;
@@ -314,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             // rows whose scale rows cannot be TMA-staged: plain loads
-            const uint16_t *sg = op ? p.s1 : p.s0;
-            const uint16_t *bg = op ? p.b1 : p.b0;
+            const uint16_t *sgp = op ? p.s1 : p.s0;
+            const uint16_t *bgp = op ? p.b1 : p.b0;
             const int ng = op ? p.ng1 : p.ng0;
             for (int idx = lane; idx < rows * kGroupsPerEntry; idx += 32) {
               const int r = idx / kGroupsPerEntry, gi = idx % kGroupsPerEntry;
@@ -323,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int g = g0 + gi;
               uint16_t sv = 0, bv = 0;
               if (row < p.N && g < ng) {
-                sv = __ldg(sg + row * ng + g);
-                bv = __ldg(bg + row * ng + g);
+                sv = __ldg(sgp + row * ng + g);
+                bv = __ldg(bgp + row * ng + g);
               }
               st_shared_u16(smem_u32(sdst) + idx * 2, sv);
               st_shared_u16(smem_u32(bdst) + idx * 2, bv);
@@ -335,13 +454,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++n_e[op];
         }
         if (!ok) break;
-        if (++kb_c == p.k_steps) {   // next tile of the codes stream
-          kb_c = 0;
-          t_c += gridDim.x;
-          n0_c = (t_c / p.m_tiles) * C::kOutCols;
-          epos[0] = epos[1] = 0;
-          eidx[0] = eidx[1] = 0;
-        }
       }
     }
     if (!ok && lane == 0) {
@@ -360,9 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int n_x = 0;
       bool ok = true;
-      for (int lt = 0; lt < my_tiles && ok; ++lt) {
-        const int m0 = (tile_of(lt) % p.m_tiles) * BM;
-        for (int kb = 0; kb < p.k_steps; ++kb) {
+      for (int ls = 0; ls < S.n_seg && ok; ++ls) {
+        const Seg sg = S.seg(ls, p);
+        const int m0 = (sg.tile % p.m_tiles) * BM;
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const int xs = n_x % Sx;
           if (!mbar_wait(&x_empty[xs], ((n_x / Sx) & 1) ^ 1u, abort_flag, p.timeout_ns, err)) {
             ok = false;
@@ -390,31 +503,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       // Chains of at most kChainSteps K steps (see the accumulation note at the
       // barriers): chain 0 accumulates in X, chains 1.. in Y, and the epilogue
-      // adds Y into X after each of them.  Completions counted per barrier:
-      // y_free P per tile, xacc_free 1 per tile, acc_full P per tile.
-      const int nc = (p.k_steps + kChainSteps - 1) / kChainSteps;
-      const int clen = (p.k_steps + nc - 1) / nc;   // K steps per chain (the last may be shorter)
-      const int P = nc > 1 ? nc - 1 : 1;
-      for (int lt = 0; lt < my_tiles && ok; ++lt) {
-        const uint32_t x_tmem = tmem_base + static_cast<uint32_t>((lt & 1) * kAccCols);
-        const uint32_t y_tmem = tmem_base + static_cast<uint32_t>(((lt + 1) & 1) * kAccCols);
+      // adds Y into X after each of them.  Completions per segment: y_free and
+      // acc_full P each, xacc_free 1; y_base counts the y_free completions of
+      // the earlier segments.
+      int y_base = 0;
+      for (int ls = 0; ls < S.n_seg && ok; ++ls) {
+        const Seg sg = S.seg(ls, p);
+        const int L = sg.kb1 - sg.kb0;
+        const int nc = (L + kChainSteps - 1) / kChainSteps;
+        const int clen = (L + nc - 1) / nc;   // K steps per chain (the last may be shorter)
+        const int P = nc > 1 ? nc - 1 : 1;
+        const uint32_t x_tmem = tmem_base + static_cast<uint32_t>((ls & 1) * kAccCols);
+        const uint32_t y_tmem = tmem_base + static_cast<uint32_t>(((ls + 1) & 1) * kAccCols);
         int c = 0, cpos = 0;   // chain and K step within it
-        for (int kb = 0; kb < p.k_steps; ++kb) {
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (cpos == 0) {
-            // X of this tile was Y of the previous one, and Y was its X:
-            // chain 0 needs the previous tile's last X += Y done, chain 1 the
-            // previous tile's X read out, chain c >= 2 the X += Y of chain c-1
+            // X of this segment was Y of the previous one, and Y was its X:
+            // chain 0 needs the previous segment's last X += Y done, chain 1
+            // the previous segment's X read out, chain c >= 2 the X += Y of
+            // chain c-1
             uint64_t *bar = nullptr;
             int n = 0;
-            if (c == 0 && lt > 0) {
+            if (c == 0 && ls > 0) {
               bar = y_free;
-              n = lt * P - 1;
-            } else if (c == 1 && lt > 0) {
+              n = y_base - 1;
+            } else if (c == 1 && ls > 0) {
               bar = xacc_free;
-              n = lt - 1;
+              n = ls - 1;
             } else if (c >= 2) {
               bar = y_free;
-              n = lt * P + c - 2;
+              n = y_base + c - 2;
             }
             if (bar != nullptr) {
               if (!mbar_wait(bar, static_cast<uint32_t>(n & 1), abort_flag, p.timeout_ns, err)) {
@@ -448,12 +566,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&b_empty[bs]);
           ++n_x;
           ++n_b;
-          if (++cpos == clen || kb + 1 == p.k_steps) {   // chain c complete
+          if (++cpos == clen || kb + 1 == sg.kb1) {   // chain c complete
             if (c >= 1 || nc == 1) umma_commit(acc_full);
             ++c;
             cpos = 0;
           }
         }
+        y_base += P;
       }
       if (!ok) {
         umma_commit(mma_done);
@@ -481,11 +600,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sbase = smem_u32(smem);
     int n_c = 0, n_b = 0, n_e = 0;
     bool ok = true;
-    for (int lt = 0; lt < my_tiles && ok; ++lt) {
-      int epos = 0;   // K step within the current scale entry
-      for (int kb = 0; kb < p.k_steps; ++kb) {
+    for (int ls = 0; ls < S.n_seg && ok; ++ls) {
+      const Seg sg = S.seg(ls, p);
+      int epos = sg.kb0 % kpe;   // K step within the current scale entry
+      for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
         const int es = n_e & 1;
-        if (epos == 0 && !(ok = warp_wait(&s_full[op * 2 + es], (n_e >> 1) & 1, abort_flag, p.timeout_ns, err)))
+        // a scale entry starts at an entry boundary or at the segment's first K step
+        if ((epos == 0 || kb == sg.kb0) &&
+            !(ok = warp_wait(&s_full[op * 2 + es], (n_e >> 1) & 1, abort_flag, p.timeout_ns, err)))
           break;
         const int cs = n_c % Sc, bs = n_b % Sb;
         if (!(ok = warp_wait(&c_full[cs], (n_c / Sc) & 1, abort_flag, p.timeout_ns, err))) break;
@@ -509,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++n_c;
         ++n_b;
-        if (++epos == kpe || kb + 1 == p.k_steps) {
+        if (++epos == kpe || kb + 1 == sg.kb1) {
           if (lane == 0) mbar_arrive(&s_empty[op * 2 + es]);
           ++n_e;
           epos = 0;
@@ -521,18 +643,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;   // TMEM lanes 32*quarter .. +31
     const int row = quarter * 32 + lane;
     const bool vec_ok = (p.N % 8) == 0;
-    const int nc = (p.k_steps + kChainSteps - 1) / kChainSteps;
-    const int P = nc > 1 ? nc - 1 : 1;   // acc_full completions per tile
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     bool ok = true;
-    for (int lt = 0; lt < my_tiles && ok; ++lt) {
-      const int t = tile_of(lt);
-      const uint32_t tbase = lane_base + static_cast<uint32_t>((lt & 1) * kAccCols);          // X
-      const uint32_t ybase = lane_base + static_cast<uint32_t>(((lt + 1) & 1) * kAccCols);    // Y
+    int a_base = 0;   // acc_full completions of the earlier segments
+    for (int ls = 0; ls < S.n_seg && ok; ++ls) {
+      const Seg sg = S.seg(ls, p);
+      const int t = sg.tile;
+      const int L = sg.kb1 - sg.kb0;
+      const int nc = (L + kChainSteps - 1) / kChainSteps;
+      const int P = nc > 1 ? nc - 1 : 1;   // acc_full completions of this segment
+      const uint32_t tbase = lane_base + static_cast<uint32_t>((ls & 1) * kAccCols);          // X
+      const uint32_t ybase = lane_base + static_cast<uint32_t>(((ls + 1) & 1) * kAccCols);    // Y
       for (int q = 0; q < P; ++q) {
         // the epilogue idles for most of a chain: wait without spinning
-        if (!(ok = warp_wait_lazy(acc_full, static_cast<uint32_t>((lt * P + q) & 1), abort_flag, p.timeout_ns, err,
-                                  500)))
+        if (!(ok = warp_wait_lazy(acc_full, static_cast<uint32_t>((a_base + q) & 1), abort_flag, p.timeout_ns,
+                                  err, 500)))
           break;
         tc_fence_after();
         if (nc > 1) {
@@ -562,51 +687,121 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(y_free);   // Y may take the next chain
       }
+      a_base += P;
       if (!ok) break;
-      const int64_t n0 = static_cast<int64_t>(t / p.m_tiles) * C::kOutCols;
-      // accumulator h holds x rows m0 + 128 h + (TMEM lane); in the fused form
-      // columns 0-63 are gate, 64-127 up
+      const int64_t m_tile0 = static_cast<int64_t>(t % p.m_tiles) * BM;
+      if (sg.kb0 > 0) {
+        // Contributor: this CTA holds K steps [kb0, kb1) of a tile another CTA
+        // finishes.  Publish the f32 accumulator (rows below M) in this CTA's
+        // partial slot, laid out [half][16-column chunk][4-column quad][row][4]
+        // so that every 16-byte store (and load) of a warp covers 512
+        // contiguous bytes, then flag this warp's rows.
+        float *part = p.ws_part + static_cast<size_t>(blockIdx.x) * kPartFloats;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        const int64_t m = static_cast<int64_t>(t % p.m_tiles) * BM + h * UM + row;
-        uint16_t *orow = p.out + m * p.N;
-        const uint32_t hbase = tbase + static_cast<uint32_t>(h * BN);
+        for (int h = 0; h < 2; ++h) {
+          const bool live = m_tile0 + h * UM + row < p.M;
 #pragma unroll 1
-        for (int c0 = 0; c0 < C::kOutCols; c0 += 16) {
-          uint32_t ra[16], rb[16];
-          __syncwarp();   // tcgen05.ld is warp-collective
-          tmem_ld16(hbase + c0, ra);
-          if (DUAL) tmem_ld16(hbase + BN / 2 + c0, rb);
-          tmem_ld_wait();
-          if (m < p.M) {
-            uint32_t packed[8];
+          for (int j = 0; j < BN / 16; ++j) {
+            uint32_t ra[16];
+            __syncwarp();   // tcgen05.ld is warp-collective
+            tmem_ld16(tbase + static_cast<uint32_t>(h * BN + 16 * j), ra);
+            tmem_ld_wait();
+            if (live) {
+              float *dst = part + (static_cast<size_t>(h * (BN / 16) + j) * 4 * UM + row) * 4;
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              float v0, v1;
-              if (DUAL) {
-                v0 = swiglu_epilogue(p.variant, __uint_as_float(ra[e]), __uint_as_float(rb[e]));
-                v1 = swiglu_epilogue(p.variant, __uint_as_float(ra[e + 1]), __uint_as_float(rb[e + 1]));
-              } else {
-                v0 = __uint_as_float(ra[e]);
-                v1 = __uint_as_float(ra[e + 1]);
-              }
-              packed[e / 2] = pack_bf16x2(v0, v1);
+              for (int i = 0; i < 4; ++i)
+                st_global_v4(dst + i * UM * 4, make_uint4(ra[4 * i], ra[4 * i + 1], ra[4 * i + 2], ra[4 * i + 3]));
             }
-            const int64_t col = n0 + c0;
-            if (vec_ok && col + 16 <= p.N) {
-              st_global_v4(orow + col, make_uint4(packed[0], packed[1], packed[2], packed[3]));
-              st_global_v4(orow + col + 8, make_uint4(packed[4], packed[5], packed[6], packed[7]));
-            } else {
+          }
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(p.ws_flags + blockIdx.x * 4 + quarter, sk_tag);
+      } else {
+        // A tile that ends inside this segment's range is complete here; one
+        // that continues past kb1 is finished here with the partials of the
+        // CTAs holding its later K steps (lower block indices, in order).
+        int n_parts = 0;
+        if (sg.kb1 < p.k_steps) {
+          const int64_t G = gridDim.x, rev = G - 1 - blockIdx.x;
+          const int64_t U = static_cast<int64_t>(p.sk_tiles) * p.k_steps;
+          const int64_t tile_end = static_cast<int64_t>(t + 1) * p.k_steps;
+          for (int64_t rc = rev + 1; rc < G && U * rc / G < tile_end; ++rc) {
+            const int c = static_cast<int>(G - 1 - rc);
+            if (!(ok = flag_wait(p.ws_flags + c * 4 + quarter, sk_tag, abort_flag, p.timeout_ns, err))) break;
+            ++n_parts;
+          }
+          if (!ok) break;
+        }
+        const int64_t n0 = static_cast<int64_t>(t / p.m_tiles) * C::kOutCols;
+        // accumulator h holds x rows m0 + 128 h + (TMEM lane); in the fused form
+        // columns 0-63 are gate, 64-127 up
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          const int64_t m = m_tile0 + h * UM + row;
+          uint16_t *orow = p.out + m * p.N;
+          const uint32_t hbase = tbase + static_cast<uint32_t>(h * BN);
+#pragma unroll 1
+          for (int c0 = 0; c0 < C::kOutCols; c0 += 16) {
+            uint32_t ra[16], rb[16];
+            __syncwarp();   // tcgen05.ld is warp-collective
+            tmem_ld16(hbase + c0, ra);
+            if (DUAL) tmem_ld16(hbase + BN / 2 + c0, rb);
+            tmem_ld_wait();
+            if (m < p.M) {
+              for (int r = 1; r <= n_parts; ++r) {
+                const float *src = p.ws_part + static_cast<size_t>(blockIdx.x - r) * kPartFloats +
+                                   (static_cast<size_t>(h * (BN / 16) + c0 / 16) * 4 * UM + row) * 4;
 #pragma unroll
-              for (int e = 0; e < 16; ++e)
-                if (col + e < p.N) orow[col + e] = static_cast<uint16_t>(packed[e / 2] >> (16 * (e & 1)));
+                for (int i = 0; i < 4; ++i) {
+                  const uint4 v = ld_global_v4(src + i * UM * 4);
+                  ra[4 * i] = __float_as_uint(__uint_as_float(ra[4 * i]) + __uint_as_float(v.x));
+                  ra[4 * i + 1] = __float_as_uint(__uint_as_float(ra[4 * i + 1]) + __uint_as_float(v.y));
+                  ra[4 * i + 2] = __float_as_uint(__uint_as_float(ra[4 * i + 2]) + __uint_as_float(v.z));
+                  ra[4 * i + 3] = __float_as_uint(__uint_as_float(ra[4 * i + 3]) + __uint_as_float(v.w));
+                }
+                if (DUAL) {
+                  const float *usrc = src + static_cast<size_t>(BN / 2 / 16) * 4 * UM * 4;   // up chunk
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    const uint4 v = ld_global_v4(usrc + i * UM * 4);
+                    rb[4 * i] = __float_as_uint(__uint_as_float(rb[4 * i]) + __uint_as_float(v.x));
+                    rb[4 * i + 1] = __float_as_uint(__uint_as_float(rb[4 * i + 1]) + __uint_as_float(v.y));
+                    rb[4 * i + 2] = __float_as_uint(__uint_as_float(rb[4 * i + 2]) + __uint_as_float(v.z));
+                    rb[4 * i + 3] = __float_as_uint(__uint_as_float(rb[4 * i + 3]) + __uint_as_float(v.w));
+                  }
+                }
+              }
+              uint32_t packed[8];
+              if (DUAL) {
+                // one variant per launch: dispatch once, then 16 branch-free elements
+                switch (p.variant) {
+                  case VAR_MATCH: epilogue16<VAR_MATCH>(ra, rb, packed); break;
+                  case VAR_F32: epilogue16<VAR_F32>(ra, rb, packed); break;
+                  case VAR_DEBUG_GATE: epilogue16<VAR_DEBUG_GATE>(ra, rb, packed); break;
+                  default: epilogue16<VAR_DEBUG_UP>(ra, rb, packed); break;
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; e += 2)
+                  packed[e / 2] = pack_bf16x2(__uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
+              }
+              const int64_t col = n0 + c0;
+              if (vec_ok && col + 16 <= p.N) {
+                st_global_v4(orow + col, make_uint4(packed[0], packed[1], packed[2], packed[3]));
+                st_global_v4(orow + col + 8, make_uint4(packed[4], packed[5], packed[6], packed[7]));
+              } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  if (col + e < p.N) orow[col + e] = static_cast<uint16_t>(packed[e / 2] >> (16 * (e & 1)));
+              }
             }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(xacc_free);   // X may take the next tile's chains 1..
+      if (lane == 0) mbar_arrive(xacc_free);   // X may take the next segment's chains 1..
     }
   }
 
@@ -615,6 +810,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
+  }
+  if (p.sk_tiles > 0 && threadIdx.x == 0) {
+    // the last CTA of the launch to get here publishes its tag as the epoch the
+    // next launch counts on from (every CTA read the epoch before arriving)
+    if (atom_add_acq_rel_gpu(p.ws_ctrl + 1, 1u) == gridDim.x - 1) {
+      *reinterpret_cast<volatile unsigned int *>(p.ws_ctrl + 1) = 0u;
+      st_release_gpu(p.ws_ctrl, sk_tag);
+    }
   }
 }
 
@@ -666,10 +869,57 @@ bool encode_scales(CUtensorMap *s, CUtensorMap *b, const QuantOperand &op, int64
                    CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+// Workspace layout: [0] epoch, [1] CTAs done; flags from byte 256 (4 per CTA);
+// partial accumulators from a 1 KB boundary, kPartFloats per CTA.
+constexpr size_t kFlagsOff = 256;
+size_t header_bytes(int num_sms) { return (kFlagsOff + 16 * static_cast<size_t>(num_sms) + 1023) & ~size_t(1023); }
+
+// Stream-K split.  With at least as many tiles as SMs, the ragged last wave
+// (rem = tiles mod SMs tiles) is shared out in equal K ranges first and the
+// whole waves follow, so a finisher's partial reads and its epilogue overlap
+// the MMAs of its next whole tile.  Where the ragged wave alone would give each
+// CTA less than half a tile of K steps, one whole wave joins the split (ranges
+// of at least one tile).  With fewer tiles than SMs all tiles are split, every
+// CTA taking at least kSkMinUnits K steps.  Auto mode splits only where whole
+// tiles would leave more than kSkMaxIdle of the SM time idle (more for fewer
+// tiles than SMs, where the finisher's epilogue cannot be hidden), and not
+// where a ragged wave of more than half the SMs is followed by fewer than
+// kSkMinWaves whole waves: there a finisher's epilogue (partial reads, then
+// the output) can hold up the second accumulation chain of its next tile by
+// more than the split saves (measured: 256 tiles of 32 K steps on 152 SMs).
+constexpr double kSkMaxIdle = 0.01;
+constexpr double kSkMaxIdleFew = 0.25;
+constexpr int64_t kSkMinUnits = 8;
+constexpr int64_t kSkMinWaves = 3;
+
+void plan_split(int64_t tiles, int64_t k_steps, int num_sms, int mode, bool have_ws, int *grid, int *sk_tiles) {
+  const int64_t G = num_sms;
+  *grid = static_cast<int>(tiles < G ? tiles : G);
+  *sk_tiles = 0;
+  if (!have_ws || mode == QSW_STREAM_K_OFF || G < 2) return;
+  const double busy = static_cast<double>(tiles) / static_cast<double>(((tiles + G - 1) / G) * G);
+  const bool auto_mode = mode == QSW_STREAM_K_AUTO;
+  if (tiles >= G) {
+    const int64_t rem = tiles % G;
+    if (rem == 0 || (auto_mode && busy >= 1.0 - kSkMaxIdle)) return;
+    if (auto_mode && 2 * rem >= G && tiles / G < kSkMinWaves) return;
+    *grid = static_cast<int>(G);
+    *sk_tiles = static_cast<int>(2 * rem >= G ? rem : rem + G);
+    return;
+  }
+  if (auto_mode && busy >= 1.0 - kSkMaxIdleFew) return;
+  const int64_t units = tiles * k_steps;
+  int64_t g = mode == QSW_STREAM_K_ALWAYS ? units : units / kSkMinUnits;
+  if (g > G) g = G;
+  if (g <= tiles) return;
+  *grid = static_cast<int>(g);
+  *sk_tiles = static_cast<int>(tiles);
+}
+
 template <int BITS0, int BITS1, bool DUAL>
 cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                         const QuantOperand *op1, int variant, void *out, cudaStream_t stream, uint64_t timeout_ns,
-                        int num_sms) {
+                        int num_sms, const SplitWorkspace &ws) {
   using C = Cfg<BITS0, BITS1, DUAL>;
   CUtensorMap tm_x, tm_c0, tm_c1, tm_s0, tm_b0, tm_s1, tm_b1;
   if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -709,6 +959,15 @@ cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   p.num_tiles = static_cast<int>(tiles);
   p.k_steps = static_cast<int>((K + BK - 1) / BK);
   p.timeout_ns = timeout_ns;
+  int grid = 0;
+  const bool have_ws = ws.ptr != nullptr && ws.bytes >= prefill_workspace_bytes(num_sms);
+  plan_split(tiles, p.k_steps, num_sms, ws.mode, have_ws, &grid, &p.sk_tiles);
+  if (p.sk_tiles > 0) {
+    uint8_t *base = static_cast<uint8_t *>(ws.ptr);
+    p.ws_ctrl = reinterpret_cast<unsigned int *>(base);
+    p.ws_flags = reinterpret_cast<unsigned int *>(base + kFlagsOff);
+    p.ws_part = reinterpret_cast<float *>(base + header_bytes(num_sms));
+  }
 
   // opt in to the large shared-memory carve-out once per device and instantiation
   static std::atomic<uint64_t> attr_done{0};
@@ -720,7 +979,6 @@ cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const Qu
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(uint64_t(1) << dev);
   }
-  const int grid = static_cast<int>(tiles < num_sms ? tiles : num_sms);
   prefill_kernel<BITS0, BITS1, DUAL><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_x, tm_c0, tm_c1, tm_s0, tm_b0,
                                                                                  tm_s1, tm_b1, p);
   return cudaGetLastError();
@@ -729,32 +987,36 @@ cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const Qu
 template <int BITS0>
 cudaError_t dual_bits1(int bits1, const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                        const QuantOperand *op1, int variant, void *out, cudaStream_t stream, uint64_t timeout_ns,
-                       int num_sms) {
+                       int num_sms, const SplitWorkspace &ws) {
   switch (bits1) {
-    case 2: return launch_impl<BITS0, 2, true>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms);
-    case 4: return launch_impl<BITS0, 4, true>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms);
-    case 8: return launch_impl<BITS0, 8, true>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms);
+    case 2: return launch_impl<BITS0, 2, true>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+    case 4: return launch_impl<BITS0, 4, true>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+    case 8: return launch_impl<BITS0, 8, true>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
     default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
+size_t prefill_workspace_bytes(int num_sms) {
+  return num_sms > 0 ? header_bytes(num_sms) + static_cast<size_t>(num_sms) * kPartFloats * sizeof(float) : 0;
+}
+
 cudaError_t launch_prefill(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                            const QuantOperand *op1, int variant, void *out, cudaStream_t stream,
-                           uint64_t timeout_ns, int num_sms) {
+                           uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws) {
   if (op1) {
     switch (op0.bits) {
-      case 2: return dual_bits1<2>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms);
-      case 4: return dual_bits1<4>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms);
-      case 8: return dual_bits1<8>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms);
+      case 2: return dual_bits1<2>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+      case 4: return dual_bits1<4>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+      case 8: return dual_bits1<8>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (op0.bits) {
-    case 2: return launch_impl<2, 2, false>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms);
-    case 4: return launch_impl<4, 4, false>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms);
-    case 8: return launch_impl<8, 8, false>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms);
+    case 2: return launch_impl<2, 2, false>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
+    case 4: return launch_impl<4, 4, false>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
+    case 8: return launch_impl<8, 8, false>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
     default: return cudaErrorInvalidValue;
   }
 }

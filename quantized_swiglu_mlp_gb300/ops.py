@@ -28,7 +28,9 @@ CNT_FUSED_TC, CNT_FUSED_GEMV, CNT_QMM_TC, CNT_QMM_GEMV, CNT_SILU_MUL = range(5)
 NUM_COUNTERS = 5
 STATUS = {0: "QSW_OK", 1: "QSW_ERR_INVALID_ARG", 2: "QSW_ERR_UNSUPPORTED", 3: "QSW_ERR_CUDA",
           4: "QSW_ERR_TIMEOUT"}
-EXPORTED = ("qswiglu_forward", "affine_qmm", "qsw_silu_mul", "qsw_check_device_errors",
+STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS = 0, 1, 2
+EXPORTED = ("qswiglu_forward", "affine_qmm", "qswiglu_forward_ws", "affine_qmm_ws", "qsw_workspace_bytes",
+            "qsw_set_stream_k", "qsw_get_stream_k", "qsw_silu_mul", "qsw_check_device_errors",
             "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_early_weight_stream",
             "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns",
             "qsw_get_counters", "qsw_reset_counters", "qsw_status_string", "qsw_version")
@@ -58,6 +60,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.qswiglu_forward.restype = i32
         lib.affine_qmm.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p]
         lib.affine_qmm.restype = i32
+        sz = ctypes.c_size_t
+        lib.qswiglu_forward_ws.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, p, p, sz, p]
+        lib.qswiglu_forward_ws.restype = i32
+        lib.affine_qmm_ws.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p, sz, p]
+        lib.affine_qmm_ws.restype = i32
+        lib.qsw_workspace_bytes.restype = sz
+        lib.qsw_set_stream_k.argtypes = [i32]
+        lib.qsw_get_stream_k.restype = i32
         lib.qsw_silu_mul.argtypes = [p, p, i64, i32, p, p]
         lib.qsw_silu_mul.restype = i32
         lib.qsw_check_device_errors.argtypes = [p]
@@ -119,9 +129,65 @@ def _operand(w, s, b, name, device, K, bits, gs):
     return rows
 
 
+_workspaces: dict = {}
+
+
+def workspace_bytes(device=None) -> int:
+    """Bytes of stream-K workspace the tensor-core kernel needs on `device`."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(load_library().qsw_workspace_bytes())
+
+
+def workspace(device=None, stream=None) -> torch.Tensor | None:
+    """The stream-K workspace used by calls on (device, stream) with workspace="auto".
+
+    Created zero-filled (and the fill completed) on first use, then kept for
+    the life of the process: one per stream, since a workspace may not be
+    shared by calls that can run concurrently.  Returns None while the current
+    stream is being captured into a CUDA graph and none exists yet (the call
+    then runs whole tiles only); make one call before capturing.
+    """
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    key = (dev.index, _stream_ptr(stream))
+    ws = _workspaces.get(key)
+    if ws is None:
+        if torch.cuda.is_current_stream_capturing():
+            return None
+        with torch.cuda.device(dev):
+            ws = torch.zeros(workspace_bytes(dev), dtype=torch.uint8, device=dev)
+            torch.cuda.current_stream(dev).synchronize()
+        _workspaces[key] = ws
+    return ws
+
+
+def _workspace_arg(ws, device, stream):
+    if isinstance(ws, str):
+        if ws != "auto":
+            raise ValueError('workspace must be "auto", None or a uint8 CUDA tensor')
+        ws = workspace(device, stream)
+    if ws is None:
+        return None, 0
+    _need(ws, "workspace", (torch.uint8,), device)
+    return ws.data_ptr(), ws.numel()
+
+
+def qsw_set_stream_k(mode: int) -> None:
+    load_library().qsw_set_stream_k(int(mode))
+
+
+def qsw_get_stream_k() -> int:
+    return int(load_library().qsw_get_stream_k())
+
+
 def qswiglu_forward(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant=MATCH,
-                    out=None, stream=None) -> torch.Tensor:
-    """hidden = silu(x . Wg^T) * (x . Wu^T) on the GPU; returns bf16 [..., I]."""
+                    out=None, stream=None, workspace="auto") -> torch.Tensor:
+    """hidden = silu(x . Wg^T) * (x . Wu^T) on the GPU; returns bf16 [..., I].
+
+    workspace: "auto" (the per-stream workspace of workspace()), None (whole
+    tiles only: the plain qswiglu_forward entry point) or a zero-initialised
+    uint8 tensor of at least workspace_bytes() bytes owned by the caller.
+    """
     lib = load_library()
     _need(x, "x", _BF16)
     H = x.shape[-1]
@@ -136,15 +202,26 @@ def qswiglu_forward(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, varia
         _need(out, "out", _BF16, x.device)
         if out.numel() != M * I:
             raise ValueError("out has the wrong size")
-    code = lib.qswiglu_forward(x2.data_ptr(), M, H, I, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(),
-                               int(gs_g), int(bits_g), wu.data_ptr(), su.data_ptr(), bu.data_ptr(),
-                               int(gs_u), int(bits_u), int(variant), out.data_ptr(), _stream_ptr(stream))
-    _check("qswiglu_forward", code)
+    ws_ptr, ws_bytes = _workspace_arg(workspace, x.device, stream)
+    if ws_ptr is None:
+        code = lib.qswiglu_forward(x2.data_ptr(), M, H, I, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(),
+                                   int(gs_g), int(bits_g), wu.data_ptr(), su.data_ptr(), bu.data_ptr(),
+                                   int(gs_u), int(bits_u), int(variant), out.data_ptr(), _stream_ptr(stream))
+        _check("qswiglu_forward", code)
+    else:
+        code = lib.qswiglu_forward_ws(x2.data_ptr(), M, H, I, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(),
+                                      int(gs_g), int(bits_g), wu.data_ptr(), su.data_ptr(), bu.data_ptr(),
+                                      int(gs_u), int(bits_u), int(variant), out.data_ptr(), ws_ptr, ws_bytes,
+                                      _stream_ptr(stream))
+        _check("qswiglu_forward_ws", code)
     return out.view(*x.shape[:-1], I)
 
 
-def affine_qmm(x, w, s, b, gs, bits, y=None, stream=None) -> torch.Tensor:
-    """y = bf16(x . W^T) with W affine-quantised; returns bf16 [..., N]."""
+def affine_qmm(x, w, s, b, gs, bits, y=None, stream=None, workspace="auto") -> torch.Tensor:
+    """y = bf16(x . W^T) with W affine-quantised; returns bf16 [..., N].
+
+    workspace: as for qswiglu_forward.
+    """
     lib = load_library()
     _need(x, "x", _BF16)
     K = x.shape[-1]
@@ -157,9 +234,15 @@ def affine_qmm(x, w, s, b, gs, bits, y=None, stream=None) -> torch.Tensor:
         _need(y, "y", _BF16, x.device)
         if y.numel() != M * N:
             raise ValueError("y has the wrong size")
-    code = lib.affine_qmm(x2.data_ptr(), M, K, N, w.data_ptr(), s.data_ptr(), b.data_ptr(),
-                          int(gs), int(bits), y.data_ptr(), _stream_ptr(stream))
-    _check("affine_qmm", code)
+    ws_ptr, ws_bytes = _workspace_arg(workspace, x.device, stream)
+    if ws_ptr is None:
+        code = lib.affine_qmm(x2.data_ptr(), M, K, N, w.data_ptr(), s.data_ptr(), b.data_ptr(),
+                              int(gs), int(bits), y.data_ptr(), _stream_ptr(stream))
+        _check("affine_qmm", code)
+    else:
+        code = lib.affine_qmm_ws(x2.data_ptr(), M, K, N, w.data_ptr(), s.data_ptr(), b.data_ptr(),
+                                 int(gs), int(bits), y.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream))
+        _check("affine_qmm_ws", code)
     return y.view(*x.shape[:-1], N)
 
 
@@ -182,10 +265,10 @@ def qsw_silu_mul(g, u, variant=MATCH, out=None, stream=None) -> torch.Tensor:
 
 
 def unfused_swiglu(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant=MATCH,
-                   stream=None) -> torch.Tensor:
+                   stream=None, workspace="auto") -> torch.Tensor:
     """The unfused comparison path: two affine_qmm calls, then silu*mul."""
-    g = affine_qmm(x, wg, sg, bg, gs_g, bits_g, stream=stream)
-    u = affine_qmm(x, wu, su, bu, gs_u, bits_u, stream=stream)
+    g = affine_qmm(x, wg, sg, bg, gs_g, bits_g, stream=stream, workspace=workspace)
+    u = affine_qmm(x, wu, su, bu, gs_u, bits_u, stream=stream, workspace=workspace)
     return qsw_silu_mul(g, u, variant, out=g, stream=stream)
 
 

@@ -135,3 +135,37 @@ def test_early_weight_stream_switch():
     finally:
         ops.qsw_set_early_weight_stream(saved)
 
+
+
+def fwd_ws(lib, ws, ws_bytes, M=4):
+    return lib.qswiglu_forward_ws(FAKE, M, 256, 64, FAKE, FAKE, FAKE, 64, 4, FAKE, FAKE, FAKE, 64, 4,
+                                  0, FAKE, ws, ws_bytes, None)
+
+
+def test_workspace_entry_points_validate_on_the_host(lib):
+    """The *_ws entry points check the workspace before anything is launched:
+    a misaligned one is unsupported, a null one means whole tiles only, and
+    argument errors are reported as for the plain entry points."""
+    assert fwd_ws(lib, FAKE + 64, 1 << 30) == UNSUPPORTED          # 256-byte alignment
+    assert fwd_ws(lib, None, 0, M=0) == OK
+    assert fwd_ws(lib, FAKE, 1 << 30, M=0) == OK
+    assert fwd_ws(lib, FAKE, 1 << 30, M=-1) == INVALID
+    assert lib.affine_qmm_ws(FAKE, 4, 256, 64, FAKE, FAKE, FAKE, 64, 4, FAKE, FAKE + 16, 1 << 30,
+                             None) == UNSUPPORTED
+    assert lib.affine_qmm_ws(FAKE, 0, 256, 64, FAKE, FAKE, FAKE, 64, 4, FAKE, FAKE, 1 << 30, None) == OK
+    # no device is current here: the size query answers 0
+    assert lib.qsw_workspace_bytes() == 0
+
+
+def test_stream_k_mode_switch(lib):
+    """Stream-K scheduling defaults to auto; out-of-range modes are ignored."""
+    saved = ops.qsw_get_stream_k()
+    try:
+        assert saved == ops.STREAM_K_AUTO
+        for mode in (ops.STREAM_K_OFF, ops.STREAM_K_ALWAYS, ops.STREAM_K_AUTO):
+            ops.qsw_set_stream_k(mode)
+            assert ops.qsw_get_stream_k() == mode
+        ops.qsw_set_stream_k(7)
+        assert ops.qsw_get_stream_k() == ops.STREAM_K_AUTO
+    finally:
+        ops.qsw_set_stream_k(saved)

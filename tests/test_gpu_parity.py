@@ -176,8 +176,10 @@ def test_fused_match_equals_unfused(dev, gemv_limit, limit):
     case = inputs.make_case(24, 1024, 264, bits_g=4, gs_g=64, bits_u=8, gs_u=32, seed=3)
     gemv_limit(limit)
     a = device_args(case, dev)
-    fused = to_bits(ops.qswiglu_forward(*a, variant=ops.MATCH))
-    unfused = to_bits(ops.unfused_swiglu(*a, variant=ops.MATCH))
+    # whole tiles: the fused and single-operand launches split K differently
+    # under stream-K scheduling, which changes the f32 summation order
+    fused = to_bits(ops.qswiglu_forward(*a, variant=ops.MATCH, workspace=None))
+    unfused = to_bits(ops.unfused_swiglu(*a, variant=ops.MATCH, workspace=None))
     ops.qsw_check_device_errors()
     if limit == 0:
         assert np.array_equal(fused, unfused)
@@ -233,6 +235,40 @@ def test_all_bf16_gate_values(dev):
     got = to_bits(ops.qsw_silu_mul(gd, ud, ops.MATCH))
     ok, info = check_match(got, oracle.silu_mul(g, u, ops.MATCH))
     assert ok, info
+
+
+def test_paired_and_scalar_match_epilogues_agree(dev):
+    """The MATCH epilogue has a paired form (two elements per bf16x2
+    instruction: tensor-core epilogue, vector silu*mul) and a scalar form
+    (small-M kernel, silu*mul tail); over every finite bf16 gate value and a
+    spread of up values the two give the same bits.  The scalar form is reached
+    through 7-element silu*mul calls (all tail), at two offsets so that every
+    element lands in one of them."""
+    h = np.arange(0, 0x10000, dtype=np.uint32)
+    g = h[np.isfinite((h << 16).view(np.float32))].astype(np.uint16)
+    n = (g.size // 8) * 8
+    g = g[:n]
+    rng = np.random.default_rng(7)
+    u = inputs.f32_to_bf16_bits(torch.from_numpy(rng.normal(0, 2, n).astype(np.float32)))
+    to_dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+    paired = to_bits(ops.qsw_silu_mul(to_dev(g), to_dev(u), ops.MATCH))
+    scalar = np.zeros(n, dtype=np.uint16)
+    seen = np.zeros(n, dtype=bool)
+    for shift in (0, 1):
+        gd, ud = to_dev(np.roll(g, -shift)), to_dev(np.roll(u, -shift))
+        out = torch.zeros_like(gd)
+        for k in range(0, n - 7, 8):
+            ops.qsw_silu_mul(gd[k:k + 7], ud[k:k + 7], ops.MATCH, out=out[k:k + 7])
+        got = np.roll(to_bits(out), shift)
+        idx = (np.arange(n) + shift) % n   # rolled position -> original position
+        covered = np.zeros(n, dtype=bool)
+        for k in range(0, n - 7, 8):
+            covered[idx[k:k + 7]] = True
+        scalar[covered & ~seen] = got[covered & ~seen]
+        seen |= covered
+    ops.qsw_check_device_errors()
+    assert seen.all()
+    assert np.array_equal(paired, scalar), np.flatnonzero(paired != scalar)[:10]
 
 
 @pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
@@ -357,3 +393,125 @@ def test_early_weight_stream_reads_previous_output(dev, gemv_limit, early_weight
         ok, info = check_match(got, want)
         assert ok, info
         x_bits = got
+
+
+# ------------------------------------------------------------- stream-K ----
+
+@pytest.fixture
+def stream_k():
+    saved = ops.qsw_get_stream_k()
+    yield ops.qsw_set_stream_k
+    ops.qsw_set_stream_k(saved)
+
+
+def _epoch(ws: torch.Tensor) -> int:
+    """The launch counter the tensor-core kernel keeps at the start of the workspace."""
+    torch.cuda.synchronize()
+    return int(ws[:4].view(torch.int32).item())
+
+
+# (M, H, I, bits_g, gs_g, bits_u, gs_u, rows): rows=None checks every row
+SK_SHAPES = [
+    # 48 tiles of 8 K steps; always-split spreads them over every SM, 2-4 CTAs
+    # per tile, most ranges starting inside a scale entry
+    (300, 512, 1536, 4, 64, 4, 64, None),
+    # mixed specs, K tail of 32, ragged N
+    (257, 2080, 384, 4, 32, 8, 32, None),
+    # 2-bit gate, 8-bit up
+    (64, 640, 136, 2, 64, 8, 64, None),
+    # 158 tiles of 64 K steps on 152 SMs: 6 + 152 tiles split over 152 ranges of
+    # ~66 K steps (three accumulation chains per range), one finisher per tile
+    (300, 4096, 5000, 4, 64, 4, 64, [0, 1, 127, 128, 255, 256, 299]),
+]
+
+
+@pytest.mark.parametrize("shape", SK_SHAPES, ids=lambda s: "M{}_H{}_I{}_g{}x{}_u{}x{}".format(*s[:7]))
+@pytest.mark.parametrize("mode", [ops.STREAM_K_OFF, ops.STREAM_K_ALWAYS], ids=["whole_tiles", "split"])
+@pytest.mark.parametrize("variant", [ops.MATCH, ops.F32], ids=["match", "f32"])
+def test_stream_k(dev, gemv_limit, stream_k, shape, mode, variant):
+    """Split and whole-tile schedules of the tensor-core kernel both match the
+    oracle; the workspace's launch counter shows which one ran."""
+    M, H, I, bg, gg, bu, gu, rows = shape
+    case = inputs.make_case(M, H, I, bits_g=bg, gs_g=gg, bits_u=bu, gs_u=gu, seed=M + I)
+    gemv_limit(0)
+    stream_k(mode)
+    ws = ops.workspace(dev)
+    e0 = _epoch(ws)
+    check_fused(case, dev, variant, rows=rows)
+    launches = 3 if variant == ops.MATCH else 1
+    assert _epoch(ws) == e0 + (launches if mode == ops.STREAM_K_ALWAYS else 0)
+
+
+@pytest.mark.parametrize("mode", [ops.STREAM_K_OFF, ops.STREAM_K_ALWAYS], ids=["whole_tiles", "split"])
+def test_stream_k_affine_qmm(dev, gemv_limit, stream_k, mode):
+    """The single-operand form (128 output columns per tile) under both schedules."""
+    case = inputs.make_case(200, 1024, 1000, bits_g=4, gs_g=64, seed=5)
+    gemv_limit(0)
+    stream_k(mode)
+    x, w, s, b, gs, bits = device_args(case, dev)[:6]
+    got = to_bits(ops.affine_qmm(x, w, s, b, gs, bits))
+    ops.qsw_check_device_errors()
+    want = oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gs, bits)
+    ok, info = check_projection(got, want)
+    assert ok, info
+
+
+def test_stream_k_graph_replays(dev, gemv_limit, stream_k):
+    """Split calls captured in a CUDA graph: every replay launches them anew
+    (the workspace's counter advances by one per call), and each replay's
+    results match the oracle for the x it was given, so no replay reads
+    partials a previous one left behind."""
+    gemv_limit(0)
+    stream_k(ops.STREAM_K_ALWAYS)
+    base = inputs.make_case(300, 512, 1536, seed=31)
+    a = device_args(base, dev)
+    x_static = a[0].clone()
+    outs = {v: torch.empty((300, 1536), dtype=torch.bfloat16, device=dev)
+            for v in (ops.MATCH, ops.DEBUG_GATE, ops.DEBUG_UP)}
+    stream = torch.cuda.Stream(device=dev)
+    ws = ops.workspace(dev, stream)
+
+    def calls():
+        for v, o in outs.items():
+            ops.qswiglu_forward(x_static, *a[1:], variant=v, out=o, stream=stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        calls()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        calls()
+    torch.cuda.synchronize()
+    for seed in (41, 42, 43):
+        xb = inputs.make_x(300, 512, seed=seed)
+        x_static.copy_(torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16))
+        for o in outs.values():
+            o.fill_(0)
+        e0 = _epoch(ws)
+        g.replay()
+        ops.qsw_check_device_errors()
+        assert _epoch(ws) == e0 + len(outs)
+        step = inputs.Case(x=xb, gate=base.gate, up=base.up)
+        h_ref, g64, u64 = oracle.qswiglu(*step.oracle_args(), variant=oracle.MATCH, return_acc=True)
+        ok, info = check_match_with_projections(
+            to_bits(outs[ops.MATCH]), to_bits(outs[ops.DEBUG_GATE]), to_bits(outs[ops.DEBUG_UP]), h_ref,
+            oracle.bf16_round_array(g64), oracle.bf16_round_array(u64), match_epilogue)
+        assert ok, info
+
+
+def test_workspace_size_is_checked(dev, gemv_limit):
+    """A caller-owned workspace smaller than qsw_workspace_bytes() is refused."""
+    case = inputs.make_case(130, 512, 200, seed=2)
+    a = device_args(case, dev)
+    need = ops.workspace_bytes(dev)
+    assert need >= 128 * 1024 * torch.cuda.get_device_properties(dev).multi_processor_count
+    small = torch.zeros(need - 1024, dtype=torch.uint8, device=dev)
+    with pytest.raises(ops.QswError):
+        ops.qswiglu_forward(*a, workspace=small)
+    mine = torch.zeros(need, dtype=torch.uint8, device=dev)
+    gemv_limit(0)
+    got = to_bits(ops.qswiglu_forward(*a, variant=ops.F32, workspace=mine))
+    ops.qsw_check_device_errors()
+    ok, info = check_f32(got, oracle.qswiglu(*case.oracle_args(), variant=oracle.F32))
+    assert ok, info
