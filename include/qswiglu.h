@@ -155,7 +155,24 @@ QSW_API qsw_status affine_qmm_ws(const void *x, int64_t M, int64_t K, int64_t N,
                       int gs, int bits, void *y, void *workspace, size_t workspace_bytes,
                       void *stream);
 
-/* Stream-K mode of the *_ws entry points (qsw_stream_k_mode, default
+/*
+ * qswiglu_forward with stream-K scheduling and no caller workspace: the
+ * split-tile partials go to a static device array of the library (sized for up
+ * to 192 SMs; more SMs run whole tiles only), so the call allocates nothing
+ * and takes no workspace argument.  The array is one per device: calls through
+ * this entry point must not run concurrently with each other (use one stream,
+ * or the *_ws form with one workspace per stream).  The first call on a device
+ * also enqueues a 4 KB memset of the array's header on `stream`.  Arguments,
+ * results and errors as for qswiglu_forward.
+ */
+QSW_API qsw_status qswiglu_forward_noalloc(const void *x, int64_t M, int64_t H, int64_t I,
+                           const uint32_t *wg, const void *sg, const void *bg,
+                           int gs_g, int bits_g,
+                           const uint32_t *wu, const void *su, const void *bu,
+                           int gs_u, int bits_u,
+                           int variant, void *out, void *stream);
+
+/* Stream-K mode of the *_ws and _noalloc entry points (qsw_stream_k_mode, default
  * QSW_STREAM_K_AUTO; other values are ignored).  Process-wide. */
 QSW_API void qsw_set_stream_k(int mode);
 QSW_API int qsw_get_stream_k(void);

@@ -93,14 +93,13 @@ qsw_status check_workspace(const void *ws, size_t bytes, qsw::SplitWorkspace *ou
   return QSW_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-qsw_status qswiglu_forward_ws(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
-                              const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su,
-                              const void *bu, int gs_u, int bits_u, int variant, void *out, void *workspace,
-                              size_t workspace_bytes, void *stream) {
+// The fused expansion behind every entry point: argument checks, then the
+// small-M or tensor-core kernel.  `static_scratch`: the tensor-core kernel
+// takes the library's static stream-K workspace (resolved only on that path).
+qsw_status fused_forward(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
+                         const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su, const void *bu,
+                         int gs_u, int bits_u, int variant, void *out, void *workspace, size_t workspace_bytes,
+                         bool static_scratch, void *stream) {
   qsw_status st = check_shape(M, H, I);
   if (st != QSW_OK) return st;
   qsw::SplitWorkspace ws;
@@ -120,10 +119,24 @@ qsw_status qswiglu_forward_ws(const void *x, int64_t M, int64_t H, int64_t I, co
                                     g_early_weights.load(std::memory_order_relaxed) != 0));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
+    if (static_scratch && qsw::prefill_static_workspace(sm_count(), s, &ws.ptr, &ws.bytes) != cudaSuccess)
+      return QSW_ERR_CUDA;
     st = from_cuda(qsw::launch_prefill(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count(), ws));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_TC].fetch_add(1, std::memory_order_relaxed);
   }
   return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+qsw_status qswiglu_forward_ws(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
+                              const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su,
+                              const void *bu, int gs_u, int bits_u, int variant, void *out, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+  return fused_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, out, workspace,
+                       workspace_bytes, false, stream);
 }
 
 qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
@@ -162,6 +175,14 @@ qsw_status affine_qmm_ws(const void *x, int64_t M, int64_t K, int64_t N, const u
 qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
                       const void *b, int gs, int bits, void *y, void *stream) {
   return affine_qmm_ws(x, M, K, N, w, s, b, gs, bits, y, nullptr, 0, stream);
+}
+
+qsw_status qswiglu_forward_noalloc(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg,
+                                   const void *sg, const void *bg, int gs_g, int bits_g, const uint32_t *wu,
+                                   const void *su, const void *bu, int gs_u, int bits_u, int variant, void *out,
+                                   void *stream) {
+  return fused_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, out, nullptr, 0, true,
+                       stream);
 }
 
 size_t qsw_workspace_bytes(void) { return qsw::prefill_workspace_bytes(sm_count()); }

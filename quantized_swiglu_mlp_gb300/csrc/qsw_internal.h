@@ -43,6 +43,11 @@ struct SplitWorkspace {
 
 size_t prefill_workspace_bytes(int num_sms);
 
+// The library's static stream-K workspace on the current device (a device
+// array of the library, not an allocation); *ptr stays null where it is too
+// small for the SM count.  Its header is zeroed on `stream` at first use.
+cudaError_t prefill_static_workspace(int num_sms, cudaStream_t stream, void **ptr, size_t *bytes);
+
 // Tensor-core kernel (tcgen05 + TMA), any M.
 cudaError_t launch_prefill(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                            const QuantOperand *op1, int variant, void *out, cudaStream_t stream,

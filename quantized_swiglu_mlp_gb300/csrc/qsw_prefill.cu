@@ -62,6 +62,14 @@ constexpr int kPartFloats = 2 * UM * BN;                  // f32 partial accumul
 
 __device__ unsigned int g_prefill_error;
 
+// Static stream-K workspace for the entry point that allocates nothing: sized
+// for up to kStaticScratchSms SMs (header + one partial slot per SM), zero at
+// module load and zeroed again (header) on first use per device.
+constexpr int kStaticScratchSms = 192;
+constexpr size_t kStaticScratchBytes =
+    4096 + static_cast<size_t>(kStaticScratchSms) * 2 * 128 * 128 * sizeof(float);
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
 template <int BITS0, int BITS1, bool DUAL>
 struct Cfg {
   static constexpr int kRows0 = DUAL ? 64 : 128;    // B rows from operand 0
@@ -1000,6 +1008,28 @@ cudaError_t dual_bits1(int bits1, const void *x, int64_t M, int64_t K, int64_t N
 
 size_t prefill_workspace_bytes(int num_sms) {
   return num_sms > 0 ? header_bytes(num_sms) + static_cast<size_t>(num_sms) * kPartFloats * sizeof(float) : 0;
+}
+
+cudaError_t prefill_static_workspace(int num_sms, cudaStream_t stream, void **ptr, size_t *bytes) {
+  static_assert(kPartFloats == 2 * 128 * 128, "static scratch slot size");
+  *ptr = nullptr;
+  *bytes = 0;
+  if (num_sms <= 0 || num_sms > kStaticScratchSms || prefill_workspace_bytes(num_sms) > kStaticScratchBytes)
+    return cudaSuccess;   // whole tiles only
+  static void *addr[64];
+  static cudaError_t status[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(once[dev], [&] {
+    status[dev] = cudaGetSymbolAddress(&addr[dev], g_static_scratch);
+    // epoch, done count and flags start at zero, on the stream of the first call
+    if (status[dev] == cudaSuccess) status[dev] = cudaMemsetAsync(addr[dev], 0, header_bytes(num_sms), stream);
+  });
+  if (status[dev] != cudaSuccess) return status[dev];
+  *ptr = addr[dev];
+  *bytes = kStaticScratchBytes;
+  return cudaSuccess;
 }
 
 cudaError_t launch_prefill(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,

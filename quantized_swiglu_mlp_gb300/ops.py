@@ -29,7 +29,8 @@ NUM_COUNTERS = 5
 STATUS = {0: "QSW_OK", 1: "QSW_ERR_INVALID_ARG", 2: "QSW_ERR_UNSUPPORTED", 3: "QSW_ERR_CUDA",
           4: "QSW_ERR_TIMEOUT"}
 STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS = 0, 1, 2
-EXPORTED = ("qswiglu_forward", "affine_qmm", "qswiglu_forward_ws", "affine_qmm_ws", "qsw_workspace_bytes",
+EXPORTED = ("qswiglu_forward", "affine_qmm", "qswiglu_forward_ws", "affine_qmm_ws", "qswiglu_forward_noalloc",
+            "qsw_workspace_bytes",
             "qsw_set_stream_k", "qsw_get_stream_k", "qsw_silu_mul", "qsw_check_device_errors",
             "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_early_weight_stream",
             "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns",
@@ -66,6 +67,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.affine_qmm_ws.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p, sz, p]
         lib.affine_qmm_ws.restype = i32
         lib.qsw_workspace_bytes.restype = sz
+        lib.qswiglu_forward_noalloc.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, p, p]
+        lib.qswiglu_forward_noalloc.restype = i32
         lib.qsw_set_stream_k.argtypes = [i32]
         lib.qsw_get_stream_k.restype = i32
         lib.qsw_silu_mul.argtypes = [p, p, i64, i32, p, p]
@@ -214,6 +217,31 @@ def qswiglu_forward(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, varia
                                       int(gs_u), int(bits_u), int(variant), out.data_ptr(), ws_ptr, ws_bytes,
                                       _stream_ptr(stream))
         _check("qswiglu_forward_ws", code)
+    return out.view(*x.shape[:-1], I)
+
+
+def qswiglu_forward_noalloc(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant=MATCH,
+                            out=None, stream=None) -> torch.Tensor:
+    """qswiglu_forward with stream-K scheduling on the library's static scratch
+    array (no workspace); calls through it must not run concurrently."""
+    lib = load_library()
+    _need(x, "x", _BF16)
+    H = x.shape[-1]
+    x2 = x.reshape(-1, H)
+    M = x2.shape[0]
+    I = _operand(wg, sg, bg, "gate", x.device, H, bits_g, gs_g)
+    if _operand(wu, su, bu, "up", x.device, H, bits_u, gs_u) != I:
+        raise ValueError("gate and up must have the same number of rows")
+    if out is None:
+        out = torch.empty((M, I), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(out, "out", _BF16, x.device)
+        if out.numel() != M * I:
+            raise ValueError("out has the wrong size")
+    code = lib.qswiglu_forward_noalloc(x2.data_ptr(), M, H, I, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(),
+                                       int(gs_g), int(bits_g), wu.data_ptr(), su.data_ptr(), bu.data_ptr(),
+                                       int(gs_u), int(bits_u), int(variant), out.data_ptr(), _stream_ptr(stream))
+    _check("qswiglu_forward_noalloc", code)
     return out.view(*x.shape[:-1], I)
 
 

@@ -169,3 +169,14 @@ def test_stream_k_mode_switch(lib):
         assert ops.qsw_get_stream_k() == ops.STREAM_K_AUTO
     finally:
         ops.qsw_set_stream_k(saved)
+
+
+def test_noalloc_entry_point_validates_on_the_host(lib):
+    """The static-scratch entry point checks its arguments before anything
+    (including its first-use set-up) touches the device."""
+    call = lambda M, variant, x=FAKE: lib.qswiglu_forward_noalloc(x, M, 256, 64, FAKE, FAKE, FAKE, 64, 4, FAKE,
+                                                                    FAKE, FAKE, 64, 4, variant, FAKE, None)
+    assert call(0, 0) == OK
+    assert call(-1, 0) == INVALID
+    assert call(4, 7) == INVALID
+    assert call(4, 0, x=FAKE + 8) == UNSUPPORTED
