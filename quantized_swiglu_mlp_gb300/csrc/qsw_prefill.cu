@@ -84,7 +84,7 @@ struct Cfg {
   static constexpr int kS1Bytes = kRows1 * 2 * kGroupsPerEntry;
   static constexpr int kEntryBytes = 2 * kS0Bytes + 2 * kS1Bytes;
   static constexpr int kSb = 4;   // B ring
-  static constexpr int kSx = 4;   // x ring
+  static constexpr int kSx = 4;   // x ring (advances with the B ring: same depth)
   static constexpr int kBudget = kMaxSmem - 1024 - kBarBytes;
   static constexpr int kFixed = kSx * kXBytes + kSb * kBBytes + 2 * kEntryBytes;
   static constexpr int kScFit = (kBudget - kFixed) / kCodesBytes;
@@ -96,6 +96,7 @@ struct Cfg {
   static constexpr int kBarOff = kSOff + 2 * kEntryBytes;
   static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
   static_assert(kSc >= 2, "codes ring too small");
+  static_assert(kSx == kSb, "the x and B rings share their barriers' slot index");
   static_assert(kCodesBytes % 1024 == 0 && kC0Bytes % 128 == 0, "codes ring alignment");
   static_assert(kEntryBytes % 128 == 0 && kS0Bytes % 128 == 0, "scale ring alignment");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
@@ -301,10 +302,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
+  // The x and B rings advance together (slot k of both holds K step k mod 4):
+  // one dequantiser also waits for the x tile before its arrival on b_full, so
+  // the MMA issuer waits on b_full alone, and one commit to b_empty releases
+  // both slots (the x producer waits on it too).  Every barrier wait in the
+  // issuer's loop is shared-memory latency on the tensor core's critical path.
   uint64_t *x_full = bars;              // x tile landed (TMA bytes)
-  uint64_t *x_empty = x_full + Sx;      // MMAs reading the x tile completed
-  uint64_t *b_full = x_empty + Sx;      // B tile written by all dequantisers
-  uint64_t *b_empty = b_full + Sb;      // MMAs reading the B tile completed
+  uint64_t *b_full = x_full + Sx;       // B tile written by all dequantisers, x tile landed
+  uint64_t *b_empty = b_full + Sb;      // MMAs reading the x and B tiles completed
   uint64_t *c_full = b_empty + Sb;      // codes landed
   uint64_t *c_empty = c_full + Sc;      // codes consumed by all dequantisers
   uint64_t *s_full = c_empty + Sc;      // [op][2] scale entry landed
@@ -333,10 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kpe1 = kGroupsPerEntry * p.gd1.gs / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Sx; ++s) {
-      mbar_init(&x_full[s], 1);
-      mbar_init(&x_empty[s], 1);
-    }
+    for (int s = 0; s < Sx; ++s) mbar_init(&x_full[s], 1);
     for (int s = 0; s < Sb; ++s) {
       mbar_init(&b_full[s], kDeqWarps);
       mbar_init(&b_empty[s], 1);
@@ -485,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m0 = (sg.tile % p.m_tiles) * BM;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           const int xs = n_x % Sx;
-          if (!mbar_wait(&x_empty[xs], ((n_x / Sx) & 1) ^ 1u, abort_flag, p.timeout_ns, err)) {
+          if (!mbar_wait(&b_empty[xs], ((n_x / Sx) & 1) ^ 1u, abort_flag, p.timeout_ns, err)) {
             ok = false;
             break;
           }
@@ -553,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_tmem = c == 0 ? x_tmem : y_tmem;
           const bool chain_start = cpos == 0;
           const int xs = n_x % Sx, bs = n_b % Sb;
-          if (!mbar_wait(&x_full[xs], (n_x / Sx) & 1, abort_flag, p.timeout_ns, err) ||
-              !mbar_wait(&b_full[bs], (n_b / Sb) & 1, abort_flag, p.timeout_ns, err)) {
+          // b_full also covers the x tile (see the barrier note)
+          if (!mbar_wait(&b_full[bs], (n_b / Sb) & 1, abort_flag, p.timeout_ns, err)) {
             ok = false;
             break;
           }
@@ -570,7 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16(d_tmem, adesc0 + 2 * kk, bdesc + 2 * kk, kIdesc, acc);
             umma_bf16(d_tmem + BN, adesc1 + 2 * kk, bdesc + 2 * kk, kIdesc, acc);
           }
-          umma_commit(&x_empty[xs]);
           umma_commit(&b_empty[bs]);
           ++n_x;
           ++n_b;
@@ -619,6 +620,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         const int cs = n_c % Sc, bs = n_b % Sb;
         if (!(ok = warp_wait(&c_full[cs], (n_c / Sc) & 1, abort_flag, p.timeout_ns, err))) break;
+        // dequantiser 0 vouches for the x tile of this K step as well; the x
+        // tile lands long before the B slot frees up, so this wait hides in
+        // the next one
+        if (dw == 0 && !(ok = warp_wait(&x_full[bs], (n_b / Sb) & 1, abort_flag, p.timeout_ns, err))) break;
         if (!(ok = warp_wait(&b_empty[bs], ((n_b / Sb) & 1) ^ 1u, abort_flag, p.timeout_ns, err))) break;
         // scale and bias of this thread's 16 codes (one group: gs is a multiple of 32)
         const uint32_t gi = gd(static_cast<uint32_t>(epos * BK + 16 * q));
