@@ -9,8 +9,14 @@ round-to-nearest-even at each point the method rounds); this module only builds
 it with gcc and marshals numpy arrays through ctypes.  Every array is host
 memory: bf16 values travel as uint16 bit patterns.
 
+Every function that takes activations has a ``dtype`` argument: "bf16" (the
+default) or "f16", the two activation dtypes the pages' kernels accept; x,
+scales, biases and results are then that dtype's bit patterns.
+
 Parity status of each function (what pins it is in tests/test_oracle_pins.py):
   bf16_round    pinned (library cast on binary32 inputs, exact rational rounding)
+  f16_round     pinned (numpy's IEEE binary16 conversion, exhaustive decode of
+                all 65536 patterns, hand-worked boundary values)
   unpack        pinned (hand-packed words, round trip)
   dequant       pinned (hand-worked rows, exact rational brute force)
   qswiglu       pinned (hand-worked 2x8 example, x=0, integer special case,
@@ -33,6 +39,13 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 
 MATCH, F32, DEBUG_GATE, DEBUG_UP = 0, 1, 2, 3
+DTYPES = {"bf16": 0, "f16": 1}
+
+
+def _dt(dtype) -> int:
+    if dtype not in DTYPES:
+        raise ValueError(f"dtype must be one of {sorted(DTYPES)}, got {dtype!r}")
+    return DTYPES[dtype]
 
 
 def build(force: bool = False) -> str:
@@ -54,18 +67,22 @@ def _declare(lib):
     lib.orc_f64_to_bf16.restype = ctypes.c_uint16
     lib.orc_bf16_to_f64.argtypes = [ctypes.c_uint16]
     lib.orc_bf16_to_f64.restype = ctypes.c_double
+    lib.orc_f64_to_f16.argtypes = [ctypes.c_double]
+    lib.orc_f64_to_f16.restype = ctypes.c_uint16
+    lib.orc_f16_to_f64.argtypes = [ctypes.c_uint16]
+    lib.orc_f16_to_f64.restype = ctypes.c_double
     lib.orc_unpack.argtypes = [p, i64, i32, p]
-    lib.orc_dequant.argtypes = [p, p, p, i64, i64, i32, i32, p]
-    q_args = [p, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32]
+    lib.orc_dequant.argtypes = [p, p, p, i64, i64, i32, i32, i32, p]
+    q_args = [p, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, i32]
     lib.orc_qswiglu.argtypes = q_args + [p]
     lib.orc_qswiglu.restype = i32
     lib.orc_qswiglu_rows.argtypes = q_args + [p, i64, p, p, p]
     lib.orc_qswiglu_rows.restype = i32
     lib.orc_qswiglu_pairs.argtypes = q_args + [p, i64, p]
     lib.orc_qswiglu_pairs.restype = i32
-    lib.orc_qmm.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p]
+    lib.orc_qmm.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, i32, p]
     lib.orc_qmm.restype = i32
-    lib.orc_silu_mul.argtypes = [p, p, i64, i32, p]
+    lib.orc_silu_mul.argtypes = [p, p, i64, i32, i32, p]
     lib.orc_num_threads.restype = i32
     lib.orc_set_num_threads.argtypes = [i32]
     return lib
@@ -113,6 +130,19 @@ class OracleLib:
         flat = np.asarray(v, dtype=np.float64).ravel()
         return np.array([f(float(t)) for t in flat], dtype=np.uint16).reshape(np.shape(v))
 
+    def f64_to_f16(self, v: float) -> int:
+        """One round-to-nearest-even of an exact double to a binary16 bit pattern."""
+        return int(self.lib.orc_f64_to_f16(float(v)))
+
+    def f16_to_f64(self, h: int) -> float:
+        return float(self.lib.orc_f16_to_f64(int(h) & 0xFFFF))
+
+    def round_array(self, v, dtype="bf16") -> np.ndarray:
+        """Doubles -> bit patterns of `dtype`, one rounding each."""
+        f = self.lib.orc_f64_to_f16 if _dt(dtype) else self.lib.orc_f64_to_bf16
+        flat = np.asarray(v, dtype=np.float64).ravel()
+        return np.array([f(float(t)) for t in flat], dtype=np.uint16).reshape(np.shape(v))
+
     def unpack(self, words: np.ndarray, n_codes: int, bits: int) -> np.ndarray:
         words = _c(words, np.uint32)
         if words.size * (32 // bits) < n_codes:
@@ -121,12 +151,12 @@ class OracleLib:
         self.lib.orc_unpack(_ptr(words), n_codes, bits, _ptr(out))
         return out
 
-    def dequant(self, w, s, b, K: int, gs: int, bits: int) -> np.ndarray:
-        """Dequantised bf16 operand as exact doubles, [rows, K]."""
+    def dequant(self, w, s, b, K: int, gs: int, bits: int, dtype="bf16") -> np.ndarray:
+        """Dequantised operand (rounded to `dtype`) as exact doubles, [rows, K]."""
         w, s, b = _c(w, np.uint32), _c(s, np.uint16), _c(b, np.uint16)
         rows = w.shape[0]
         out = np.empty((rows, K), dtype=np.float64)
-        self.lib.orc_dequant(_ptr(w), _ptr(s), _ptr(b), rows, K, gs, bits, _ptr(out))
+        self.lib.orc_dequant(_ptr(w), _ptr(s), _ptr(b), rows, K, gs, bits, _dt(dtype), _ptr(out))
         return out
 
     @staticmethod
@@ -148,8 +178,8 @@ class OracleLib:
         return keep, args, M, H, I
 
     def qswiglu(self, x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u,
-                variant=MATCH, rows=None, return_acc=False):
-        """hidden [len(rows) or M, I] as bf16 bit patterns (uint16).
+                variant=MATCH, rows=None, return_acc=False, dtype="bf16"):
+        """hidden [len(rows) or M, I] as bit patterns (uint16) of `dtype`.
 
         With return_acc, also returns the unrounded f64 gate and up projections."""
         keep, args, M, H, I = self._qargs(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u)
@@ -163,7 +193,7 @@ class OracleLib:
         out = np.empty((n_rows, I), dtype=np.uint16)
         g = np.empty((n_rows, I), dtype=np.float64) if return_acc else None
         u = np.empty((n_rows, I), dtype=np.float64) if return_acc else None
-        rc = self.lib.orc_qswiglu_rows(*args, int(variant), rows_p, n_rows, _ptr(out),
+        rc = self.lib.orc_qswiglu_rows(*args, int(variant), _dt(dtype), rows_p, n_rows, _ptr(out),
                                        _ptr(g) if return_acc else None,
                                        _ptr(u) if return_acc else None)
         del keep, rows_arr
@@ -171,38 +201,40 @@ class OracleLib:
             raise MemoryError("oracle allocation failed")
         return (out, g, u) if return_acc else out
 
-    def qswiglu_pairs(self, x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, pairs):
-        """hidden[m, i] for each (m, i) in pairs ([n, 2] int64), as uint16."""
+    def qswiglu_pairs(self, x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, pairs,
+                      dtype="bf16"):
+        """hidden[m, i] for each (m, i) in pairs ([n, 2] int64), as uint16 bits of `dtype`."""
         keep, args, M, H, I = self._qargs(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u)
         pairs = _c(np.asarray(pairs, dtype=np.int64).reshape(-1, 2), np.int64)
         if pairs.size and (pairs[:, 0].min() < 0 or pairs[:, 0].max() >= M
                            or pairs[:, 1].min() < 0 or pairs[:, 1].max() >= I):
             raise IndexError("pair out of range")
         out = np.empty(pairs.shape[0], dtype=np.uint16)
-        rc = self.lib.orc_qswiglu_pairs(*args, int(variant), _ptr(pairs), pairs.shape[0], _ptr(out))
+        rc = self.lib.orc_qswiglu_pairs(*args, int(variant), _dt(dtype), _ptr(pairs), pairs.shape[0],
+                                        _ptr(out))
         del keep
         if rc != 0:
             raise MemoryError("oracle allocation failed")
         return out
 
-    def qmm(self, x, w, s, b, gs, bits):
-        """Unfused quantised linear y = bf16(x . W^T) as uint16 [M, N]."""
+    def qmm(self, x, w, s, b, gs, bits, dtype="bf16"):
+        """Unfused quantised linear y = T(x . W^T) as uint16 [M, N] bits of T = `dtype`."""
         x, w, s, b = _c(x, np.uint16), _c(w, np.uint32), _c(s, np.uint16), _c(b, np.uint16)
         M, K = x.shape
         N = w.shape[0]
         if w.shape != (N, K * bits // 32) or s.shape != (N, K // gs) or b.shape != s.shape:
             raise ValueError("shape mismatch")
         y = np.empty((M, N), dtype=np.uint16)
-        if self.lib.orc_qmm(_ptr(x), M, K, N, _ptr(w), _ptr(s), _ptr(b), gs, bits, _ptr(y)) != 0:
+        if self.lib.orc_qmm(_ptr(x), M, K, N, _ptr(w), _ptr(s), _ptr(b), gs, bits, _dt(dtype), _ptr(y)) != 0:
             raise MemoryError("oracle allocation failed")
         return y
 
-    def silu_mul(self, g, u, variant=MATCH):
+    def silu_mul(self, g, u, variant=MATCH, dtype="bf16"):
         g, u = _c(g, np.uint16), _c(u, np.uint16)
         if g.shape != u.shape:
             raise ValueError("shape mismatch")
         out = np.empty_like(g)
-        self.lib.orc_silu_mul(_ptr(g), _ptr(u), g.size, int(variant), _ptr(out))
+        self.lib.orc_silu_mul(_ptr(g), _ptr(u), g.size, int(variant), _dt(dtype), _ptr(out))
         return out
 
 
@@ -238,7 +270,7 @@ def source_text() -> str:
 def __getattr__(name):
     # module-level shortcuts: oracle.qswiglu(...), oracle.qmm(...), ...
     if name in ("num_threads", "set_num_threads", "f64_to_bf16", "bf16_to_f64",
-                "bf16_round_array", "unpack", "dequant", "qswiglu", "qswiglu_pairs",
-                "qmm", "silu_mul"):
+                "bf16_round_array", "f64_to_f16", "f16_to_f64", "round_array", "unpack", "dequant",
+                "qswiglu", "qswiglu_pairs", "qmm", "silu_mul"):
         return getattr(default(), name)
     raise AttributeError(name)

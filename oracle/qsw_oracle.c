@@ -27,13 +27,16 @@
  * Readings taken where the pages are silent (all listed in the design notes):
  *  - codes are packed little-endian: code k of a row sits at bits
  *    (k mod pf)*bits of word k/pf, pf = 32/bits;
- *  - w = scale*q + bias, rounded ONCE to bf16 (round to nearest, ties to even);
+ *  - w = scale*q + bias, rounded ONCE to the activation dtype T (round to
+ *    nearest, ties to even);
  *  - accumulation is exact-product / f64-sum (the float accumulator's order is
  *    free, so the oracle takes the most accurate one);
- *  - F32 keeps gate and up unrounded: hidden = bf16(g * u / (1 + exp(-g))).
+ *  - F32 keeps gate and up unrounded: hidden = T(g * u / (1 + exp(-g))).
  *
- * Everything is computed in f64 with explicit bf16 rounding at each point where
- * the method rounds.  bf16 values travel as their raw uint16 bit patterns.
+ * T is bf16 or f16 (fusedSwigluSupported() accepts both activation dtypes);
+ * x, scales, biases and results share it.  Everything is computed in f64 with
+ * explicit rounding to T at each point where the method rounds.  T values
+ * travel as their raw uint16 bit patterns.
  */
 #include <math.h>
 #include <stdint.h>
@@ -95,6 +98,60 @@ uint16_t orc_f64_to_bf16(double v)
     return (uint16_t)(sign | ((bits >> 16) & 0x7FFFu));
 }
 
+/* ---------------------------------------------------------------- f16 ----- */
+
+/* IEEE binary16 bit pattern -> exact double: 1 sign bit, 5 exponent bits
+ * (bias 15), 10 stored fraction bits; exponent field 0 holds the subnormals
+ * (spacing 2^-24), 31 the infinities and NaNs. */
+double orc_f16_to_f64(uint16_t h)
+{
+    int sign = (h >> 15) & 1, ex = (h >> 10) & 0x1F, fr = h & 0x3FF;
+    double a;
+    if (ex == 0) a = ldexp((double)fr, -24);
+    else if (ex == 31) a = fr ? NAN : INFINITY;
+    else a = ldexp((double)(1024 + fr), ex - 25);
+    return sign ? -a : a;
+}
+
+/*
+ * double -> binary16 with ONE rounding (nearest, ties to even) from the exact
+ * double value.  A normal number carries 11 significant bits; below 2^-14 the
+ * spacing is fixed at 2^-24.  Values that round to 2^16 or beyond are inf
+ * (the largest finite binary16 is (2 - 2^-10) * 2^15 = 65504).
+ */
+uint16_t orc_f64_to_f16(double v)
+{
+    if (isnan(v)) return (uint16_t)(signbit(v) ? 0xFE00u : 0x7E00u);
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return (uint16_t)(sign | 0x7C00u);
+
+    int e2;
+    frexp(a, &e2);
+    int e = e2 - 1;              /* 2^e <= a < 2^(e+1) */
+    int ulp_exp = e - 10;
+    if (ulp_exp < -24) ulp_exp = -24;
+    double r = ldexp(round_half_even(ldexp(a, -ulp_exp)), ulp_exp);
+    if (r >= 65536.0) return (uint16_t)(sign | 0x7C00u);
+    if (r < ldexp(1.0, -14))     /* subnormal (or the smallest normal, same encoding) */
+        return (uint16_t)(sign | (uint16_t)ldexp(r, 24));
+    frexp(r, &e2);
+    e = e2 - 1;                  /* rounding may have carried into the next binade */
+    int fr = (int)(ldexp(r, 10 - e) - 1024.0);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)fr);
+}
+
+/* ------------------------------------------------------- activation dtype -- */
+
+/* The activation dtype T of the pages' kernels: bf16 (ORC_BF16) or f16
+ * (ORC_F16).  x, the scales and biases, the dequantised weights, the stored
+ * projections and hidden are all T; every rounding point rounds to T. */
+enum { ORC_BF16 = 0, ORC_F16 = 1 };
+
+static double act_to_f64(uint16_t h, int dt) { return dt == ORC_F16 ? orc_f16_to_f64(h) : orc_bf16_to_f64(h); }
+static uint16_t f64_to_act(double v, int dt) { return dt == ORC_F16 ? orc_f64_to_f16(v) : orc_f64_to_bf16(v); }
+
 /* ------------------------------------------------------------ codes ------- */
 
 /* Code k of a packed row: word k/pf, bit offset (k mod pf)*bits, LSB first. */
@@ -113,55 +170,55 @@ void orc_unpack(const uint32_t *words, int64_t n_codes, int bits, uint8_t *codes
 
 /*
  * Dequantise rows [0, rows) of a [rows, K] affine-quantised matrix into the
- * bf16 operand the block MMA consumes, returned as exact doubles:
- *     w[r,k] = bf16( scale[r, k/gs] * q[r,k] + bias[r, k/gs] ).
+ * operand the block MMA consumes (dtype T, see above), returned as exact doubles:
+ *     w[r,k] = T( scale[r, k/gs] * q[r,k] + bias[r, k/gs] ).
  * scale*q has at most 16 significant bits; the sum with the bias is exact in
  * double whenever the exponents of scale and bias differ by less than ~36,
  * which holds for every input the generators produce.
  */
 void orc_dequant(const uint32_t *w, const uint16_t *s, const uint16_t *b,
-                 int64_t rows, int64_t K, int gs, int bits, double *out)
+                 int64_t rows, int64_t K, int gs, int bits, int dt, double *out)
 {
     int64_t words_per_row = K * bits / 32;
     int64_t groups_per_row = K / gs;
     for (int64_t r = 0; r < rows; ++r) {
         const uint32_t *wr = w + r * words_per_row;
         for (int64_t k = 0; k < K; ++k) {
-            double sc = orc_bf16_to_f64(s[r * groups_per_row + k / gs]);
-            double bi = orc_bf16_to_f64(b[r * groups_per_row + k / gs]);
+            double sc = act_to_f64(s[r * groups_per_row + k / gs], dt);
+            double bi = act_to_f64(b[r * groups_per_row + k / gs], dt);
             double q = (double)code_at(wr, k, bits);
-            out[r * K + k] = orc_bf16_to_f64(orc_f64_to_bf16(sc * q + bi));
+            out[r * K + k] = act_to_f64(f64_to_act(sc * q + bi, dt), dt);
         }
     }
 }
 
 /* ----------------------------------------------------------- epilogues ---- */
 
-static double rb(double v) { return orc_bf16_to_f64(orc_f64_to_bf16(v)); }
+static double ract(double v, int dt) { return act_to_f64(f64_to_act(v, dt), dt); }
 
-/* MATCH: gate/up arrive as bf16 (the stored projection); sigmoid, silu and the
- * product are each rounded to bf16, op for op with sigmoid -> mul -> mul. */
-static double match_epilogue(double gb, double ub)
+/* MATCH: gate/up arrive as T (the stored projection); sigmoid, silu and the
+ * product are each rounded to T, op for op with sigmoid -> mul -> mul. */
+static double match_epilogue(double gb, double ub, int dt)
 {
-    double sig = rb(1.0 / (1.0 + exp(-gb)));
-    double silu = rb(gb * sig);
-    return rb(silu * ub);
+    double sig = ract(1.0 / (1.0 + exp(-gb)), dt);
+    double silu = ract(gb * sig, dt);
+    return ract(silu * ub, dt);
 }
 
 /* F32: no intermediate rounding; silu(g)*u = g*u/(1+exp(-g)) rounded once. */
-static double f32_epilogue(double g, double u)
+static double f32_epilogue(double g, double u, int dt)
 {
-    return rb(g * u / (1.0 + exp(-g)));
+    return ract(g * u / (1.0 + exp(-g)), dt);
 }
 
-static uint16_t epilogue(int variant, double g, double u)
+static uint16_t epilogue(int variant, double g, double u, int dt)
 {
     switch (variant) {
-    case ORC_MATCH:      return orc_f64_to_bf16(match_epilogue(rb(g), rb(u)));
-    case ORC_F32:        return orc_f64_to_bf16(f32_epilogue(g, u));
-    case ORC_DEBUG_GATE: return orc_f64_to_bf16(g);
-    case ORC_DEBUG_UP:   return orc_f64_to_bf16(u);
-    default:             return 0x7FC0u;
+    case ORC_MATCH:      return f64_to_act(match_epilogue(ract(g, dt), ract(u, dt), dt), dt);
+    case ORC_F32:        return f64_to_act(f32_epilogue(g, u, dt), dt);
+    case ORC_DEBUG_GATE: return f64_to_act(g, dt);
+    case ORC_DEBUG_UP:   return f64_to_act(u, dt);
+    default:             return dt == ORC_F16 ? 0x7E00u : 0x7FC0u;
     }
 }
 
@@ -174,11 +231,11 @@ static double dot_f64(const double *xr, const double *wr, int64_t K)
     return acc;
 }
 
-static double *bf16_rows_to_f64(const uint16_t *x, int64_t rows, int64_t K)
+static double *act_rows_to_f64(const uint16_t *x, int64_t rows, int64_t K, int dt)
 {
     double *xd = (double *)malloc(sizeof(double) * (size_t)(rows * K > 0 ? rows * K : 1));
     if (!xd) return NULL;
-    for (int64_t i = 0; i < rows * K; ++i) xd[i] = orc_bf16_to_f64(x[i]);
+    for (int64_t i = 0; i < rows * K; ++i) xd[i] = act_to_f64(x[i], dt);
     return xd;
 }
 
@@ -209,7 +266,7 @@ void orc_set_num_threads(int n)
 int orc_qswiglu_rows(const uint16_t *x, int64_t M, int64_t H, int64_t I,
                      const uint32_t *wg, const uint16_t *sg, const uint16_t *bg, int gs_g, int bits_g,
                      const uint32_t *wu, const uint16_t *su, const uint16_t *bu, int gs_u, int bits_u,
-                     int variant, const int64_t *rows, int64_t n_rows,
+                     int variant, int dt, const int64_t *rows, int64_t n_rows,
                      uint16_t *out, double *g_acc, double *u_acc)
 {
     if (rows == NULL) n_rows = M;
@@ -217,7 +274,7 @@ int orc_qswiglu_rows(const uint16_t *x, int64_t M, int64_t H, int64_t I,
     if (!xd) return -1;
     for (int64_t j = 0; j < n_rows; ++j) {
         int64_t m = rows ? rows[j] : j;
-        for (int64_t k = 0; k < H; ++k) xd[j * H + k] = orc_bf16_to_f64(x[m * H + k]);
+        for (int64_t k = 0; k < H; ++k) xd[j * H + k] = act_to_f64(x[m * H + k], dt);
     }
     int64_t wpr_g = H * bits_g / 32, wpr_u = H * bits_u / 32;
     int64_t gpr_g = H / gs_g, gpr_u = H / gs_u;
@@ -232,12 +289,12 @@ int orc_qswiglu_rows(const uint16_t *x, int64_t M, int64_t H, int64_t I,
         } else {
 #pragma omp for schedule(dynamic, 16)
             for (int64_t i = 0; i < I; ++i) {
-                orc_dequant(wg + i * wpr_g, sg + i * gpr_g, bg + i * gpr_g, 1, H, gs_g, bits_g, wgr);
-                orc_dequant(wu + i * wpr_u, su + i * gpr_u, bu + i * gpr_u, 1, H, gs_u, bits_u, wur);
+                orc_dequant(wg + i * wpr_g, sg + i * gpr_g, bg + i * gpr_g, 1, H, gs_g, bits_g, dt, wgr);
+                orc_dequant(wu + i * wpr_u, su + i * gpr_u, bu + i * gpr_u, 1, H, gs_u, bits_u, dt, wur);
                 for (int64_t j = 0; j < n_rows; ++j) {
                     double g = dot_f64(xd + j * H, wgr, H);
                     double u = dot_f64(xd + j * H, wur, H);
-                    out[j * I + i] = epilogue(variant, g, u);
+                    out[j * I + i] = epilogue(variant, g, u, dt);
                     if (g_acc) g_acc[j * I + i] = g;
                     if (u_acc) u_acc[j * I + i] = u;
                 }
@@ -253,10 +310,10 @@ int orc_qswiglu_rows(const uint16_t *x, int64_t M, int64_t H, int64_t I,
 int orc_qswiglu(const uint16_t *x, int64_t M, int64_t H, int64_t I,
                 const uint32_t *wg, const uint16_t *sg, const uint16_t *bg, int gs_g, int bits_g,
                 const uint32_t *wu, const uint16_t *su, const uint16_t *bu, int gs_u, int bits_u,
-                int variant, uint16_t *out)
+                int variant, int dt, uint16_t *out)
 {
     return orc_qswiglu_rows(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u,
-                            variant, NULL, M, out, NULL, NULL);
+                            variant, dt, NULL, M, out, NULL, NULL);
 }
 
 /*
@@ -266,7 +323,7 @@ int orc_qswiglu(const uint16_t *x, int64_t M, int64_t H, int64_t I,
 int orc_qswiglu_pairs(const uint16_t *x, int64_t M, int64_t H, int64_t I,
                       const uint32_t *wg, const uint16_t *sg, const uint16_t *bg, int gs_g, int bits_g,
                       const uint32_t *wu, const uint16_t *su, const uint16_t *bu, int gs_u, int bits_u,
-                      int variant, const int64_t *pairs, int64_t n, uint16_t *out)
+                      int variant, int dt, const int64_t *pairs, int64_t n, uint16_t *out)
 {
     (void)M; (void)I;
     int64_t wpr_g = H * bits_g / 32, wpr_u = H * bits_u / 32;
@@ -283,10 +340,10 @@ int orc_qswiglu_pairs(const uint16_t *x, int64_t M, int64_t H, int64_t I,
 #pragma omp for schedule(dynamic, 8)
             for (int64_t p = 0; p < n; ++p) {
                 int64_t m = pairs[2 * p], i = pairs[2 * p + 1];
-                for (int64_t k = 0; k < H; ++k) xr[k] = orc_bf16_to_f64(x[m * H + k]);
-                orc_dequant(wg + i * wpr_g, sg + i * gpr_g, bg + i * gpr_g, 1, H, gs_g, bits_g, wgr);
-                orc_dequant(wu + i * wpr_u, su + i * gpr_u, bu + i * gpr_u, 1, H, gs_u, bits_u, wur);
-                out[p] = epilogue(variant, dot_f64(xr, wgr, H), dot_f64(xr, wur, H));
+                for (int64_t k = 0; k < H; ++k) xr[k] = act_to_f64(x[m * H + k], dt);
+                orc_dequant(wg + i * wpr_g, sg + i * gpr_g, bg + i * gpr_g, 1, H, gs_g, bits_g, dt, wgr);
+                orc_dequant(wu + i * wpr_u, su + i * gpr_u, bu + i * gpr_u, 1, H, gs_u, bits_u, dt, wur);
+                out[p] = epilogue(variant, dot_f64(xr, wgr, H), dot_f64(xr, wur, H), dt);
             }
         }
         free(buf);
@@ -297,14 +354,14 @@ int orc_qswiglu_pairs(const uint16_t *x, int64_t M, int64_t H, int64_t I,
 /* ------------------------------------------------ unfused composition ----- */
 
 /*
- * Quantised linear y = bf16(x . W^T): the float accumulator cast to the
+ * Quantised linear y = T(x . W^T): the float accumulator cast to the
  * activation dtype at the store.  x [M,K], W packed [N, K*bits/32], y [M,N].
  */
 int orc_qmm(const uint16_t *x, int64_t M, int64_t K, int64_t N,
-            const uint32_t *w, const uint16_t *s, const uint16_t *b, int gs, int bits,
+            const uint32_t *w, const uint16_t *s, const uint16_t *b, int gs, int bits, int dt,
             uint16_t *y)
 {
-    double *xd = bf16_rows_to_f64(x, M, K);
+    double *xd = act_rows_to_f64(x, M, K, dt);
     if (!xd) return -1;
     int64_t wpr = K * bits / 32, gpr = K / gs;
     int failed = 0;
@@ -317,9 +374,9 @@ int orc_qmm(const uint16_t *x, int64_t M, int64_t K, int64_t N,
         } else {
 #pragma omp for schedule(dynamic, 16)
             for (int64_t n = 0; n < N; ++n) {
-                orc_dequant(w + n * wpr, s + n * gpr, b + n * gpr, 1, K, gs, bits, wr);
+                orc_dequant(w + n * wpr, s + n * gpr, b + n * gpr, 1, K, gs, bits, dt, wr);
                 for (int64_t m = 0; m < M; ++m)
-                    y[m * N + n] = orc_f64_to_bf16(dot_f64(xd + m * K, wr, K));
+                    y[m * N + n] = f64_to_act(dot_f64(xd + m * K, wr, K), dt);
             }
         }
         free(wr);
@@ -329,15 +386,15 @@ int orc_qmm(const uint16_t *x, int64_t M, int64_t K, int64_t N,
 }
 
 /*
- * Elementwise silu(g)*u over bf16 arrays, as the unfused path applies it to the
- * two stored projections.  MATCH rounds sigmoid, silu and the product to bf16;
+ * Elementwise silu(g)*u over T arrays, as the unfused path applies it to the
+ * two stored projections.  MATCH rounds sigmoid, silu and the product to T;
  * F32 rounds once at the store.
  */
-void orc_silu_mul(const uint16_t *g, const uint16_t *u, int64_t n, int variant, uint16_t *out)
+void orc_silu_mul(const uint16_t *g, const uint16_t *u, int64_t n, int variant, int dt, uint16_t *out)
 {
     for (int64_t i = 0; i < n; ++i) {
-        double gv = orc_bf16_to_f64(g[i]), uv = orc_bf16_to_f64(u[i]);
-        double h = (variant == ORC_F32) ? f32_epilogue(gv, uv) : match_epilogue(gv, uv);
-        out[i] = orc_f64_to_bf16(h);
+        double gv = act_to_f64(g[i], dt), uv = act_to_f64(u[i], dt);
+        double h = (variant == ORC_F32) ? f32_epilogue(gv, uv, dt) : match_epilogue(gv, uv, dt);
+        out[i] = f64_to_act(h, dt);
     }
 }

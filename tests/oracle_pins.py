@@ -5,7 +5,8 @@ against the real oracle (tests/test_oracle_pins.py) and against copies with a
 planted mistake (tests/test_oracle_mutants.py), which must fail at least one.
 
 Independent references used here, none of which is the oracle's own code:
-  * the library float32 -> bf16 cast (torch), which rounds to nearest even;
+  * the library float32 -> bf16 and float32 -> binary16 casts (torch), which
+    round to nearest even, and numpy's float16 type for decoding binary16;
   * "round to odd" to binary32 followed by that library cast, which gives the
     correctly rounded bf16 of any double because binary32 keeps more than two
     extra bits (Boldo and Melquiond, "Emulation of FMA and correctly rounded
@@ -58,6 +59,25 @@ def bf16_val(h: int) -> float:
     return float(np.array([h << 16], dtype=np.uint32).view(np.float32)[0])
 
 
+def lib_f16_bits(v32: np.ndarray) -> np.ndarray:
+    """Library cast float32 -> IEEE binary16 (round to nearest even), as uint16 bits."""
+    t = torch.from_numpy(np.ascontiguousarray(v32, dtype=np.float32))
+    return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+
+
+def ref_f16(v: float) -> int:
+    """Correctly rounded binary16 of a double: round to odd in binary32 (13 spare
+    bits), then the library cast."""
+    return int(lib_f16_bits(np.array([round_to_odd_f32(float(v))], dtype=np.float32))[0])
+
+
+def f16_val(h: int) -> float:
+    return float(np.array([h], dtype=np.uint16).view(np.float16)[0])
+
+
+REF = {"bf16": (ref_bf16, bf16_val), "f16": (ref_f16, f16_val)}
+
+
 def ref_round(v: float) -> float:
     return bf16_val(ref_bf16(v))
 
@@ -74,8 +94,11 @@ def ref_codes_from_words(words, n, bits):
 
 
 def brute_force(case: inputs.Case, variant: int) -> np.ndarray:
-    """Dequantise whole matrices with Fractions, then a triple loop."""
-    x = [[Fraction(bf16_val(int(h))) for h in row] for row in case.x]
+    """Dequantise whole matrices with Fractions, then a triple loop (in the
+    case's activation dtype)."""
+    to_bits, val = REF[case.dtype]
+    rnd = lambda v: val(to_bits(v))
+    x = [[Fraction(val(int(h))) for h in row] for row in case.x]
     M, H, I = case.M, case.H, case.I
 
     def deq(qm: inputs.QuantMatrix):
@@ -84,9 +107,9 @@ def brute_force(case: inputs.Case, variant: int) -> np.ndarray:
         for i in range(I):
             row = []
             for k in range(H):
-                s = Fraction(bf16_val(int(qm.scales[i, k // qm.gs])))
-                b = Fraction(bf16_val(int(qm.biases[i, k // qm.gs])))
-                row.append(Fraction(ref_round(float(s * codes[i][k] + b))))
+                s = Fraction(val(int(qm.scales[i, k // qm.gs])))
+                b = Fraction(val(int(qm.biases[i, k // qm.gs])))
+                row.append(Fraction(rnd(float(s * codes[i][k] + b))))
             W.append(row)
         return W
 
@@ -97,16 +120,16 @@ def brute_force(case: inputs.Case, variant: int) -> np.ndarray:
             g = float(sum(x[m][k] * Wg[i][k] for k in range(H)))
             u = float(sum(x[m][k] * Wu[i][k] for k in range(H)))
             if variant == MATCH:
-                gb, ub = ref_round(g), ref_round(u)
-                sig = ref_round(1.0 / (1.0 + math.exp(-gb)))
-                silu = ref_round(gb * sig)
-                out[m, i] = ref_bf16(silu * ub)
+                gb, ub = rnd(g), rnd(u)
+                sig = rnd(1.0 / (1.0 + math.exp(-gb)))
+                silu = rnd(gb * sig)
+                out[m, i] = to_bits(silu * ub)
             elif variant == F32:
-                out[m, i] = ref_bf16(g * u / (1.0 + math.exp(-g)))
+                out[m, i] = to_bits(g * u / (1.0 + math.exp(-g)))
             elif variant == DEBUG_GATE:
-                out[m, i] = ref_bf16(g)
+                out[m, i] = to_bits(g)
             else:
-                out[m, i] = ref_bf16(u)
+                out[m, i] = to_bits(u)
     return out
 
 
@@ -323,6 +346,100 @@ def pin_sampled_pairs(orc):
     assert np.array_equal(rows, full[[4, 1]])
 
 
+# ---------------------------------------------------- f16 activations -----
+
+def pin_f16_decode(orc):
+    """Every binary16 bit pattern widens to numpy's float16 value."""
+    hs = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    want = hs.view(np.float16).astype(np.float64)
+    got = np.array([orc.f16_to_f64(int(h)) for h in hs])
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], want[~nan])
+
+
+def pin_f16_double(orc, n=4000, seed=13):
+    """One correct rounding of doubles to binary16: midpoints nudged by a few
+    double ulps, exact ties, the subnormal range and the overflow threshold."""
+    rng = np.random.default_rng(seed)
+    vals = []
+    for _ in range(n):
+        h = int(rng.integers(0x0001, 0x7BFF))
+        lo, hi = f16_val(h), f16_val(h + 1)
+        mid = (lo + hi) / 2
+        sgn = math.copysign(1.0, rng.standard_normal())
+        for d in (-3, -1, 0, 1, 3):
+            vals.append(sgn * (mid + d * math.ulp(mid)))
+    vals += [2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -26, 2.0 ** -14 - 2.0 ** -25, 65504.0,
+             65519.99, 65520.0, 65536.0, 1e6, -1e-9, 0.0, -0.0, 1.0 + 2.0 ** -11]
+    got = [orc.f64_to_f16(v) for v in vals]
+    want = [ref_f16(v) for v in vals]
+    assert got == want, "binary16 rounding of doubles is not a single correct rounding"
+
+
+def pin_f16_hand_example(orc):
+    gd, case = _hand_case()
+    with open(os.path.join(GOLDEN, "hand_2x8_f16.json")) as f:
+        g16 = json.load(f)
+    f16 = lambda vals: lib_f16_bits(np.asarray(vals, dtype=np.float32))
+    q = lambda qm, s, b: inputs.QuantMatrix(qm.packed, f16(s).reshape(2, 1), f16(b).reshape(2, 1), 8, 4)
+    c16 = inputs.Case(x=f16(gd["x"]).reshape(2, 8), gate=q(case.gate, gd["sg"], gd["bg"]),
+                      up=q(case.up, gd["su"], gd["bu"]), dtype="f16")
+    out, g, u = orc.qswiglu(*c16.oracle_args(), variant=MATCH, return_acc=True, dtype="f16")
+    assert np.array_equal(g, np.array(gd["g"])) and np.array_equal(u, np.array(gd["u"]))
+    assert np.array_equal(out, f16(g16["match"])), out
+    assert np.array_equal(orc.qswiglu(*c16.oracle_args(), variant=F32, dtype="f16"), f16(g16["f32"]))
+    dg = orc.qswiglu(*c16.oracle_args(), variant=DEBUG_GATE, dtype="f16")
+    du = orc.qswiglu(*c16.oracle_args(), variant=DEBUG_UP, dtype="f16")
+    sm = orc.silu_mul(dg.ravel(), du.ravel(), MATCH, dtype="f16").reshape(2, 2)
+    assert np.array_equal(sm, f16(g16["match"]))
+    # the same case read as bf16 gives the bf16 golden values: the dtype matters
+    assert not np.array_equal(f16(g16["match"]), lib_bf16_bits(np.asarray(gd["match"], np.float32)))
+
+
+def pin_f16_brute_force(orc):
+    cases = [
+        inputs.make_case(2, 64, 3, bits_g=4, gs_g=32, seed=14, dtype="f16"),
+        inputs.make_case(2, 64, 2, bits_g=8, gs_g=64, bits_u=2, gs_u=32, seed=15, dtype="f16",
+                         scale_range=(0.05, 0.3)),
+    ]
+    for case in cases:
+        for v in (MATCH, F32, DEBUG_GATE, DEBUG_UP):
+            got = orc.qswiglu(*case.oracle_args(), variant=v, dtype="f16")
+            want = brute_force(case, v)
+            assert np.array_equal(got, want), (case.meta, v, got, want)
+        y = orc.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, case.gate.gs,
+                    case.gate.bits, dtype="f16")
+        assert np.array_equal(y, brute_force(case, DEBUG_GATE))
+        w = orc.dequant(case.gate.packed, case.gate.scales, case.gate.biases, case.H, case.gate.gs,
+                        case.gate.bits, dtype="f16")
+        codes = np.array([ref_codes_from_words(r, case.H, case.gate.bits) for r in case.gate.packed])
+        for i in range(case.I):
+            for k in range(0, case.H, 7):
+                s = f16_val(int(case.gate.scales[i, k // case.gate.gs]))
+                b = f16_val(int(case.gate.biases[i, k // case.gate.gs]))
+                assert w[i, k] == f16_val(ref_f16(float(Fraction(s) * int(codes[i, k]) + Fraction(b))))
+
+
+def pin_f16_silu_exhaustive(orc):
+    """Every binary16 gate value in [-16, 16] through the elementwise step,
+    against the step-by-step definition in binary16."""
+    hs = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    vals = hs.view(np.float16).astype(np.float64)
+    g = hs[np.isfinite(vals) & (np.abs(vals) <= 16.0)]
+    for uval in (1.0, -3.0, 0.3):
+        u = lib_f16_bits(np.full(g.shape, uval, np.float32))
+        ub = f16_val(int(u[0]))
+        got_m = orc.silu_mul(g, u, MATCH, dtype="f16")
+        got_f = orc.silu_mul(g, u, F32, dtype="f16")
+        for j in range(0, g.size, 5):
+            gv = f16_val(int(g[j]))
+            sig = f16_val(ref_f16(1.0 / (1.0 + math.exp(-gv))))
+            assert got_m[j] == ref_f16(f16_val(ref_f16(gv * sig)) * ub), (gv, uval)
+            assert got_f[j] == ref_f16(gv * ub / (1.0 + math.exp(-gv))), (gv, uval)
+
+
 ALL_PINS = [pin_bf16_binary32, pin_bf16_double, pin_unpack, pin_hand_example,
             pin_zero_input, pin_integer_case, pin_brute_force, pin_k_permutation,
-            pin_silu_values, pin_silu_exhaustive, pin_match_is_unfused, pin_sampled_pairs]
+            pin_silu_values, pin_silu_exhaustive, pin_match_is_unfused, pin_sampled_pairs,
+            pin_f16_decode, pin_f16_double, pin_f16_hand_example, pin_f16_brute_force,
+            pin_f16_silu_exhaustive]
