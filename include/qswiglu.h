@@ -71,6 +71,15 @@ typedef enum {
     QSW_DEBUG_UP = 3     /* hidden := bf16(x . Wu^T), the stored up projection */
 } qsw_variant;
 
+/* Activation dtype of the *_ex entry points: x, the scales and biases of
+ * both operands, and the result (fusedSwigluSupported() accepts bf16 or f16
+ * activations; the dequantised weights, the stored projections and every MATCH
+ * rounding are in the same dtype).  The other entry points are bf16. */
+typedef enum {
+    QSW_ACT_BF16 = 0,
+    QSW_ACT_F16 = 1
+} qsw_act_dtype;
+
 /* Indices into the dispatch counters (fused-swiglu-kernel.ts keeps a call
  * counter so a test can prove the kernel ran). */
 enum {
@@ -172,7 +181,29 @@ QSW_API qsw_status qswiglu_forward_noalloc(const void *x, int64_t M, int64_t H, 
                            int gs_u, int bits_u,
                            int variant, void *out, void *stream);
 
-/* Stream-K mode of the *_ws and _noalloc entry points (qsw_stream_k_mode, default
+/*
+ * The general forms: qswiglu_forward_ws / affine_qmm_ws / qsw_silu_mul with an
+ * activation dtype (qsw_act_dtype; anything else returns QSW_ERR_INVALID_ARG).
+ * With QSW_ACT_F16, x, scales, biases and the result are IEEE binary16 bit
+ * patterns (same layouts and alignment), the dequantised weights are
+ * f16(s*q + b) and the tensor cores run on f16 operands; everything else
+ * (arguments, workspace, results, errors) is as for the bf16 forms.
+ */
+QSW_API qsw_status qswiglu_forward_ex(const void *x, int64_t M, int64_t H, int64_t I,
+                           const uint32_t *wg, const void *sg, const void *bg,
+                           int gs_g, int bits_g,
+                           const uint32_t *wu, const void *su, const void *bu,
+                           int gs_u, int bits_u,
+                           int variant, int act_dtype, void *out,
+                           void *workspace, size_t workspace_bytes, void *stream);
+QSW_API qsw_status affine_qmm_ex(const void *x, int64_t M, int64_t K, int64_t N,
+                      const uint32_t *w, const void *s, const void *b,
+                      int gs, int bits, int act_dtype, void *y,
+                      void *workspace, size_t workspace_bytes, void *stream);
+QSW_API qsw_status qsw_silu_mul_ex(const void *g, const void *u, int64_t n, int variant,
+                        int act_dtype, void *out, void *stream);
+
+/* Stream-K mode of the *_ws, *_ex and _noalloc entry points (qsw_stream_k_mode, default
  * QSW_STREAM_K_AUTO; other values are ignored).  Process-wide. */
 QSW_API void qsw_set_stream_k(int mode);
 QSW_API int qsw_get_stream_k(void);

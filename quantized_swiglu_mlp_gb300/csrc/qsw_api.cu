@@ -98,13 +98,14 @@ qsw_status check_workspace(const void *ws, size_t bytes, qsw::SplitWorkspace *ou
 // takes the library's static stream-K workspace (resolved only on that path).
 qsw_status fused_forward(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
                          const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su, const void *bu,
-                         int gs_u, int bits_u, int variant, void *out, void *workspace, size_t workspace_bytes,
-                         bool static_scratch, void *stream) {
+                         int gs_u, int bits_u, int variant, int act, void *out, void *workspace,
+                         size_t workspace_bytes, bool static_scratch, void *stream) {
   qsw_status st = check_shape(M, H, I);
   if (st != QSW_OK) return st;
   qsw::SplitWorkspace ws;
   if ((st = check_workspace(workspace, workspace_bytes, &ws)) != QSW_OK) return st;
   if (variant < QSW_MATCH || variant > QSW_DEBUG_UP) return QSW_ERR_INVALID_ARG;
+  if (act != QSW_ACT_BF16 && act != QSW_ACT_F16) return QSW_ERR_INVALID_ARG;
   if ((st = check_operand(wg, sg, bg, H, gs_g, bits_g)) != QSW_OK) return st;
   if ((st = check_operand(wu, su, bu, H, gs_u, bits_u)) != QSW_OK) return st;
   if (M == 0) return QSW_OK;   // nothing to read or write: x and out may be null
@@ -115,13 +116,14 @@ qsw_status fused_forward(const void *x, int64_t M, int64_t H, int64_t I, const u
   const qsw::QuantOperand u{wu, static_cast<const uint16_t *>(su), static_cast<const uint16_t *>(bu), gs_u, bits_u};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M <= gemv_max_m() && qsw::gemv_fits(M, H, I, g, &u, sm_count())) {
-    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count(),
+    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, act, out, s, g_timeout_ns.load(), sm_count(),
                                     g_early_weights.load(std::memory_order_relaxed) != 0));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
     if (static_scratch && qsw::prefill_static_workspace(sm_count(), s, &ws.ptr, &ws.bytes) != cudaSuccess)
       return QSW_ERR_CUDA;
-    st = from_cuda(qsw::launch_prefill(x, M, H, I, g, &u, variant, out, s, g_timeout_ns.load(), sm_count(), ws));
+    st = from_cuda(
+        qsw::launch_prefill(x, M, H, I, g, &u, variant, act, out, s, g_timeout_ns.load(), sm_count(), ws));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_TC].fetch_add(1, std::memory_order_relaxed);
   }
   return st;
@@ -131,12 +133,20 @@ qsw_status fused_forward(const void *x, int64_t M, int64_t H, int64_t I, const u
 
 extern "C" {
 
+qsw_status qswiglu_forward_ex(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
+                              const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su,
+                              const void *bu, int gs_u, int bits_u, int variant, int act_dtype, void *out,
+                              void *workspace, size_t workspace_bytes, void *stream) {
+  return fused_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, act_dtype, out,
+                       workspace, workspace_bytes, false, stream);
+}
+
 qsw_status qswiglu_forward_ws(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
                               const void *bg, int gs_g, int bits_g, const uint32_t *wu, const void *su,
                               const void *bu, int gs_u, int bits_u, int variant, void *out, void *workspace,
                               size_t workspace_bytes, void *stream) {
-  return fused_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, out, workspace,
-                       workspace_bytes, false, stream);
+  return fused_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, QSW_ACT_BF16, out,
+                       workspace, workspace_bytes, false, stream);
 }
 
 qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const uint32_t *wg, const void *sg,
@@ -146,13 +156,14 @@ qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const
                             stream);
 }
 
-qsw_status affine_qmm_ws(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
-                         const void *b, int gs, int bits, void *y, void *workspace, size_t workspace_bytes,
-                         void *stream) {
+qsw_status affine_qmm_ex(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
+                         const void *b, int gs, int bits, int act_dtype, void *y, void *workspace,
+                         size_t workspace_bytes, void *stream) {
   qsw_status st = check_shape(M, K, N);
   if (st != QSW_OK) return st;
   qsw::SplitWorkspace ws;
   if ((st = check_workspace(workspace, workspace_bytes, &ws)) != QSW_OK) return st;
+  if (act_dtype != QSW_ACT_BF16 && act_dtype != QSW_ACT_F16) return QSW_ERR_INVALID_ARG;
   if ((st = check_operand(w, s, b, K, gs, bits)) != QSW_OK) return st;
   if (M == 0) return QSW_OK;   // nothing to read or write: x and y may be null
   if (!x || !y) return QSW_ERR_INVALID_ARG;
@@ -161,15 +172,21 @@ qsw_status affine_qmm_ws(const void *x, int64_t M, int64_t K, int64_t N, const u
   const qsw::QuantOperand op{w, static_cast<const uint16_t *>(s), static_cast<const uint16_t *>(b), gs, bits};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (M <= gemv_max_m() && qsw::gemv_fits(M, K, N, op, nullptr, sm_count())) {
-    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs, g_timeout_ns.load(), sm_count(),
-                                    g_early_weights.load(std::memory_order_relaxed) != 0));
+    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, act_dtype, y, cs, g_timeout_ns.load(),
+                                    sm_count(), g_early_weights.load(std::memory_order_relaxed) != 0));
     if (st == QSW_OK) g_counters[QSW_CNT_QMM_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
-    st = from_cuda(qsw::launch_prefill(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, y, cs, g_timeout_ns.load(),
-                                       sm_count(), ws));
+    st = from_cuda(qsw::launch_prefill(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, act_dtype, y, cs,
+                                       g_timeout_ns.load(), sm_count(), ws));
     if (st == QSW_OK) g_counters[QSW_CNT_QMM_TC].fetch_add(1, std::memory_order_relaxed);
   }
   return st;
+}
+
+qsw_status affine_qmm_ws(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
+                         const void *b, int gs, int bits, void *y, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+  return affine_qmm_ex(x, M, K, N, w, s, b, gs, bits, QSW_ACT_BF16, y, workspace, workspace_bytes, stream);
 }
 
 qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
@@ -181,8 +198,8 @@ qsw_status qswiglu_forward_noalloc(const void *x, int64_t M, int64_t H, int64_t 
                                    const void *sg, const void *bg, int gs_g, int bits_g, const uint32_t *wu,
                                    const void *su, const void *bu, int gs_u, int bits_u, int variant, void *out,
                                    void *stream) {
-  return fused_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, out, nullptr, 0, true,
-                       stream);
+  return fused_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, QSW_ACT_BF16, out,
+                       nullptr, 0, true, stream);
 }
 
 size_t qsw_workspace_bytes(void) { return qsw::prefill_workspace_bytes(sm_count()); }
@@ -193,15 +210,22 @@ void qsw_set_stream_k(int mode) {
 
 int qsw_get_stream_k(void) { return g_stream_k.load(); }
 
-qsw_status qsw_silu_mul(const void *g, const void *u, int64_t n, int variant, void *out, void *stream) {
+qsw_status qsw_silu_mul_ex(const void *g, const void *u, int64_t n, int variant, int act_dtype, void *out,
+                           void *stream) {
   if (n < 0) return QSW_ERR_INVALID_ARG;
   if (variant != QSW_MATCH && variant != QSW_F32) return QSW_ERR_INVALID_ARG;
+  if (act_dtype != QSW_ACT_BF16 && act_dtype != QSW_ACT_F16) return QSW_ERR_INVALID_ARG;
   if (n == 0) return QSW_OK;
   if (!g || !u || !out) return QSW_ERR_INVALID_ARG;
   if (!aligned(g, 16) || !aligned(u, 16) || !aligned(out, 16)) return QSW_ERR_UNSUPPORTED;
-  const qsw_status st = from_cuda(qsw::launch_silu_mul(g, u, n, variant, out, static_cast<cudaStream_t>(stream)));
+  const qsw_status st =
+      from_cuda(qsw::launch_silu_mul(g, u, n, variant, act_dtype, out, static_cast<cudaStream_t>(stream)));
   if (st == QSW_OK) g_counters[QSW_CNT_SILU_MUL].fetch_add(1, std::memory_order_relaxed);
   return st;
+}
+
+qsw_status qsw_silu_mul(const void *g, const void *u, int64_t n, int variant, void *out, void *stream) {
+  return qsw_silu_mul_ex(g, u, n, variant, QSW_ACT_BF16, out, stream);
 }
 
 qsw_status qsw_check_device_errors(void *stream) {
@@ -246,6 +270,6 @@ const char *qsw_status_string(qsw_status s) {
   }
 }
 
-int qsw_version(void) { return 102; }
+int qsw_version(void) { return 103; }
 
 }  // extern "C"

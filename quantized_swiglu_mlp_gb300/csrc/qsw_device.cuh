@@ -12,6 +12,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -259,11 +260,12 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor: kind::f16 with bf16 A/B, f32 D, both K-major.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n) {
+// Instruction descriptor: kind::f16 with A and B both of `fmt` (0 f16,
+// 1 bf16: the two operands always share their type), f32 D, both K-major.
+__host__ __device__ constexpr uint32_t umma_idesc_f16kind(int m, int n, uint32_t fmt) {
   return (1u << 4)                                   // D format f32
-         | (1u << 7)                                 // A format bf16
-         | (1u << 10)                                // B format bf16
+         | (fmt << 7)                                // A format
+         | (fmt << 10)                               // B format
          | (static_cast<uint32_t>(n >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(m >> 4) << 24);    // M / 16
 }
@@ -308,8 +310,58 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 __device__ __forceinline__ float bf16x2_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16x2_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-// bf16 value 128 in both halves; (0x4300 | q) is the bf16 value 128 + q for q < 128.
-constexpr uint32_t kBf16x2_128 = 0x43004300u;
+// ------------------------------------------------------ activation dtype ----
+// The activation dtype T of x, the scales and biases, the dequantised weights
+// (the tensor-core operands) and hidden: bf16 or f16.  Each trait supplies
+// the paired (two values per 32-bit register) arithmetic the kernels use.
+
+struct ActBf16 {
+  static constexpr int kId = 0;
+  static constexpr uint32_t kUmmaFormat = 1;   // instruction-descriptor A/B format
+  // 128 in both halves: (0x4300 | q) is the bf16 value 128 + q for q < 128
+  static constexpr uint32_t kMagic2 = 0x43004300u;
+  __device__ __forceinline__ static uint32_t sub2(uint32_t a, uint32_t b) { return bf16x2_sub(a, b); }
+  __device__ __forceinline__ static uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) { return bf16x2_fma(a, b, c); }
+  __device__ __forceinline__ static uint32_t mul2(uint32_t a, uint32_t b) { return bf16x2_mul(a, b); }
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) { return pack_bf16x2(lo, hi); }
+  __device__ __forceinline__ static float lo(uint32_t v) { return bf16x2_lo(v); }
+  __device__ __forceinline__ static float hi(uint32_t v) { return bf16x2_hi(v); }
+  __device__ __forceinline__ static uint16_t store(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+};
+
+struct ActF16 {
+  static constexpr int kId = 1;
+  static constexpr uint32_t kUmmaFormat = 0;
+  // 1024 in both halves: (0x6400 | q) is the f16 value 1024 + q for q < 1024
+  static constexpr uint32_t kMagic2 = 0x64006400u;
+  __device__ __forceinline__ static uint32_t sub2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  __device__ __forceinline__ static uint32_t fma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+  }
+  __device__ __forceinline__ static uint32_t mul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+  }
+  __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+  }
+  __device__ __forceinline__ static float lo(uint32_t v) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xffffu)));
+  }
+  __device__ __forceinline__ static float hi(uint32_t v) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
+  }
+  __device__ __forceinline__ static uint16_t store(float v) { return __half_as_ushort(__float2half_rn(v)); }
+};
 
 // Exact integer code -> bf16 value for 8-bit codes: the byte is placed in the
 // mantissa of the f32 2^23 and 2^23 is subtracted (exact), then narrowed
@@ -320,16 +372,20 @@ __device__ __forceinline__ float code8_to_f32(uint32_t word, uint32_t byte_sel) 
 }
 
 // ----------------------------------------------------- dequantisation -------
-// Eight consecutive codes of one row -> eight bf16 weights w = bf16(s*q + b),
-// returned as four bf16x2 words.  `s2`/`b2` hold the group's scale and bias in
-// both halves.  The natural order puts code 2j in the low half of word j and
-// code 2j+1 in the high half (k order, as the tensor-core tile needs).
+// Eight consecutive codes of one row -> eight weights w = T(s*q + b) (one
+// rounding, fma.rn on the pair), returned as four T x2 words.  `s2`/`b2` hold
+// the group's scale and bias in both halves.  The natural order puts code 2j
+// in the low half of word j and code 2j+1 in the high half (k order, as the
+// tensor-core tile needs).  Codes of 2 and 4 bits become exact T values by
+// placing them in the mantissa of a power of two (A::kMagic2) and subtracting
+// it; 8-bit codes go through f32 for bf16 (128 + q overflows its 7-bit
+// mantissa), and the same way for f16.
 
-template <int BITS>
+template <int BITS, class A>
 struct Dequant8;
 
-template <>
-struct Dequant8<4> {
+template <class A>
+struct Dequant8<4, A> {
   // `w` holds the eight codes (code j at bits 4j).
   __device__ __forceinline__ static void natural(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
     const uint32_t v = w >> 4;   // low nibble of byte j of v = code 2j+1
@@ -337,8 +393,8 @@ struct Dequant8<4> {
     for (int j = 0; j < 4; ++j) {
       // byte j of w -> byte 0, byte j of v -> byte 2; keep the low nibbles
       const uint32_t t = prmt(w, v, static_cast<uint32_t>(j) | (static_cast<uint32_t>(4 + j) << 8));
-      const uint32_t q = bf16x2_sub(and_or(t, 0x000F000Fu, kBf16x2_128), kBf16x2_128);
-      o[j] = bf16x2_fma(q, s2, b2);
+      const uint32_t q = A::sub2(and_or(t, 0x000F000Fu, A::kMagic2), A::kMagic2);
+      o[j] = A::fma2(q, s2, b2);
     }
   }
   // Interleaved order (codes j and j+4 in word j): cheaper, used where the K
@@ -346,32 +402,32 @@ struct Dequant8<4> {
   __device__ __forceinline__ static void interleaved(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t q = bf16x2_sub(and_or(w >> (4 * j), 0x000F000Fu, kBf16x2_128), kBf16x2_128);
-      o[j] = bf16x2_fma(q, s2, b2);
+      const uint32_t q = A::sub2(and_or(w >> (4 * j), 0x000F000Fu, A::kMagic2), A::kMagic2);
+      o[j] = A::fma2(q, s2, b2);
     }
   }
 };
 
-template <>
-struct Dequant8<8> {
+template <class A>
+struct Dequant8<8, A> {
   // `w0` holds codes 0..3, `w1` codes 4..7 (one byte each).
   __device__ __forceinline__ static void natural(uint32_t w0, uint32_t w1, uint32_t s2, uint32_t b2,
                                                  uint32_t (&o)[4]) {
-    o[0] = bf16x2_fma(pack_bf16x2(code8_to_f32(w0, 0), code8_to_f32(w0, 1)), s2, b2);
-    o[1] = bf16x2_fma(pack_bf16x2(code8_to_f32(w0, 2), code8_to_f32(w0, 3)), s2, b2);
-    o[2] = bf16x2_fma(pack_bf16x2(code8_to_f32(w1, 0), code8_to_f32(w1, 1)), s2, b2);
-    o[3] = bf16x2_fma(pack_bf16x2(code8_to_f32(w1, 2), code8_to_f32(w1, 3)), s2, b2);
+    o[0] = A::fma2(A::pack2(code8_to_f32(w0, 0), code8_to_f32(w0, 1)), s2, b2);
+    o[1] = A::fma2(A::pack2(code8_to_f32(w0, 2), code8_to_f32(w0, 3)), s2, b2);
+    o[2] = A::fma2(A::pack2(code8_to_f32(w1, 0), code8_to_f32(w1, 1)), s2, b2);
+    o[3] = A::fma2(A::pack2(code8_to_f32(w1, 2), code8_to_f32(w1, 3)), s2, b2);
   }
   __device__ __forceinline__ static void interleaved(uint32_t w0, uint32_t w1, uint32_t s2, uint32_t b2,
                                                      uint32_t (&o)[4]) {
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      o[j] = bf16x2_fma(pack_bf16x2(code8_to_f32(w0, j), code8_to_f32(w1, j)), s2, b2);
+      o[j] = A::fma2(A::pack2(code8_to_f32(w0, j), code8_to_f32(w1, j)), s2, b2);
   }
 };
 
-template <>
-struct Dequant8<2> {
+template <class A>
+struct Dequant8<2, A> {
   // `h` holds the eight codes in its low 16 bits (code j at bits 2j).
   __device__ __forceinline__ static void natural(uint32_t h, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
     const uint32_t v2 = h >> 2, v4 = h >> 4, v6 = h >> 6;
@@ -384,8 +440,8 @@ struct Dequant8<2> {
     const uint32_t t[4] = {t0, t1, t2, t3};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t q = bf16x2_sub(and_or(t[j], 0x00030003u, kBf16x2_128), kBf16x2_128);
-      o[j] = bf16x2_fma(q, s2, b2);
+      const uint32_t q = A::sub2(and_or(t[j], 0x00030003u, A::kMagic2), A::kMagic2);
+      o[j] = A::fma2(q, s2, b2);
     }
   }
   __device__ __forceinline__ static void interleaved(uint32_t h, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) {
@@ -393,8 +449,8 @@ struct Dequant8<2> {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const uint32_t t = prmt(h >> (2 * j), 0u, 0x0100u);
-      const uint32_t q = bf16x2_sub(and_or(t, 0x00030003u, kBf16x2_128), kBf16x2_128);
-      o[j] = bf16x2_fma(q, s2, b2);
+      const uint32_t q = A::sub2(and_or(t, 0x00030003u, A::kMagic2), A::kMagic2);
+      o[j] = A::fma2(q, s2, b2);
     }
   }
 };
@@ -423,22 +479,29 @@ struct GroupDiv {
 
 enum : int { VAR_MATCH = 0, VAR_F32 = 1, VAR_DEBUG_GATE = 2, VAR_DEBUG_UP = 3 };
 
-__device__ __forceinline__ float round_bf16(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
-
 // sigma(v) = 1 / (1 + e^-v) with the hardware exponential and reciprocal
 // approximations: branch-free, so an epilogue thread overlaps the 16 elements
-// it holds.  Their few-ulp f32 error is far below the bf16 rounding that
-// follows; for v < -88 the denominator overflows and sigma is 0 (the true value
-// is below 2^-126).
+// it holds.  Their few-ulp f32 error is far below the rounding to the
+// activation dtype that follows; for v < -88 the denominator overflows and
+// sigma is 0 (the true value is below 2^-126).
 __device__ __forceinline__ float sigmoid_fast(float v) { return __fdividef(1.0f, 1.0f + __expf(-v)); }
 
-// hidden = silu(g) * u for one element, from the f32 projections.
+// v rounded to the activation dtype and back (exact widening).
+template <class A>
+__device__ __forceinline__ float round_act(float v) {
+  const uint32_t p = A::pack2(v, 0.0f);
+  return A::lo(p);
+}
+
+// hidden = silu(g) * u for one element, from the f32 projections; the caller
+// rounds the result to the activation dtype at the store.
+template <class A>
 __device__ __forceinline__ float swiglu_epilogue(int variant, float g, float u) {
   if (variant == VAR_MATCH) {
-    const float gb = round_bf16(g), ub = round_bf16(u);
-    const float sig = round_bf16(sigmoid_fast(gb));
-    const float silu = round_bf16(gb * sig);
-    return silu * ub;   // exact product of two bf16; rounded once by the caller's store
+    const float gb = round_act<A>(g), ub = round_act<A>(u);
+    const float sig = round_act<A>(sigmoid_fast(gb));
+    const float silu = round_act<A>(gb * sig);
+    return silu * ub;   // exact product of two T values; rounded once by the caller's store
   }
   if (variant == VAR_F32) return (g * sigmoid_fast(g)) * u;
   return variant == VAR_DEBUG_GATE ? g : u;
@@ -447,13 +510,14 @@ __device__ __forceinline__ float swiglu_epilogue(int variant, float g, float u) 
 // The MATCH epilogue of two elements at once, (g0, u0) in the low half of the
 // result and (g1, u1) in the high half: the same roundings as
 // swiglu_epilogue(VAR_MATCH) followed by the store's rounding, since a product
-// of two bf16 values is exact in f32 and mul.rn.bf16x2 rounds that exact
-// product to nearest even.  Bit-identical to the scalar form, in about half
-// the instructions.
+// of two bf16 (or two f16) values is exact in f32 and mul.rn on the pair
+// rounds that exact product to nearest even.  Bit-identical to the scalar
+// form, in about half the instructions.
+template <class A>
 __device__ __forceinline__ uint32_t swiglu_match2(float g0, float g1, float u0, float u1) {
-  const uint32_t gb = pack_bf16x2(g0, g1), ub = pack_bf16x2(u0, u1);
-  const uint32_t sig = pack_bf16x2(sigmoid_fast(bf16x2_lo(gb)), sigmoid_fast(bf16x2_hi(gb)));
-  return bf16x2_mul(bf16x2_mul(gb, sig), ub);
+  const uint32_t gb = A::pack2(g0, g1), ub = A::pack2(u0, u1);
+  const uint32_t sig = A::pack2(sigmoid_fast(A::lo(gb)), sigmoid_fast(A::hi(gb)));
+  return A::mul2(A::mul2(gb, sig), ub);
 }
 
 }  // namespace qsw

@@ -19,7 +19,8 @@
 //  * x is the same for every unit: it is staged once per CTA in shared memory,
 //    already permuted into MMA B-fragment order (bank-conflict-free reads).
 //  * a lane (g = lane/4, c = lane%4) dequantises 32 codes of gate row g and of
-//    up row g to bf16 in registers (w = bf16(s*q + b), one rounding) and feeds
+//    up row g to the activation dtype T (bf16 or f16) in registers
+//    (w = T(s*q + b), one rounding) and feeds
 //    them as A rows g and g+8 of mma.sync m16n8k16 with x (8 rows, zero padded)
 //    as B: one MMA yields gate and up of the same outputs.  The K order inside
 //    each 8-code group is interleaved (codes j, j+4); x is permuted the same way.
@@ -69,12 +70,22 @@ struct GemvParams {
   uint64_t timeout_ns;
 };
 
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// D += A . B, m16n8k16, f32 accumulators, A and B in the activation dtype.
+template <class A>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  if constexpr (A::kId == ActF16::kId) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
 }
 
 __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -102,7 +113,7 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
 }
 
 // 32 codes of one row (the lane's chunk of a 128-code block), from shared memory.
-template <int BITS>
+template <int BITS, class A>
 struct Chunk {
   static constexpr int kWords = kChunk * BITS / 32;   // 4, 8 or 2
   uint32_t w[kWords];
@@ -125,11 +136,11 @@ struct Chunk {
   // eight codes (sub-chunk j), interleaved pairing (codes p, p+4 in word p)
   __device__ __forceinline__ void dequant(int j, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) const {
     if constexpr (BITS == 4) {
-      Dequant8<4>::interleaved(w[j], s2, b2, o);
+      Dequant8<4, A>::interleaved(w[j], s2, b2, o);
     } else if constexpr (BITS == 8) {
-      Dequant8<8>::interleaved(w[2 * j], w[2 * j + 1], s2, b2, o);
+      Dequant8<8, A>::interleaved(w[2 * j], w[2 * j + 1], s2, b2, o);
     } else {
-      Dequant8<2>::interleaved(w[j >> 1] >> (16 * (j & 1)), s2, b2, o);
+      Dequant8<2, A>::interleaved(w[j >> 1] >> (16 * (j & 1)), s2, b2, o);
     }
   }
 };
@@ -162,7 +173,7 @@ __device__ __forceinline__ void issue_unit(const GemvParams &p, uint8_t *base, u
   }
 }
 
-template <int BITS0, int BITS1, bool DUAL, int NG>
+template <int BITS0, int BITS1, bool DUAL, int NG, class A>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
   constexpr int R = DUAL ? 8 : 16;          // output rows per unit
   constexpr int BB = DUAL ? BITS1 : BITS0;
@@ -325,8 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
       // replaced by zeros, and every lane runs the MMAs
       const uint32_t k = kb * kBlockK + c * kChunk;
       const bool kval = k < K;
-      Chunk<BITS0> ca;
-      Chunk<BB> cb;
+      Chunk<BITS0, A> ca;
+      Chunk<BB, A> cb;
       uint32_t sa = 0, ba = 0, sb = 0, bb = 0;
       if (kval) {
         ca.load(rowa + kb * (kBlockK * BITS0 / 8));
@@ -338,9 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
         bb = lds_u16(b_b + ib);
       } else {
 #pragma unroll
-        for (int q = 0; q < Chunk<BITS0>::kWords; ++q) ca.w[q] = 0;
+        for (int q = 0; q < Chunk<BITS0, A>::kWords; ++q) ca.w[q] = 0;
 #pragma unroll
-        for (int q = 0; q < Chunk<BB>::kWords; ++q) cb.w[q] = 0;
+        for (int q = 0; q < Chunk<BB, A>::kWords; ++q) cb.w[q] = 0;
       }
       __syncwarp();
       const uint32_t sa2 = splat_bf16(static_cast<uint16_t>(sa)), ba2 = splat_bf16(static_cast<uint16_t>(ba));
@@ -362,8 +373,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
           // k_local 2c+8,2c+9 <- pair 2h+1
           const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
           const uint32_t a1[4] = {pa[2], pb[2], pa[3], pb[3]};
-          mma_bf16_16816(acc[G], a0, xf.x, xf.y);
-          mma_bf16_16816(acc[G], a1, xf.z, xf.w);
+          mma_16816<A>(acc[G], a0, xf.x, xf.y);
+          mma_16816<A>(acc[G], a1, xf.z, xf.w);
         }
       }
 #pragma unroll
@@ -426,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
           s0 += rw[qa];
           if (DUAL) s1 += rw[(n & 1) + 2];
         }
-        const float v = DUAL ? swiglu_epilogue(p.variant, s0, s1) : s0;
-        p.out[static_cast<int64_t>(m) * p.N + i_out] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+        const float v = DUAL ? swiglu_epilogue<A>(p.variant, s0, s1) : s0;
+        p.out[static_cast<int64_t>(m) * p.N + i_out] = A::store(v);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(rfree);
@@ -480,7 +491,7 @@ Layout plan(int64_t K, int64_t N, int M, int gs0, int gs1, int bits0, int bits1,
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int BITS0, int BITS1, bool DUAL, int NG>
+template <int BITS0, int BITS1, bool DUAL, int NG, class A>
 cudaError_t launch_cfg(GemvParams p, const Layout &l, cudaStream_t stream, int num_sms) {
   constexpr int R = DUAL ? 8 : 16;
   p.pitch0 = p.K * BITS0 / 8;
@@ -497,7 +508,7 @@ cudaError_t launch_cfg(GemvParams p, const Layout &l, cudaStream_t stream, int n
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(attr_done.load() & (uint64_t(1) << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<BITS0, BITS1, DUAL, NG>,
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<BITS0, BITS1, DUAL, NG, A>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(uint64_t(1) << dev);
@@ -512,23 +523,42 @@ cudaError_t launch_cfg(GemvParams p, const Layout &l, cudaStream_t stream, int n
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.early ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_kernel<BITS0, BITS1, DUAL, NG>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_kernel<BITS0, BITS1, DUAL, NG, A>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int BITS0, int BITS1, bool DUAL>
+template <int BITS0, int BITS1, bool DUAL, class A>
 cudaError_t launch_ng(const GemvParams &p, const Layout &l, cudaStream_t stream, int num_sms) {
-  if (p.M <= 8) return launch_cfg<BITS0, BITS1, DUAL, 1>(p, l, stream, num_sms);
-  if (p.M <= 16) return launch_cfg<BITS0, BITS1, DUAL, 2>(p, l, stream, num_sms);
-  return launch_cfg<BITS0, BITS1, DUAL, 4>(p, l, stream, num_sms);
+  if (p.M <= 8) return launch_cfg<BITS0, BITS1, DUAL, 1, A>(p, l, stream, num_sms);
+  if (p.M <= 16) return launch_cfg<BITS0, BITS1, DUAL, 2, A>(p, l, stream, num_sms);
+  return launch_cfg<BITS0, BITS1, DUAL, 4, A>(p, l, stream, num_sms);
 }
 
-template <int BITS0>
+template <int BITS0, class A>
 cudaError_t launch_dual_bits1(const GemvParams &p, const Layout &l, int bits1, cudaStream_t stream, int num_sms) {
   switch (bits1) {
-    case 2: return launch_ng<BITS0, 2, true>(p, l, stream, num_sms);
-    case 4: return launch_ng<BITS0, 4, true>(p, l, stream, num_sms);
-    case 8: return launch_ng<BITS0, 8, true>(p, l, stream, num_sms);
+    case 2: return launch_ng<BITS0, 2, true, A>(p, l, stream, num_sms);
+    case 4: return launch_ng<BITS0, 4, true, A>(p, l, stream, num_sms);
+    case 8: return launch_ng<BITS0, 8, true, A>(p, l, stream, num_sms);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class A>
+cudaError_t launch_act(const GemvParams &p, const Layout &l, int bits0, int bits1, bool dual, cudaStream_t stream,
+                       int num_sms) {
+  if (dual) {
+    switch (bits0) {
+      case 2: return launch_dual_bits1<2, A>(p, l, bits1, stream, num_sms);
+      case 4: return launch_dual_bits1<4, A>(p, l, bits1, stream, num_sms);
+      case 8: return launch_dual_bits1<8, A>(p, l, bits1, stream, num_sms);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (bits0) {
+    case 2: return launch_ng<2, 2, false, A>(p, l, stream, num_sms);
+    case 4: return launch_ng<4, 4, false, A>(p, l, stream, num_sms);
+    case 8: return launch_ng<8, 8, false, A>(p, l, stream, num_sms);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -546,7 +576,7 @@ bool gemv_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const Q
 }
 
 cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                        const QuantOperand *op1, int variant, void *out, cudaStream_t stream,
+                        const QuantOperand *op1, int variant, int act, void *out, cudaStream_t stream,
                         uint64_t timeout_ns, int num_sms, bool early_weights) {
   if (!gemv_fits(M, K, N, op0, op1, num_sms)) return cudaErrorInvalidValue;
   const QuantOperand &o1 = op1 ? *op1 : op0;
@@ -570,20 +600,9 @@ cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   p.out = static_cast<uint16_t *>(out);
   p.timeout_ns = timeout_ns;
   p.early = early_weights ? 1 : 0;
-  if (op1) {
-    switch (op0.bits) {
-      case 2: return launch_dual_bits1<2>(p, l, op1->bits, stream, num_sms);
-      case 4: return launch_dual_bits1<4>(p, l, op1->bits, stream, num_sms);
-      case 8: return launch_dual_bits1<8>(p, l, op1->bits, stream, num_sms);
-      default: return cudaErrorInvalidValue;
-    }
-  }
-  switch (op0.bits) {
-    case 2: return launch_ng<2, 2, false>(p, l, stream, num_sms);
-    case 4: return launch_ng<4, 4, false>(p, l, stream, num_sms);
-    case 8: return launch_ng<8, 8, false>(p, l, stream, num_sms);
-    default: return cudaErrorInvalidValue;
-  }
+  if (act == ActF16::kId) return launch_act<ActF16>(p, l, op0.bits, o1.bits, op1 != nullptr, stream, num_sms);
+  if (act == ActBf16::kId) return launch_act<ActBf16>(p, l, op0.bits, o1.bits, op1 != nullptr, stream, num_sms);
+  return cudaErrorInvalidValue;
 }
 
 // Read and clear the device error word of this translation unit's kernels.

@@ -242,7 +242,7 @@ __device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
 // 16 consecutive codes of one row (quarter q of a K step) -> two 16-byte
 // chunks of bf16 weights, stored at the swizzled positions of chunks 2q and
 // 2q+1 of B-tile row `row`.
-template <int BITS>
+template <int BITS, class A>
 __device__ __forceinline__ void dequant16(uint32_t codes_addr, uint32_t s2, uint32_t b2, uint32_t brow_addr, int row,
                                           int q) {
   uint32_t w[BITS / 2 > 0 ? BITS / 2 : 1];   // 16 codes = BITS/2 words
@@ -263,11 +263,11 @@ __device__ __forceinline__ void dequant16(uint32_t codes_addr, uint32_t s2, uint
   for (int i = 0; i < 2; ++i) {   // chunk i: codes 8i .. 8i+7 of the 16
     uint32_t o[4];
     if constexpr (BITS == 4) {
-      Dequant8<4>::natural(w[i], s2, b2, o);
+      Dequant8<4, A>::natural(w[i], s2, b2, o);
     } else if constexpr (BITS == 8) {
-      Dequant8<8>::natural(w[2 * i], w[2 * i + 1], s2, b2, o);
+      Dequant8<8, A>::natural(w[2 * i], w[2 * i + 1], s2, b2, o);
     } else {
-      Dequant8<2>::natural(w[0] >> (16 * i), s2, b2, o);
+      Dequant8<2, A>::natural(w[0] >> (16 * i), s2, b2, o);
     }
     // 128-byte swizzle: 16-byte chunk c of row n lands at chunk c ^ (n mod 8)
     const int c = 2 * q + i;
@@ -275,21 +275,21 @@ __device__ __forceinline__ void dequant16(uint32_t codes_addr, uint32_t s2, uint
   }
 }
 
-// SwiGLU epilogue of 16 (gate, up) accumulator pairs -> 8 packed bf16 pairs.
-template <int VARIANT>
+// SwiGLU epilogue of 16 (gate, up) accumulator pairs -> 8 packed pairs of T.
+template <int VARIANT, class A>
 __device__ __forceinline__ void epilogue16(const uint32_t (&g)[16], const uint32_t (&u)[16], uint32_t (&out)[8]) {
 #pragma unroll
   for (int e = 0; e < 16; e += 2) {
     if (VARIANT == VAR_MATCH)
-      out[e / 2] = swiglu_match2(__uint_as_float(g[e]), __uint_as_float(g[e + 1]), __uint_as_float(u[e]),
-                                 __uint_as_float(u[e + 1]));
+      out[e / 2] = swiglu_match2<A>(__uint_as_float(g[e]), __uint_as_float(g[e + 1]), __uint_as_float(u[e]),
+                                    __uint_as_float(u[e + 1]));
     else
-      out[e / 2] = pack_bf16x2(swiglu_epilogue(VARIANT, __uint_as_float(g[e]), __uint_as_float(u[e])),
-                               swiglu_epilogue(VARIANT, __uint_as_float(g[e + 1]), __uint_as_float(u[e + 1])));
+      out[e / 2] = A::pack2(swiglu_epilogue<A>(VARIANT, __uint_as_float(g[e]), __uint_as_float(u[e])),
+                            swiglu_epilogue<A>(VARIANT, __uint_as_float(g[e + 1]), __uint_as_float(u[e + 1])));
   }
 }
 
-template <int BITS0, int BITS1, bool DUAL>
+template <int BITS0, int BITS1, bool DUAL, class A>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_c0,
                    const __grid_constant__ CUtensorMap tm_c1, const __grid_constant__ CUtensorMap tm_s0,
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue --
     if (lane == 0) {
-      constexpr uint32_t kIdesc = umma_idesc_bf16(UM, BN);
+      constexpr uint32_t kIdesc = umma_idesc_f16kind(UM, BN, A::kUmmaFormat);
       int n_x = 0, n_b = 0;
       bool ok = true;
       // Chains of at most kChainSteps K steps (see the accumulation note at the
@@ -633,9 +633,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t caddr = sbase + c_row + static_cast<uint32_t>(cs * C::kCodesBytes);
         const uint32_t baddr = sbase + static_cast<uint32_t>(C::kBOff + bs * kBBytes + row * 128);
         if (op == 0)
-          dequant16<BITS0>(caddr, s2, b2, baddr, row, q);
+          dequant16<BITS0, A>(caddr, s2, b2, baddr, row, q);
         else
-          dequant16<BITS1>(caddr, s2, b2, baddr, row, q);
+          dequant16<BITS1, A>(caddr, s2, b2, baddr, row, q);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -789,15 +789,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (DUAL) {
                 // one variant per launch: dispatch once, then 16 branch-free elements
                 switch (p.variant) {
-                  case VAR_MATCH: epilogue16<VAR_MATCH>(ra, rb, packed); break;
-                  case VAR_F32: epilogue16<VAR_F32>(ra, rb, packed); break;
-                  case VAR_DEBUG_GATE: epilogue16<VAR_DEBUG_GATE>(ra, rb, packed); break;
-                  default: epilogue16<VAR_DEBUG_UP>(ra, rb, packed); break;
+                  case VAR_MATCH: epilogue16<VAR_MATCH, A>(ra, rb, packed); break;
+                  case VAR_F32: epilogue16<VAR_F32, A>(ra, rb, packed); break;
+                  case VAR_DEBUG_GATE: epilogue16<VAR_DEBUG_GATE, A>(ra, rb, packed); break;
+                  default: epilogue16<VAR_DEBUG_UP, A>(ra, rb, packed); break;
                 }
               } else {
 #pragma unroll
                 for (int e = 0; e < 16; e += 2)
-                  packed[e / 2] = pack_bf16x2(__uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
+                  packed[e / 2] = A::pack2(__uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
               }
               const int64_t col = n0 + c0;
               if (vec_ok && col + 16 <= p.N) {
@@ -929,13 +929,15 @@ void plan_split(int64_t tiles, int64_t k_steps, int num_sms, int mode, bool have
   *sk_tiles = static_cast<int>(tiles);
 }
 
-template <int BITS0, int BITS1, bool DUAL>
+template <int BITS0, int BITS1, bool DUAL, class A>
 cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                         const QuantOperand *op1, int variant, void *out, cudaStream_t stream, uint64_t timeout_ns,
                         int num_sms, const SplitWorkspace &ws) {
   using C = Cfg<BITS0, BITS1, DUAL>;
   CUtensorMap tm_x, tm_c0, tm_c1, tm_s0, tm_b0, tm_s1, tm_b1;
-  if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, K, M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
+  const CUtensorMapDataType x_type = A::kId == ActF16::kId ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!encode_2d(&tm_x, x_type, 2, x, K, M, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_2d(&tm_c0, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, op0.w, K * BITS0 / 32, N, BK * BITS0 / 32, C::kRows0,
                  CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -987,24 +989,44 @@ cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(attr_done.load() & (uint64_t(1) << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<BITS0, BITS1, DUAL>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<BITS0, BITS1, DUAL, A>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(uint64_t(1) << dev);
   }
-  prefill_kernel<BITS0, BITS1, DUAL><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_x, tm_c0, tm_c1, tm_s0, tm_b0,
+  prefill_kernel<BITS0, BITS1, DUAL, A><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_x, tm_c0, tm_c1, tm_s0, tm_b0,
                                                                                  tm_s1, tm_b1, p);
   return cudaGetLastError();
 }
 
-template <int BITS0>
+template <int BITS0, class A>
 cudaError_t dual_bits1(int bits1, const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                        const QuantOperand *op1, int variant, void *out, cudaStream_t stream, uint64_t timeout_ns,
                        int num_sms, const SplitWorkspace &ws) {
   switch (bits1) {
-    case 2: return launch_impl<BITS0, 2, true>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-    case 4: return launch_impl<BITS0, 4, true>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-    case 8: return launch_impl<BITS0, 8, true>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+    case 2: return launch_impl<BITS0, 2, true, A>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+    case 4: return launch_impl<BITS0, 4, true, A>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+    case 8: return launch_impl<BITS0, 8, true, A>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class A>
+cudaError_t launch_act(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
+                       const QuantOperand *op1, int variant, void *out, cudaStream_t stream, uint64_t timeout_ns,
+                       int num_sms, const SplitWorkspace &ws) {
+  if (op1) {
+    switch (op0.bits) {
+      case 2: return dual_bits1<2, A>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+      case 4: return dual_bits1<4, A>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+      case 8: return dual_bits1<8, A>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (op0.bits) {
+    case 2: return launch_impl<2, 2, false, A>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
+    case 4: return launch_impl<4, 4, false, A>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
+    case 8: return launch_impl<8, 8, false, A>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1038,22 +1060,11 @@ cudaError_t prefill_static_workspace(int num_sms, cudaStream_t stream, void **pt
 }
 
 cudaError_t launch_prefill(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                           const QuantOperand *op1, int variant, void *out, cudaStream_t stream,
+                           const QuantOperand *op1, int variant, int act, void *out, cudaStream_t stream,
                            uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws) {
-  if (op1) {
-    switch (op0.bits) {
-      case 2: return dual_bits1<2>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-      case 4: return dual_bits1<4>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-      case 8: return dual_bits1<8>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-      default: return cudaErrorInvalidValue;
-    }
-  }
-  switch (op0.bits) {
-    case 2: return launch_impl<2, 2, false>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
-    case 4: return launch_impl<4, 4, false>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
-    case 8: return launch_impl<8, 8, false>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
-    default: return cudaErrorInvalidValue;
-  }
+  if (act == ActF16::kId) return launch_act<ActF16>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+  if (act == ActBf16::kId) return launch_act<ActBf16>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+  return cudaErrorInvalidValue;
 }
 
 // Read and clear the device error word of this translation unit's kernels.

@@ -6,10 +6,12 @@ passed to the C entry points, which enqueue the CUDA kernels.  There is no
 fallback: if the library is missing or a call fails, these functions raise.
 
 Tensor conventions (torch, all on one CUDA device, contiguous):
-  x            bfloat16 [M, H]           (leading dims are flattened into M)
+  x            bfloat16 or float16 [M, H]   (leading dims are flattened into M)
   w            int32 or uint32 [rows, H*bits/32]  packed codes, little-endian
-  scales/biases bfloat16 [rows, H/gs]
-  result       bfloat16 [M, rows]
+  scales/biases x's dtype [rows, H/gs]
+  result       x's dtype [M, rows]
+The activation dtype (bf16 or f16) is taken from x; the calls go to the
+library's *_ex entry points with that dtype.
 """
 from __future__ import annotations
 
@@ -29,8 +31,9 @@ NUM_COUNTERS = 5
 STATUS = {0: "QSW_OK", 1: "QSW_ERR_INVALID_ARG", 2: "QSW_ERR_UNSUPPORTED", 3: "QSW_ERR_CUDA",
           4: "QSW_ERR_TIMEOUT"}
 STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS = 0, 1, 2
+ACT_BF16, ACT_F16 = 0, 1
 EXPORTED = ("qswiglu_forward", "affine_qmm", "qswiglu_forward_ws", "affine_qmm_ws", "qswiglu_forward_noalloc",
-            "qsw_workspace_bytes",
+            "qswiglu_forward_ex", "affine_qmm_ex", "qsw_silu_mul_ex", "qsw_workspace_bytes",
             "qsw_set_stream_k", "qsw_get_stream_k", "qsw_silu_mul", "qsw_check_device_errors",
             "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_early_weight_stream",
             "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns",
@@ -69,6 +72,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.qsw_workspace_bytes.restype = sz
         lib.qswiglu_forward_noalloc.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, p, p]
         lib.qswiglu_forward_noalloc.restype = i32
+        lib.qswiglu_forward_ex.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, i32, p,
+                                           p, sz, p]
+        lib.qswiglu_forward_ex.restype = i32
+        lib.affine_qmm_ex.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, i32, p, p, sz, p]
+        lib.affine_qmm_ex.restype = i32
+        lib.qsw_silu_mul_ex.argtypes = [p, p, i64, i32, i32, p, p]
+        lib.qsw_silu_mul_ex.restype = i32
         lib.qsw_set_stream_k.argtypes = [i32]
         lib.qsw_get_stream_k.restype = i32
         lib.qsw_silu_mul.argtypes = [p, p, i64, i32, p, p]
@@ -118,12 +128,13 @@ def _need(t: torch.Tensor, name: str, dtypes, device=None) -> torch.Tensor:
 
 _PACKED = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
 _BF16 = (torch.bfloat16,)
+_ACT = {torch.bfloat16: ACT_BF16, torch.float16: ACT_F16}
 
 
-def _operand(w, s, b, name, device, K, bits, gs):
+def _operand(w, s, b, name, device, K, bits, gs, dtype=torch.bfloat16):
     _need(w, f"{name} packed weights", _PACKED, device)
-    _need(s, f"{name} scales", _BF16, device)
-    _need(b, f"{name} biases", _BF16, device)
+    _need(s, f"{name} scales", (dtype,), device)
+    _need(b, f"{name} biases", (dtype,), device)
     rows = w.shape[0]
     if w.dim() != 2 or w.shape[1] * 32 != K * bits:
         raise ValueError(f"{name} packed weights must be [rows, K*bits/32], got {tuple(w.shape)}")
@@ -188,42 +199,38 @@ def qswiglu_forward(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, varia
     """hidden = silu(x . Wg^T) * (x . Wu^T) on the GPU; returns bf16 [..., I].
 
     workspace: "auto" (the per-stream workspace of workspace()), None (whole
-    tiles only: the plain qswiglu_forward entry point) or a zero-initialised
-    uint8 tensor of at least workspace_bytes() bytes owned by the caller.
+    tiles only) or a zero-initialised uint8 tensor of at least
+    workspace_bytes() bytes owned by the caller.  x may be bfloat16 or float16;
+    scales, biases and the result share its dtype.
     """
     lib = load_library()
-    _need(x, "x", _BF16)
+    _need(x, "x", tuple(_ACT))
+    dt = x.dtype
     H = x.shape[-1]
     x2 = x.reshape(-1, H)
     M = x2.shape[0]
-    I = _operand(wg, sg, bg, "gate", x.device, H, bits_g, gs_g)
-    if _operand(wu, su, bu, "up", x.device, H, bits_u, gs_u) != I:
+    I = _operand(wg, sg, bg, "gate", x.device, H, bits_g, gs_g, dt)
+    if _operand(wu, su, bu, "up", x.device, H, bits_u, gs_u, dt) != I:
         raise ValueError("gate and up must have the same number of rows")
     if out is None:
-        out = torch.empty((M, I), dtype=torch.bfloat16, device=x.device)
+        out = torch.empty((M, I), dtype=dt, device=x.device)
     else:
-        _need(out, "out", _BF16, x.device)
+        _need(out, "out", (dt,), x.device)
         if out.numel() != M * I:
             raise ValueError("out has the wrong size")
     ws_ptr, ws_bytes = _workspace_arg(workspace, x.device, stream)
-    if ws_ptr is None:
-        code = lib.qswiglu_forward(x2.data_ptr(), M, H, I, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(),
-                                   int(gs_g), int(bits_g), wu.data_ptr(), su.data_ptr(), bu.data_ptr(),
-                                   int(gs_u), int(bits_u), int(variant), out.data_ptr(), _stream_ptr(stream))
-        _check("qswiglu_forward", code)
-    else:
-        code = lib.qswiglu_forward_ws(x2.data_ptr(), M, H, I, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(),
-                                      int(gs_g), int(bits_g), wu.data_ptr(), su.data_ptr(), bu.data_ptr(),
-                                      int(gs_u), int(bits_u), int(variant), out.data_ptr(), ws_ptr, ws_bytes,
-                                      _stream_ptr(stream))
-        _check("qswiglu_forward_ws", code)
+    code = lib.qswiglu_forward_ex(x2.data_ptr(), M, H, I, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(),
+                                  int(gs_g), int(bits_g), wu.data_ptr(), su.data_ptr(), bu.data_ptr(),
+                                  int(gs_u), int(bits_u), int(variant), _ACT[dt], out.data_ptr(), ws_ptr,
+                                  ws_bytes, _stream_ptr(stream))
+    _check("qswiglu_forward_ex", code)
     return out.view(*x.shape[:-1], I)
 
 
 def qswiglu_forward_noalloc(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant=MATCH,
                             out=None, stream=None) -> torch.Tensor:
-    """qswiglu_forward with stream-K scheduling on the library's static scratch
-    array (no workspace); calls through it must not run concurrently."""
+    """qswiglu_forward (bf16) with stream-K scheduling on the library's static
+    scratch array (no workspace); calls through it must not run concurrently."""
     lib = load_library()
     _need(x, "x", _BF16)
     H = x.shape[-1]
@@ -248,47 +255,43 @@ def qswiglu_forward_noalloc(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_
 def affine_qmm(x, w, s, b, gs, bits, y=None, stream=None, workspace="auto") -> torch.Tensor:
     """y = bf16(x . W^T) with W affine-quantised; returns bf16 [..., N].
 
-    workspace: as for qswiglu_forward.
+    workspace: as for qswiglu_forward; x may be bfloat16 or float16.
     """
     lib = load_library()
-    _need(x, "x", _BF16)
+    _need(x, "x", tuple(_ACT))
+    dt = x.dtype
     K = x.shape[-1]
     x2 = x.reshape(-1, K)
     M = x2.shape[0]
-    N = _operand(w, s, b, "w", x.device, K, bits, gs)
+    N = _operand(w, s, b, "w", x.device, K, bits, gs, dt)
     if y is None:
-        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+        y = torch.empty((M, N), dtype=dt, device=x.device)
     else:
-        _need(y, "y", _BF16, x.device)
+        _need(y, "y", (dt,), x.device)
         if y.numel() != M * N:
             raise ValueError("y has the wrong size")
     ws_ptr, ws_bytes = _workspace_arg(workspace, x.device, stream)
-    if ws_ptr is None:
-        code = lib.affine_qmm(x2.data_ptr(), M, K, N, w.data_ptr(), s.data_ptr(), b.data_ptr(),
-                              int(gs), int(bits), y.data_ptr(), _stream_ptr(stream))
-        _check("affine_qmm", code)
-    else:
-        code = lib.affine_qmm_ws(x2.data_ptr(), M, K, N, w.data_ptr(), s.data_ptr(), b.data_ptr(),
-                                 int(gs), int(bits), y.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream))
-        _check("affine_qmm_ws", code)
+    code = lib.affine_qmm_ex(x2.data_ptr(), M, K, N, w.data_ptr(), s.data_ptr(), b.data_ptr(),
+                             int(gs), int(bits), _ACT[dt], y.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream))
+    _check("affine_qmm_ex", code)
     return y.view(*x.shape[:-1], N)
 
 
 def qsw_silu_mul(g, u, variant=MATCH, out=None, stream=None) -> torch.Tensor:
-    """out = silu(g) * u elementwise over bf16 tensors of equal shape."""
+    """out = silu(g) * u elementwise over bf16 (or float16) tensors of equal shape."""
     lib = load_library()
-    _need(g, "g", _BF16)
-    _need(u, "u", _BF16, g.device)
+    _need(g, "g", tuple(_ACT))
+    _need(u, "u", (g.dtype,), g.device)
     if g.shape != u.shape:
         raise ValueError("g and u must have the same shape")
     if out is None:
         out = torch.empty_like(g)
     else:
-        _need(out, "out", _BF16, g.device)
+        _need(out, "out", (g.dtype,), g.device)
         if out.numel() != g.numel():
             raise ValueError("out has the wrong size")
-    _check("qsw_silu_mul", lib.qsw_silu_mul(g.data_ptr(), u.data_ptr(), g.numel(), int(variant),
-                                            out.data_ptr(), _stream_ptr(stream)))
+    _check("qsw_silu_mul_ex", lib.qsw_silu_mul_ex(g.data_ptr(), u.data_ptr(), g.numel(), int(variant),
+                                                  _ACT[g.dtype], out.data_ptr(), _stream_ptr(stream)))
     return out
 
 

@@ -35,15 +35,15 @@ def gemv_limit():
     ops.qsw_set_gemv_max_m(saved)
 
 
-def check(variant, got, want):
+def check(variant, got, want, dtype="bf16"):
     """F32 and the stored projections against the oracle (MATCH goes through
     check_fused, which also needs the projections)."""
     if variant == ops.MATCH:
-        ok, info = check_match(got, want)
+        ok, info = check_match(got, want, dtype)
     elif variant == ops.F32:
-        ok, info = check_f32(got, want)
+        ok, info = check_f32(got, want, dtype)
     else:
-        ok, info = check_projection(got, want)
+        ok, info = check_projection(got, want, dtype)
     assert ok, info
 
 
@@ -53,8 +53,8 @@ def run_fused(case, dev, variant, args=None):
     return to_bits(out)
 
 
-def match_epilogue(g, u):
-    return oracle.silu_mul(np.ascontiguousarray(g), np.ascontiguousarray(u), oracle.MATCH)
+def match_epilogue(g, u, dtype="bf16"):
+    return oracle.silu_mul(np.ascontiguousarray(g), np.ascontiguousarray(u), oracle.MATCH, dtype=dtype)
 
 
 def check_fused(case, dev, variant, rows=None, pairs=None):
@@ -68,22 +68,25 @@ def check_fused(case, dev, variant, rows=None, pairs=None):
         sel = (pairs[:, 0], pairs[:, 1])
     else:
         sel = (slice(None),)
+    dt = case.dtype
     if pairs is not None:
-        want = {v: oracle.qswiglu_pairs(*case.oracle_args(), v, pairs)
+        want = {v: oracle.qswiglu_pairs(*case.oracle_args(), v, pairs, dtype=dt)
                 for v in (variant, ops.DEBUG_GATE, ops.DEBUG_UP)}
         h_ref, g_ref, u_ref = want[variant], want[ops.DEBUG_GATE], want[ops.DEBUG_UP]
     elif variant == ops.MATCH:
-        h_ref, g64, u64 = oracle.qswiglu(*case.oracle_args(), variant=variant, rows=rows, return_acc=True)
-        g_ref, u_ref = oracle.bf16_round_array(g64), oracle.bf16_round_array(u64)
+        h_ref, g64, u64 = oracle.qswiglu(*case.oracle_args(), variant=variant, rows=rows, return_acc=True,
+                                         dtype=dt)
+        g_ref, u_ref = oracle.round_array(g64, dt), oracle.round_array(u64, dt)
     else:
-        h_ref = oracle.qswiglu(*case.oracle_args(), variant=variant, rows=rows)
+        h_ref = oracle.qswiglu(*case.oracle_args(), variant=variant, rows=rows, dtype=dt)
     if variant == ops.MATCH:
         g_gpu = run_fused(case, dev, ops.DEBUG_GATE, a)[sel]
         u_gpu = run_fused(case, dev, ops.DEBUG_UP, a)[sel]
-        ok, info = check_match_with_projections(got[sel], g_gpu, u_gpu, h_ref, g_ref, u_ref, match_epilogue)
+        ok, info = check_match_with_projections(got[sel], g_gpu, u_gpu, h_ref, g_ref, u_ref,
+                                                lambda g, u: match_epilogue(g, u, dt), dt)
         assert ok, info
     else:
-        check(variant, got[sel], h_ref)
+        check(variant, got[sel], h_ref, dt)
     return got
 
 
@@ -515,3 +518,144 @@ def test_workspace_size_is_checked(dev, gemv_limit):
     ops.qsw_check_device_errors()
     ok, info = check_f32(got, oracle.qswiglu(*case.oracle_args(), variant=oracle.F32))
     assert ok, info
+
+
+# ------------------------------------------------------ f16 activations ----
+
+F16_TC_SHAPES = [
+    (130, 512, 200, 4, 64, 4, 64),     # 2 M tiles, ragged N
+    (257, 2080, 384, 4, 32, 8, 32),    # K tail, mixed specs
+    (200, 640, 136, 2, 64, 8, 64),     # 2-bit gate, 8-bit up
+]
+F16_GEMV_SHAPES = [
+    (1, 512, 8, 4, 64, 4, 64),
+    (3, 512, 203, 4, 64, 4, 64),       # ragged last unit
+    (4, 2304, 136, 8, 32, 4, 32),      # 8-bit gate
+    (9, 1024, 48, 4, 128, 8, 32),      # two x row groups
+]
+
+
+@pytest.mark.parametrize("shape", F16_TC_SHAPES, ids=_ids(F16_TC_SHAPES))
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAMES[v])
+def test_f16_tensor_core_kernel(dev, gemv_limit, shape, variant):
+    """f16 activations (x, scales, biases, hidden) on the tensor-core kernel."""
+    M, H, I, bg, gg, bu, gu = shape
+    case = inputs.make_case(M, H, I, bits_g=bg, gs_g=gg, bits_u=bu, gs_u=gu, seed=M * 5 + H, dtype="f16")
+    gemv_limit(0)
+    before = ops.qsw_get_counters()[ops.CNT_FUSED_TC]
+    got = check_fused(case, dev, variant)
+    assert ops.qsw_get_counters()[ops.CNT_FUSED_TC] > before
+    assert got.dtype == np.uint16
+
+
+@pytest.mark.parametrize("shape", F16_GEMV_SHAPES, ids=_ids(F16_GEMV_SHAPES))
+@pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAMES[v])
+def test_f16_small_m_kernel(dev, gemv_limit, shape, variant):
+    M, H, I, bg, gg, bu, gu = shape
+    case = inputs.make_case(M, H, I, bits_g=bg, gs_g=gg, bits_u=bu, gs_u=gu, seed=M * 3 + H, dtype="f16")
+    gemv_limit(32)
+    before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
+    check_fused(case, dev, variant)
+    assert ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] > before
+
+
+@pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
+@pytest.mark.parametrize("bits,gs", [(4, 64), (8, 32), (2, 64)])
+def test_f16_affine_qmm(dev, gemv_limit, limit, bits, gs):
+    M, K, N = (5, 1024, 300) if limit else (140, 640, 300)
+    case = inputs.make_case(M, K, N, bits_g=bits, gs_g=gs, seed=bits + gs + 1, dtype="f16")
+    gemv_limit(limit)
+    x, w, s, b, _, _ = device_args(case, dev)[:6]
+    y = ops.affine_qmm(x, w, s, b, gs, bits)
+    assert y.dtype == torch.float16
+    got = to_bits(y)
+    ops.qsw_check_device_errors()
+    want = oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gs, bits, dtype="f16")
+    ok, info = check_projection(got, want, "f16")
+    assert ok, info
+
+
+def test_f16_all_gate_values(dev):
+    """Every finite f16 gate value through the elementwise MATCH and F32 steps,
+    and the paired (vector) and scalar (tail) forms bit for bit."""
+    h = np.arange(0, 0x10000, dtype=np.uint32).astype(np.uint16)
+    g = h[np.isfinite(h.view(np.float16))]
+    n = (g.size // 8) * 8
+    g = g[:n]
+    u = inputs.f32_to_bits(torch.full((n,), 1.5), "f16")
+    gd = inputs.bits_to_device(g, dev, "f16")
+    ud = inputs.bits_to_device(u, dev, "f16")
+    for variant, chk in ((ops.MATCH, check_match), (ops.F32, check_f32)):
+        got = to_bits(ops.qsw_silu_mul(gd, ud, variant))
+        ok, info = chk(got, oracle.silu_mul(g, u, variant, dtype="f16"), "f16")
+        assert ok, info
+    paired = to_bits(ops.qsw_silu_mul(gd, ud, ops.MATCH))
+    scalar = np.zeros(n, dtype=np.uint16)
+    out = torch.zeros_like(gd)
+    for k in range(0, n - 7, 8):
+        ops.qsw_silu_mul(gd[k:k + 7], ud[k:k + 7], ops.MATCH, out=out[k:k + 7])
+    ops.qsw_check_device_errors()
+    got7 = to_bits(out)
+    mask = (np.arange(n) % 8) != 7
+    assert np.array_equal(paired[mask], got7[mask])
+
+
+@pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
+def test_f16_fused_match_equals_unfused(dev, gemv_limit, limit):
+    case = inputs.make_case(24, 1024, 264, bits_g=4, gs_g=64, bits_u=8, gs_u=32, seed=4, dtype="f16")
+    gemv_limit(limit)
+    a = device_args(case, dev)
+    fused = to_bits(ops.qswiglu_forward(*a, variant=ops.MATCH, workspace=None))
+    unfused = to_bits(ops.unfused_swiglu(*a, variant=ops.MATCH, workspace=None))
+    ops.qsw_check_device_errors()
+    if limit == 0:
+        assert np.array_equal(fused, unfused)
+    else:
+        ok, info = check_match(fused, unfused, "f16")
+        assert ok, info
+
+
+@pytest.mark.parametrize("mode", [ops.STREAM_K_OFF, ops.STREAM_K_ALWAYS], ids=["whole_tiles", "split"])
+def test_f16_stream_k(dev, gemv_limit, stream_k, mode):
+    case = inputs.make_case(300, 512, 1536, seed=77, dtype="f16")
+    gemv_limit(0)
+    stream_k(mode)
+    check_fused(case, dev, ops.MATCH)
+
+
+def test_f16_full_mid_prefill(dev, gemv_limit):
+    """The mid-prefill shape with f16 activations, sampled rows, in the
+    benchmark's launch configuration."""
+    kw = dict(inputs.WORKLOADS["mid_prefill"])
+    case = inputs.make_case(dtype="f16", seed=0, **kw)
+    _sampled(case, dev, ops.MATCH, [0, 1, 127, 128, 300, 511], 16, gemv_limit)
+
+
+def test_f16_full_decode(dev, gemv_limit):
+    kw = dict(inputs.WORKLOADS["decode"])
+    case = inputs.make_case(dtype="f16", seed=0, **kw)
+    _sampled(case, dev, ops.MATCH, [0], 16, gemv_limit)
+
+
+def test_plain_bf16_entry_points(dev, gemv_limit):
+    """The fixed-signature entry points (bf16, no workspace) called directly
+    through the C ABI."""
+    lib = ops.load_library()
+    case = inputs.make_case(40, 512, 136, seed=19)
+    x, wg, sg, bg, gsg, btg, wu, su, bu, gsu, btu = device_args(case, dev)
+    s = torch.cuda.current_stream().cuda_stream
+    for limit in (0, 32):
+        gemv_limit(limit)
+        out = torch.empty((40, 136), dtype=torch.bfloat16, device=dev)
+        assert lib.qswiglu_forward(x.data_ptr(), 40, 512, 136, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(), gsg, btg,
+                                   wu.data_ptr(), su.data_ptr(), bu.data_ptr(), gsu, btu, ops.F32, out.data_ptr(),
+                                   s) == 0
+        y = torch.empty((40, 136), dtype=torch.bfloat16, device=dev)
+        assert lib.affine_qmm(x.data_ptr(), 40, 512, 136, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(), gsg, btg,
+                              y.data_ptr(), s) == 0
+        ops.qsw_check_device_errors()
+        ok, info = check_f32(to_bits(out), oracle.qswiglu(*case.oracle_args(), variant=oracle.F32))
+        assert ok, info
+        want = oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gsg, btg)
+        ok, info = check_projection(to_bits(y), want)
+        assert ok, info

@@ -1,10 +1,17 @@
 """Acceptance bounds of the GPU path against the oracle.
 
-MATCH:  |gpu - oracle| <= 2 bf16 ulps of the oracle value + 1e-3, elementwise;
-        the stored gate/up projections (debug variants) equal the oracle's on
-        at least 99.9 % of elements.
+MATCH:  |gpu - oracle| <= 2 ulps (of the activation dtype) of the oracle value
+        + 1e-3, elementwise; the stored gate/up projections (debug variants)
+        equal the oracle's on at least 99.9 % of elements for bf16.
 F32:    |gpu - oracle| <= 1e-3 + 8e-3 * |oracle|, elementwise.
 Integer and byte results are compared bit for bit.
+
+f16 activations (the bounds are stated for bf16; these are the readings for
+f16): the ulp bounds are f16 ulps, and the exact-projection rate is 99 %.  The
+f32 accumulator's error is the same whatever the output dtype, but f16's
+rounding grid is 8 times finer than bf16's, so the same error moves about 8
+times as many sums across a rounding boundary (the bf16 rate of 99.9 % scales
+to about 99.2 %).
 """
 from __future__ import annotations
 
@@ -13,7 +20,7 @@ import numpy as np
 MATCH_ULPS = 2
 ABS_TOL = 1e-3
 F32_RTOL = 8e-3
-EXACT_FRACTION = 0.999
+EXACT_FRACTION = {"bf16": 0.999, "f16": 0.99}
 
 
 def bf16_to_f64(h) -> np.ndarray:
@@ -28,6 +35,23 @@ def bf16_ulp(v: np.ndarray) -> np.ndarray:
         e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
     e = np.maximum(e, -126.0)
     return np.where(a > 0, np.exp2(e - 7.0), 2.0 ** -133)
+
+
+def f16_to_f64(h) -> np.ndarray:
+    return np.asarray(h, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def f16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of binary16 numbers at |v| (11 significant bits, subnormal floor)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -14.0)
+    return np.where(a > 0, np.exp2(e - 10.0), 2.0 ** -24)
+
+
+TO_F64 = {"bf16": bf16_to_f64, "f16": f16_to_f64}
+ULP = {"bf16": bf16_ulp, "f16": f16_ulp}
 
 
 def _summary(gpu, ref, bound):
@@ -47,13 +71,13 @@ def _summary(gpu, ref, bound):
     return n_bad == 0, info
 
 
-def check_match(gpu_bits, oracle_bits):
-    gpu, ref = bf16_to_f64(gpu_bits), bf16_to_f64(oracle_bits)
-    return _summary(gpu, ref, MATCH_ULPS * bf16_ulp(ref) + ABS_TOL)
+def check_match(gpu_bits, oracle_bits, dtype="bf16"):
+    gpu, ref = TO_F64[dtype](gpu_bits), TO_F64[dtype](oracle_bits)
+    return _summary(gpu, ref, MATCH_ULPS * ULP[dtype](ref) + ABS_TOL)
 
 
-def check_f32(gpu_bits, oracle_bits):
-    gpu, ref = bf16_to_f64(gpu_bits), bf16_to_f64(oracle_bits)
+def check_f32(gpu_bits, oracle_bits, dtype="bf16"):
+    gpu, ref = TO_F64[dtype](gpu_bits), TO_F64[dtype](oracle_bits)
     return _summary(gpu, ref, ABS_TOL + F32_RTOL * np.abs(ref))
 
 
@@ -63,7 +87,7 @@ def exact_fraction(gpu_bits, oracle_bits) -> float:
     return float((a == b).mean()) if a.size else 1.0
 
 
-def check_match_with_projections(h_gpu, g_gpu, u_gpu, h_ref, g_ref, u_ref, epilogue):
+def check_match_with_projections(h_gpu, g_gpu, u_gpu, h_ref, g_ref, u_ref, epilogue, dtype="bf16"):
     """MATCH check that accounts for the projections' rounding.
 
     The GPU accumulates in f32, in another order than the oracle's f64 sum, so
@@ -77,12 +101,12 @@ def check_match_with_projections(h_gpu, g_gpu, u_gpu, h_ref, g_ref, u_ref, epilo
         epilogue applied to the GPU's own projections (`epilogue(g, u)`)."""
     h_gpu, g_gpu, u_gpu = (np.asarray(a, dtype=np.uint16) for a in (h_gpu, g_gpu, u_gpu))
     h_ref, g_ref, u_ref = (np.asarray(a, dtype=np.uint16) for a in (h_ref, g_ref, u_ref))
-    ok_g, info_g = check_projection(g_gpu, g_ref)
-    ok_u, info_u = check_projection(u_gpu, u_ref)
+    ok_g, info_g = check_projection(g_gpu, g_ref, dtype)
+    ok_u, info_u = check_projection(u_gpu, u_ref, dtype)
     same = (g_gpu == g_ref) & (u_gpu == u_ref)
-    ok_same, info_same = check_match(h_gpu[same], h_ref[same])
+    ok_same, info_same = check_match(h_gpu[same], h_ref[same], dtype)
     alt = epilogue(g_gpu[~same], u_gpu[~same]) if (~same).any() else np.zeros(0, np.uint16)
-    ok_alt, info_alt = check_match(h_gpu[~same], alt)
+    ok_alt, info_alt = check_match(h_gpu[~same], alt, dtype)
     info = {"gate": info_g, "up": info_u, "agreeing": info_same, "flipped": info_alt,
             "flipped_fraction": float((~same).mean()) if same.size else 0.0}
     return ok_g and ok_u and ok_same and ok_alt, info
@@ -91,15 +115,15 @@ def check_match_with_projections(h_gpu, g_gpu, u_gpu, h_ref, g_ref, u_ref, epilo
 MIN_RATE_SAMPLE = 10_000
 
 
-def check_projection(gpu_bits, oracle_bits):
+def check_projection(gpu_bits, oracle_bits, dtype="bf16"):
     """Stored gate/up projection: every element within 1 ulp + 1e-3 (the
     absolute term covers sums that cancel to near zero), and bit-identical on
     >= 99.9 % of elements.  The 99.9 % figure is a rate, so it is enforced on
     samples of at least MIN_RATE_SAMPLE elements (a handful of elements cannot
     resolve a 0.1 % rate); smaller samples report it."""
     frac = exact_fraction(gpu_bits, oracle_bits)
-    gpu, ref = bf16_to_f64(gpu_bits), bf16_to_f64(oracle_bits)
-    ok_close, info = _summary(gpu, ref, bf16_ulp(ref) + ABS_TOL)
+    gpu, ref = TO_F64[dtype](gpu_bits), TO_F64[dtype](oracle_bits)
+    ok_close, info = _summary(gpu, ref, ULP[dtype](ref) + ABS_TOL)
     info["exact_fraction"] = frac
-    rate_ok = frac >= EXACT_FRACTION or np.size(gpu_bits) < MIN_RATE_SAMPLE
+    rate_ok = frac >= EXACT_FRACTION[dtype] or np.size(gpu_bits) < MIN_RATE_SAMPLE
     return (rate_ok and ok_close), info
