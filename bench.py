@@ -271,11 +271,30 @@ def bench_decode(args, dev, stream, peaks, peak_src):
     out_host = torch.empty((1, case.I), dtype=torch.bfloat16, pin_memory=True)
     x_dev = torch.empty_like(x)
 
+    def e2e_calls(r):
+        x_dev.copy_(x_host, non_blocking=True)
+        ops.qswiglu_forward(x_dev, *reps[r], variant=variant, out=out, stream=stream)
+        out_host.copy_(out, non_blocking=True)
+
+    # A decode loop replays its step as a CUDA graph: one graph per weight
+    # replica (so that the weights still come from HBM), each holding the
+    # pinned-memory copy of x in, the public qswiglu_forward call and the copy
+    # of hidden out.  No host synchronisation between steps.
+    with torch.cuda.stream(stream):
+        for r in range(replicas):
+            e2e_calls(r)
+    torch.cuda.synchronize()
+    e2e_graphs = []
+    for r in range(replicas):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            e2e_calls(r)
+        e2e_graphs.append(g)
+    torch.cuda.synchronize()
+
     def e2e_step(i):
         with torch.cuda.stream(stream):
-            x_dev.copy_(x_host, non_blocking=True)
-            ops.qswiglu_forward(x_dev, *reps[i % replicas], variant=variant, out=out, stream=stream)
-            out_host.copy_(out, non_blocking=True)
+            e2e_graphs[i % replicas].replay()
 
     e2e_ms = time_calls(e2e_step, args.steps, args.warmup, stream)
     world, rank, _ = dist_info()
@@ -307,6 +326,45 @@ def bench_prefill(args, dev, stream, peaks, peak_src):
         res.update(_bench_mid(args, dev, stream))
     if args.only in ("all", "sweep"):
         res.update(_bench_mixed_sweep(args, dev, stream))
+    if args.only in ("all", "f16"):
+        res.update(_bench_f16(args, dev, stream))
+    return res
+
+
+def _bench_f16(args, dev, stream):
+    """The mid and large prefill shapes and the decode shape with f16
+    activations (x, scales, biases and hidden in f16), MATCH."""
+    import torch
+    from quantized_swiglu_mlp_gb300 import inputs, ops
+
+    res = {}
+    for name in ("mid_prefill", "large_prefill"):
+        kw = dict(inputs.WORKLOADS[name])
+        case = inputs.make_case(dtype="f16", seed=0, **kw)
+        a = to_device(case, dev)
+        out = torch.empty((case.M, case.I), dtype=torch.float16, device=dev)
+        flops = 4.0 * case.M * case.H * case.I
+        steps = args.prefill_steps
+        ms = time_graph(lambda i: ops.qswiglu_forward(*a, variant=ops.MATCH, out=out, stream=stream), steps, 3,
+                        stream)
+        per = ms / 1e3 / steps
+        res[f"{name.split('_')[0]}_f16"] = {"tflops": round(flops / per / 1e12, 1), "us_per_call": round(per * 1e6, 1)}
+        del a, out
+        torch.cuda.empty_cache()
+    kw = dict(inputs.WORKLOADS["decode"])
+    case = inputs.make_case(dtype="f16", seed=0, **kw)
+    wbytes = weight_bytes(case)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    base = to_device(case, dev)
+    reps = [base[1:]] + [tuple(t.clone() if isinstance(t, torch.Tensor) else t for t in base[1:])
+                         for _ in range(max(1, int(np.ceil(3.2 * l2 / wbytes))) - 1)]
+    out = torch.empty((1, case.I), dtype=torch.float16, device=dev)
+    steps = 200
+    ms = time_graph(lambda i: ops.qswiglu_forward(base[0], *reps[i % len(reps)], variant=ops.MATCH, out=out,
+                                                  stream=stream), steps, 3, stream)
+    us = ms * 1e3 / steps
+    res["decode_f16"] = {"us": round(us, 2), "weight_GBps": round(wbytes / us / 1e3, 1)}
+    ops.qsw_check_device_errors(stream)
     return res
 
 
@@ -482,6 +540,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "roofline": d["roofline"],
         "e2e": {"value": round(e2e, 1), "unit": "GB/s", "h2d_bytes_per_step": 2 * 2048,
+                "mode": "per step one CUDA-graph replay: pinned H2D copy of x, qswiglu_forward, "
+                        "D2H copy of hidden to pinned memory; no host sync between steps",
                 "d2h_bytes_per_step": 2 * 8192},
         "gpu_launches": d["launches"] * world,
         "clocks": d["clocks"],
@@ -576,7 +636,7 @@ def main(argv=None):
                     help="stream-K scheduling of the tensor-core kernel (library switch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--only", choices=["all", "decode", "large", "mid", "sweep"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "large", "mid", "sweep", "f16"], default="all",
                     help="run one workload only (profiling); the JSON line then carries what ran")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="untimed load before the timed region, so the clock sampler sees it")
