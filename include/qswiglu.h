@@ -188,6 +188,10 @@ QSW_API qsw_status qswiglu_forward_noalloc(const void *x, int64_t M, int64_t H, 
  * patterns (same layouts and alignment), the dequantised weights are
  * f16(s*q + b) and the tensor cores run on f16 operands; everything else
  * (arguments, workspace, results, errors) is as for the bf16 forms.
+ * affine_qmm_ex also takes `residual`: NULL, or [M, N] in the activation dtype
+ * (16-byte aligned) added to the f32 accumulator before the one rounding,
+ * y = T(x . W^T + residual); it may be y itself (each element is read before
+ * it is written, by the same thread).
  */
 QSW_API qsw_status qswiglu_forward_ex(const void *x, int64_t M, int64_t H, int64_t I,
                            const uint32_t *wg, const void *sg, const void *bg,
@@ -198,10 +202,32 @@ QSW_API qsw_status qswiglu_forward_ex(const void *x, int64_t M, int64_t H, int64
                            void *workspace, size_t workspace_bytes, void *stream);
 QSW_API qsw_status affine_qmm_ex(const void *x, int64_t M, int64_t K, int64_t N,
                       const uint32_t *w, const void *s, const void *b,
-                      int gs, int bits, int act_dtype, void *y,
+                      int gs, int bits, int act_dtype, const void *residual, void *y,
                       void *workspace, size_t workspace_bytes, void *stream);
 QSW_API qsw_status qsw_silu_mul_ex(const void *g, const void *u, int64_t n, int variant,
                         int act_dtype, void *out, void *stream);
+
+/*
+ * The whole MLP block with its residual (fused-mlp-kernel.ts on the pages:
+ * the output is h + mlp(x)):
+ *     hidden[M, I] = the fused expansion of x (variant QSW_MATCH or QSW_F32),
+ *     y[M, Ho]     = T( h + hidden . Wd^T ),
+ * down weights Wd packed [Ho, I*bits_d/32] with scales/biases [Ho, I/gs_d].
+ * Two launches on `stream`: the fused expansion writes `hidden` (caller-owned,
+ * [M, I] in the activation dtype, 16-byte aligned), then the down projection
+ * adds the residual `h` ([M, Ho], or NULL for none; it may be y) to its f32
+ * accumulator before the one rounding: deterministic, no atomics.  I must meet
+ * the K rules of affine_qmm for the down weights (multiple of 32 and of gs_d).
+ * The workspace (optional, as for the *_ws forms) serves both launches.
+ * Argument errors in either stage return before anything is launched.
+ */
+QSW_API qsw_status qsw_mlp_forward_ex(const void *x, const void *h, int64_t M, int64_t H,
+                           int64_t I, int64_t Ho,
+                           const uint32_t *wg, const void *sg, const void *bg, int gs_g, int bits_g,
+                           const uint32_t *wu, const void *su, const void *bu, int gs_u, int bits_u,
+                           const uint32_t *wd, const void *sd, const void *bd, int gs_d, int bits_d,
+                           int variant, int act_dtype, void *hidden, void *y,
+                           void *workspace, size_t workspace_bytes, void *stream);
 
 /* Stream-K mode of the *_ws, *_ex and _noalloc entry points (qsw_stream_k_mode, default
  * QSW_STREAM_K_AUTO; other values are ignored).  Process-wide. */

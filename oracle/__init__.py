@@ -21,7 +21,8 @@ Parity status of each function (what pins it is in tests/test_oracle_pins.py):
   dequant       pinned (hand-worked rows, exact rational brute force)
   qswiglu       pinned (hand-worked 2x8 example, x=0, integer special case,
                 brute force on tiny shapes, K-permutation invariance)
-  qmm           pinned (integer special case, brute force)
+  qmm           pinned (integer special case, brute force, residual brute force)
+  mlp           pinned (x=0 gives y=h, brute force of the whole block, composition)
   silu_mul      pinned (hand-worked values, silu(0)=0, MATCH == fused MATCH)
 """
 from __future__ import annotations
@@ -80,8 +81,11 @@ def _declare(lib):
     lib.orc_qswiglu_rows.restype = i32
     lib.orc_qswiglu_pairs.argtypes = q_args + [p, i64, p]
     lib.orc_qswiglu_pairs.restype = i32
-    lib.orc_qmm.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, i32, p]
+    lib.orc_qmm.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, i32, p, p]
     lib.orc_qmm.restype = i32
+    lib.orc_mlp.argtypes = [p, p, i64, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32,
+                            p, p, p, i32, i32, i32, i32, p, p]
+    lib.orc_mlp.restype = i32
     lib.orc_silu_mul.argtypes = [p, p, i64, i32, i32, p]
     lib.orc_num_threads.restype = i32
     lib.orc_set_num_threads.argtypes = [i32]
@@ -217,17 +221,42 @@ class OracleLib:
             raise MemoryError("oracle allocation failed")
         return out
 
-    def qmm(self, x, w, s, b, gs, bits, dtype="bf16"):
-        """Unfused quantised linear y = T(x . W^T) as uint16 [M, N] bits of T = `dtype`."""
+    def qmm(self, x, w, s, b, gs, bits, dtype="bf16", residual=None):
+        """Quantised linear y = T(x . W^T + residual) as uint16 [M, N] bits of T = `dtype`."""
         x, w, s, b = _c(x, np.uint16), _c(w, np.uint32), _c(s, np.uint16), _c(b, np.uint16)
         M, K = x.shape
         N = w.shape[0]
         if w.shape != (N, K * bits // 32) or s.shape != (N, K // gs) or b.shape != s.shape:
             raise ValueError("shape mismatch")
+        r = None if residual is None else _c(residual, np.uint16)
+        if r is not None and r.shape != (M, N):
+            raise ValueError("residual shape mismatch")
         y = np.empty((M, N), dtype=np.uint16)
-        if self.lib.orc_qmm(_ptr(x), M, K, N, _ptr(w), _ptr(s), _ptr(b), gs, bits, _dt(dtype), _ptr(y)) != 0:
+        if self.lib.orc_qmm(_ptr(x), M, K, N, _ptr(w), _ptr(s), _ptr(b), gs, bits, _dt(dtype),
+                            None if r is None else _ptr(r), _ptr(y)) != 0:
             raise MemoryError("oracle allocation failed")
         return y
+
+    def mlp(self, x, h, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, wd, sd, bd, gs_d, bits_d,
+            variant=MATCH, dtype="bf16"):
+        """Whole MLP block y = T(h + hidden . Wd^T); returns (y [M, Ho], hidden [M, I])."""
+        keep, args, M, H, I = self._qargs(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u)
+        wd, sd, bd = _c(wd, np.uint32), _c(sd, np.uint16), _c(bd, np.uint16)
+        Ho = wd.shape[0]
+        if wd.shape != (Ho, I * bits_d // 32) or sd.shape != (Ho, I // gs_d) or bd.shape != sd.shape:
+            raise ValueError("down weight shape mismatch")
+        hh = None if h is None else _c(h, np.uint16)
+        if hh is not None and hh.shape != (M, Ho):
+            raise ValueError("residual shape mismatch")
+        hidden = np.empty((M, I), dtype=np.uint16)
+        y = np.empty((M, Ho), dtype=np.uint16)
+        rc = self.lib.orc_mlp(args[0], None if hh is None else _ptr(hh), M, H, I, Ho, *args[4:],
+                              _ptr(wd), _ptr(sd), _ptr(bd), gs_d, bits_d, int(variant), _dt(dtype),
+                              _ptr(hidden), _ptr(y))
+        del keep
+        if rc != 0:
+            raise MemoryError("oracle allocation failed")
+        return y, hidden
 
     def silu_mul(self, g, u, variant=MATCH, dtype="bf16"):
         g, u = _c(g, np.uint16), _c(u, np.uint16)
@@ -271,6 +300,6 @@ def __getattr__(name):
     # module-level shortcuts: oracle.qswiglu(...), oracle.qmm(...), ...
     if name in ("num_threads", "set_num_threads", "f64_to_bf16", "bf16_to_f64",
                 "bf16_round_array", "f64_to_f16", "f16_to_f64", "round_array", "unpack", "dequant",
-                "qswiglu", "qswiglu_pairs", "qmm", "silu_mul"):
+                "qswiglu", "qswiglu_pairs", "qmm", "mlp", "silu_mul"):
         return getattr(default(), name)
     raise AttributeError(name)

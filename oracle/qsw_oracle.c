@@ -354,12 +354,14 @@ int orc_qswiglu_pairs(const uint16_t *x, int64_t M, int64_t H, int64_t I,
 /* ------------------------------------------------ unfused composition ----- */
 
 /*
- * Quantised linear y = T(x . W^T): the float accumulator cast to the
- * activation dtype at the store.  x [M,K], W packed [N, K*bits/32], y [M,N].
+ * Quantised linear y = T(x . W^T + r): the float accumulator cast to the
+ * activation dtype at the store.  x [M,K], W packed [N, K*bits/32], y [M,N];
+ * r [M,N] (optional, NULL = 0) is a residual added before that one rounding,
+ * as the whole-MLP kernel of fused-mlp-kernel.ts adds h to its accumulator.
  */
 int orc_qmm(const uint16_t *x, int64_t M, int64_t K, int64_t N,
             const uint32_t *w, const uint16_t *s, const uint16_t *b, int gs, int bits, int dt,
-            uint16_t *y)
+            const uint16_t *r, uint16_t *y)
 {
     double *xd = act_rows_to_f64(x, M, K, dt);
     if (!xd) return -1;
@@ -375,14 +377,34 @@ int orc_qmm(const uint16_t *x, int64_t M, int64_t K, int64_t N,
 #pragma omp for schedule(dynamic, 16)
             for (int64_t n = 0; n < N; ++n) {
                 orc_dequant(w + n * wpr, s + n * gpr, b + n * gpr, 1, K, gs, bits, dt, wr);
-                for (int64_t m = 0; m < M; ++m)
-                    y[m * N + n] = f64_to_act(dot_f64(xd + m * K, wr, K), dt);
+                for (int64_t m = 0; m < M; ++m) {
+                    double acc = dot_f64(xd + m * K, wr, K);
+                    if (r) acc += act_to_f64(r[m * N + n], dt);
+                    y[m * N + n] = f64_to_act(acc, dt);
+                }
             }
         }
         free(wr);
     }
     free(xd);
     return failed ? -1 : 0;
+}
+
+/*
+ * The whole MLP block (fused-mlp-kernel.ts, "the kernel outputs h + mlp(x)"):
+ * hidden = the fused expansion of x in T (variant MATCH or F32), then
+ * y = T(h + hidden . Wd^T) with the sum over I in f64 and one rounding.
+ * hidden [M, I] and y [M, Ho] are outputs; h [M, Ho] may be NULL (no residual).
+ */
+int orc_mlp(const uint16_t *x, const uint16_t *h, int64_t M, int64_t H, int64_t I, int64_t Ho,
+            const uint32_t *wg, const uint16_t *sg, const uint16_t *bg, int gs_g, int bits_g,
+            const uint32_t *wu, const uint16_t *su, const uint16_t *bu, int gs_u, int bits_u,
+            const uint32_t *wd, const uint16_t *sd, const uint16_t *bd, int gs_d, int bits_d,
+            int variant, int dt, uint16_t *hidden, uint16_t *y)
+{
+    int rc = orc_qswiglu(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, dt, hidden);
+    if (rc != 0) return rc;
+    return orc_qmm(hidden, M, I, Ho, wd, sd, bd, gs_d, bits_d, dt, h, y);
 }
 
 /*

@@ -116,14 +116,14 @@ qsw_status fused_forward(const void *x, int64_t M, int64_t H, int64_t I, const u
   const qsw::QuantOperand u{wu, static_cast<const uint16_t *>(su), static_cast<const uint16_t *>(bu), gs_u, bits_u};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (M <= gemv_max_m() && qsw::gemv_fits(M, H, I, g, &u, sm_count())) {
-    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, act, out, s, g_timeout_ns.load(), sm_count(),
+    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, act, out, nullptr, s, g_timeout_ns.load(), sm_count(),
                                     g_early_weights.load(std::memory_order_relaxed) != 0));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
     if (static_scratch && qsw::prefill_static_workspace(sm_count(), s, &ws.ptr, &ws.bytes) != cudaSuccess)
       return QSW_ERR_CUDA;
     st = from_cuda(
-        qsw::launch_prefill(x, M, H, I, g, &u, variant, act, out, s, g_timeout_ns.load(), sm_count(), ws));
+        qsw::launch_prefill(x, M, H, I, g, &u, variant, act, out, nullptr, s, g_timeout_ns.load(), sm_count(), ws));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_TC].fetch_add(1, std::memory_order_relaxed);
   }
   return st;
@@ -157,8 +157,8 @@ qsw_status qswiglu_forward(const void *x, int64_t M, int64_t H, int64_t I, const
 }
 
 qsw_status affine_qmm_ex(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
-                         const void *b, int gs, int bits, int act_dtype, void *y, void *workspace,
-                         size_t workspace_bytes, void *stream) {
+                         const void *b, int gs, int bits, int act_dtype, const void *residual, void *y,
+                         void *workspace, size_t workspace_bytes, void *stream) {
   qsw_status st = check_shape(M, K, N);
   if (st != QSW_OK) return st;
   qsw::SplitWorkspace ws;
@@ -167,16 +167,16 @@ qsw_status affine_qmm_ex(const void *x, int64_t M, int64_t K, int64_t N, const u
   if ((st = check_operand(w, s, b, K, gs, bits)) != QSW_OK) return st;
   if (M == 0) return QSW_OK;   // nothing to read or write: x and y may be null
   if (!x || !y) return QSW_ERR_INVALID_ARG;
-  if (!aligned(x, 16) || !aligned(y, 16)) return QSW_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(residual, 16)) return QSW_ERR_UNSUPPORTED;
 
   const qsw::QuantOperand op{w, static_cast<const uint16_t *>(s), static_cast<const uint16_t *>(b), gs, bits};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   if (M <= gemv_max_m() && qsw::gemv_fits(M, K, N, op, nullptr, sm_count())) {
-    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, act_dtype, y, cs, g_timeout_ns.load(),
+    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, act_dtype, y, residual, cs, g_timeout_ns.load(),
                                     sm_count(), g_early_weights.load(std::memory_order_relaxed) != 0));
     if (st == QSW_OK) g_counters[QSW_CNT_QMM_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
-    st = from_cuda(qsw::launch_prefill(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, act_dtype, y, cs,
+    st = from_cuda(qsw::launch_prefill(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, act_dtype, y, residual, cs,
                                        g_timeout_ns.load(), sm_count(), ws));
     if (st == QSW_OK) g_counters[QSW_CNT_QMM_TC].fetch_add(1, std::memory_order_relaxed);
   }
@@ -186,7 +186,7 @@ qsw_status affine_qmm_ex(const void *x, int64_t M, int64_t K, int64_t N, const u
 qsw_status affine_qmm_ws(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
                          const void *b, int gs, int bits, void *y, void *workspace, size_t workspace_bytes,
                          void *stream) {
-  return affine_qmm_ex(x, M, K, N, w, s, b, gs, bits, QSW_ACT_BF16, y, workspace, workspace_bytes, stream);
+  return affine_qmm_ex(x, M, K, N, w, s, b, gs, bits, QSW_ACT_BF16, nullptr, y, workspace, workspace_bytes, stream);
 }
 
 qsw_status affine_qmm(const void *x, int64_t M, int64_t K, int64_t N, const uint32_t *w, const void *s,
@@ -200,6 +200,32 @@ qsw_status qswiglu_forward_noalloc(const void *x, int64_t M, int64_t H, int64_t 
                                    void *stream) {
   return fused_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, QSW_ACT_BF16, out,
                        nullptr, 0, true, stream);
+}
+
+qsw_status qsw_mlp_forward_ex(const void *x, const void *h, int64_t M, int64_t H, int64_t I, int64_t Ho,
+                              const uint32_t *wg, const void *sg, const void *bg, int gs_g, int bits_g,
+                              const uint32_t *wu, const void *su, const void *bu, int gs_u, int bits_u,
+                              const uint32_t *wd, const void *sd, const void *bd, int gs_d, int bits_d,
+                              int variant, int act_dtype, void *hidden, void *y, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+  // every argument of both stages is checked before the first launch
+  if (variant != QSW_MATCH && variant != QSW_F32) return QSW_ERR_INVALID_ARG;
+  qsw_status st = check_shape(M, H, I);
+  if (st != QSW_OK || (st = check_shape(M, I, Ho)) != QSW_OK) return st;
+  if ((st = check_operand(wg, sg, bg, H, gs_g, bits_g)) != QSW_OK) return st;
+  if ((st = check_operand(wu, su, bu, H, gs_u, bits_u)) != QSW_OK) return st;
+  if ((st = check_operand(wd, sd, bd, I, gs_d, bits_d)) != QSW_OK) return st;
+  if (act_dtype != QSW_ACT_BF16 && act_dtype != QSW_ACT_F16) return QSW_ERR_INVALID_ARG;
+  qsw::SplitWorkspace ws;
+  if ((st = check_workspace(workspace, workspace_bytes, &ws)) != QSW_OK) return st;
+  if (M == 0) return QSW_OK;
+  if (!x || !hidden || !y) return QSW_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(hidden, 16) || !aligned(y, 16) || !aligned(h, 16)) return QSW_ERR_UNSUPPORTED;
+  st = fused_forward(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, act_dtype, hidden,
+                     workspace, workspace_bytes, false, stream);
+  if (st != QSW_OK) return st;
+  return affine_qmm_ex(hidden, M, I, Ho, wd, sd, bd, gs_d, bits_d, act_dtype, h, y, workspace, workspace_bytes,
+                       stream);
 }
 
 size_t qsw_workspace_bytes(void) { return qsw::prefill_workspace_bytes(sm_count()); }

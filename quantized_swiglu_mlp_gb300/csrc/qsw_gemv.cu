@@ -59,6 +59,7 @@ struct GemvParams {
   uint32_t ng0, ng1;      // groups per row (K / gs)
   int variant;
   uint16_t *out;
+  const uint16_t *res;    // single-operand form: [M, N] added before the rounding (or null)
   int units, slots;
   int pitch0, pitch1;     // packed bytes per row of operand 0 / 1
   int sb_off;             // byte offset of the scale/bias rows inside a slot
@@ -437,8 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
           s0 += rw[qa];
           if (DUAL) s1 += rw[(n & 1) + 2];
         }
-        const float v = DUAL ? swiglu_epilogue<A>(p.variant, s0, s1) : s0;
-        p.out[static_cast<int64_t>(m) * p.N + i_out] = A::store(v);
+        const int64_t o = static_cast<int64_t>(m) * p.N + i_out;
+        const float v = DUAL ? swiglu_epilogue<A>(p.variant, s0, s1) : (p.res ? s0 + A::lo(p.res[o]) : s0);
+        p.out[o] = A::store(v);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(rfree);
@@ -576,8 +578,8 @@ bool gemv_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const Q
 }
 
 cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                        const QuantOperand *op1, int variant, int act, void *out, cudaStream_t stream,
-                        uint64_t timeout_ns, int num_sms, bool early_weights) {
+                        const QuantOperand *op1, int variant, int act, void *out, const void *residual,
+                        cudaStream_t stream, uint64_t timeout_ns, int num_sms, bool early_weights) {
   if (!gemv_fits(M, K, N, op0, op1, num_sms)) return cudaErrorInvalidValue;
   const QuantOperand &o1 = op1 ? *op1 : op0;
   const Layout l = plan(K, N, static_cast<int>(M), op0.gs, o1.gs, op0.bits, o1.bits, op1 != nullptr, num_sms);
@@ -598,6 +600,7 @@ cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   p.ng1 = static_cast<uint32_t>(K / o1.gs);
   p.variant = variant;
   p.out = static_cast<uint16_t *>(out);
+  p.res = op1 ? nullptr : static_cast<const uint16_t *>(residual);
   p.timeout_ns = timeout_ns;
   p.early = early_weights ? 1 : 0;
   if (act == ActF16::kId) return launch_act<ActF16>(p, l, op0.bits, o1.bits, op1 != nullptr, stream, num_sms);

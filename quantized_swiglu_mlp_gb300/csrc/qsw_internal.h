@@ -21,7 +21,9 @@ struct QuantOperand {
 };
 
 // `act` (every launcher): the activation dtype, QSW_ACT_BF16 or QSW_ACT_F16 --
-// x, scales, biases and the result share it.
+// x, scales, biases and the result share it.  `residual` (single-operand form
+// only, else ignored): null, or [M, N] of that dtype added to the f32
+// accumulator before the one rounding; it may be the output buffer itself.
 //
 // Small-M kernel: rows of x up to 32.  `dual` selects the fused SwiGLU
 // (gate + up, epilogue `variant`) or a single quantised linear (y = bf16(x.W^T)).
@@ -29,8 +31,8 @@ struct QuantOperand {
 // before waiting for the preceding work (the caller guarantees that no earlier
 // work on the stream writes the weight arrays).
 cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                        const QuantOperand *op1, int variant, int act, void *out, cudaStream_t stream,
-                        uint64_t timeout_ns, int num_sms, bool early_weights);
+                        const QuantOperand *op1, int variant, int act, void *out, const void *residual,
+                        cudaStream_t stream, uint64_t timeout_ns, int num_sms, bool early_weights);
 
 // Whether the small-M kernel can stage rows of length K (else the tensor-core
 // kernel serves every M).
@@ -53,8 +55,8 @@ cudaError_t prefill_static_workspace(int num_sms, cudaStream_t stream, void **pt
 
 // Tensor-core kernel (tcgen05 + TMA), any M.
 cudaError_t launch_prefill(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                           const QuantOperand *op1, int variant, int act, void *out, cudaStream_t stream,
-                           uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws);
+                           const QuantOperand *op1, int variant, int act, void *out, const void *residual,
+                           cudaStream_t stream, uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws);
 
 cudaError_t launch_silu_mul(const void *g, const void *u, int64_t n, int variant, int act, void *out,
                             cudaStream_t stream);

@@ -111,6 +111,7 @@ struct PrefillParams {
   int sb_tma0, sb_tma1;      // scale ring filled by TMA (else by plain loads)
   int variant;
   uint16_t *out;
+  const uint16_t *res;       // single-operand form: [M, N] added to the accumulator before the rounding (or null)
   int m_tiles, num_tiles, k_steps;
   int sk_tiles;              // tiles [0, sk_tiles) are shared out stream-K style (0: none)
   float *ws_part;            // [grid][kPartFloats] partial accumulators of split tiles
@@ -795,9 +796,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                   default: epilogue16<VAR_DEBUG_UP, A>(ra, rb, packed); break;
                 }
               } else {
+                // y = T(acc + r): the residual joins the f32 accumulator, one rounding
+                uint32_t r2[8];
+                const int64_t rcol = n0 + c0;
+                if (p.res == nullptr) {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) r2[e] = 0u;   // +0 in both halves, bf16 and f16
+                } else if (vec_ok && rcol + 16 <= p.N) {
+                  const uint4 v0 = ld_global_v4(p.res + m * p.N + rcol);
+                  const uint4 v1 = ld_global_v4(p.res + m * p.N + rcol + 8);
+                  r2[0] = v0.x; r2[1] = v0.y; r2[2] = v0.z; r2[3] = v0.w;
+                  r2[4] = v1.x; r2[5] = v1.y; r2[6] = v1.z; r2[7] = v1.w;
+                } else {
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) {
+                    const uint32_t lo = rcol + 2 * e < p.N ? p.res[m * p.N + rcol + 2 * e] : 0u;
+                    const uint32_t hi = rcol + 2 * e + 1 < p.N ? p.res[m * p.N + rcol + 2 * e + 1] : 0u;
+                    r2[e] = lo | (hi << 16);
+                  }
+                }
 #pragma unroll
                 for (int e = 0; e < 16; e += 2)
-                  packed[e / 2] = A::pack2(__uint_as_float(ra[e]), __uint_as_float(ra[e + 1]));
+                  packed[e / 2] = A::pack2(__uint_as_float(ra[e]) + A::lo(r2[e / 2]),
+                                           __uint_as_float(ra[e + 1]) + A::hi(r2[e / 2]));
               }
               const int64_t col = n0 + c0;
               if (vec_ok && col + 16 <= p.N) {
@@ -931,8 +952,8 @@ void plan_split(int64_t tiles, int64_t k_steps, int num_sms, int mode, bool have
 
 template <int BITS0, int BITS1, bool DUAL, class A>
 cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                        const QuantOperand *op1, int variant, void *out, cudaStream_t stream, uint64_t timeout_ns,
-                        int num_sms, const SplitWorkspace &ws) {
+                        const QuantOperand *op1, int variant, void *out, const void *res, cudaStream_t stream,
+                        uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws) {
   using C = Cfg<BITS0, BITS1, DUAL>;
   CUtensorMap tm_x, tm_c0, tm_c1, tm_s0, tm_b0, tm_s1, tm_b1;
   const CUtensorMapDataType x_type = A::kId == ActF16::kId ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
@@ -967,6 +988,7 @@ cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   if (p.sb_tma1 && !encode_scales(&tm_s1, &tm_b1, *op1, K, N, C::kRows1)) return cudaErrorInvalidValue;
   p.variant = variant;
   p.out = static_cast<uint16_t *>(out);
+  p.res = DUAL ? nullptr : static_cast<const uint16_t *>(res);
   p.m_tiles = static_cast<int>((M + BM - 1) / BM);
   const int64_t n_tiles = (N + C::kOutCols - 1) / C::kOutCols;
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * n_tiles;
@@ -1001,32 +1023,32 @@ cudaError_t launch_impl(const void *x, int64_t M, int64_t K, int64_t N, const Qu
 
 template <int BITS0, class A>
 cudaError_t dual_bits1(int bits1, const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                       const QuantOperand *op1, int variant, void *out, cudaStream_t stream, uint64_t timeout_ns,
-                       int num_sms, const SplitWorkspace &ws) {
+                       const QuantOperand *op1, int variant, void *out, const void *res, cudaStream_t stream,
+                       uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws) {
   switch (bits1) {
-    case 2: return launch_impl<BITS0, 2, true, A>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-    case 4: return launch_impl<BITS0, 4, true, A>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-    case 8: return launch_impl<BITS0, 8, true, A>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+    case 2: return launch_impl<BITS0, 2, true, A>(x, M, K, N, op0, op1, variant, out, res, stream, timeout_ns, num_sms, ws);
+    case 4: return launch_impl<BITS0, 4, true, A>(x, M, K, N, op0, op1, variant, out, res, stream, timeout_ns, num_sms, ws);
+    case 8: return launch_impl<BITS0, 8, true, A>(x, M, K, N, op0, op1, variant, out, res, stream, timeout_ns, num_sms, ws);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <class A>
 cudaError_t launch_act(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                       const QuantOperand *op1, int variant, void *out, cudaStream_t stream, uint64_t timeout_ns,
-                       int num_sms, const SplitWorkspace &ws) {
+                       const QuantOperand *op1, int variant, void *out, const void *res, cudaStream_t stream,
+                       uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws) {
   if (op1) {
     switch (op0.bits) {
-      case 2: return dual_bits1<2, A>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-      case 4: return dual_bits1<4, A>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-      case 8: return dual_bits1<8, A>(op1->bits, x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+      case 2: return dual_bits1<2, A>(op1->bits, x, M, K, N, op0, op1, variant, out, res, stream, timeout_ns, num_sms, ws);
+      case 4: return dual_bits1<4, A>(op1->bits, x, M, K, N, op0, op1, variant, out, res, stream, timeout_ns, num_sms, ws);
+      case 8: return dual_bits1<8, A>(op1->bits, x, M, K, N, op0, op1, variant, out, res, stream, timeout_ns, num_sms, ws);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (op0.bits) {
-    case 2: return launch_impl<2, 2, false, A>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
-    case 4: return launch_impl<4, 4, false, A>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
-    case 8: return launch_impl<8, 8, false, A>(x, M, K, N, op0, nullptr, variant, out, stream, timeout_ns, num_sms, ws);
+    case 2: return launch_impl<2, 2, false, A>(x, M, K, N, op0, nullptr, variant, out, res, stream, timeout_ns, num_sms, ws);
+    case 4: return launch_impl<4, 4, false, A>(x, M, K, N, op0, nullptr, variant, out, res, stream, timeout_ns, num_sms, ws);
+    case 8: return launch_impl<8, 8, false, A>(x, M, K, N, op0, nullptr, variant, out, res, stream, timeout_ns, num_sms, ws);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1060,10 +1082,12 @@ cudaError_t prefill_static_workspace(int num_sms, cudaStream_t stream, void **pt
 }
 
 cudaError_t launch_prefill(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                           const QuantOperand *op1, int variant, int act, void *out, cudaStream_t stream,
-                           uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws) {
-  if (act == ActF16::kId) return launch_act<ActF16>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
-  if (act == ActBf16::kId) return launch_act<ActBf16>(x, M, K, N, op0, op1, variant, out, stream, timeout_ns, num_sms, ws);
+                           const QuantOperand *op1, int variant, int act, void *out, const void *residual,
+                           cudaStream_t stream, uint64_t timeout_ns, int num_sms, const SplitWorkspace &ws) {
+  if (act == ActF16::kId)
+    return launch_act<ActF16>(x, M, K, N, op0, op1, variant, out, residual, stream, timeout_ns, num_sms, ws);
+  if (act == ActBf16::kId)
+    return launch_act<ActBf16>(x, M, K, N, op0, op1, variant, out, residual, stream, timeout_ns, num_sms, ws);
   return cudaErrorInvalidValue;
 }
 

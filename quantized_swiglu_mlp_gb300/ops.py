@@ -33,7 +33,7 @@ STATUS = {0: "QSW_OK", 1: "QSW_ERR_INVALID_ARG", 2: "QSW_ERR_UNSUPPORTED", 3: "Q
 STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS = 0, 1, 2
 ACT_BF16, ACT_F16 = 0, 1
 EXPORTED = ("qswiglu_forward", "affine_qmm", "qswiglu_forward_ws", "affine_qmm_ws", "qswiglu_forward_noalloc",
-            "qswiglu_forward_ex", "affine_qmm_ex", "qsw_silu_mul_ex", "qsw_workspace_bytes",
+            "qswiglu_forward_ex", "affine_qmm_ex", "qsw_silu_mul_ex", "qsw_mlp_forward_ex", "qsw_workspace_bytes",
             "qsw_set_stream_k", "qsw_get_stream_k", "qsw_silu_mul", "qsw_check_device_errors",
             "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_early_weight_stream",
             "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns",
@@ -75,8 +75,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.qswiglu_forward_ex.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32, i32, i32, p,
                                            p, sz, p]
         lib.qswiglu_forward_ex.restype = i32
-        lib.affine_qmm_ex.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, i32, p, p, sz, p]
+        lib.affine_qmm_ex.argtypes = [p, i64, i64, i64, p, p, p, i32, i32, i32, p, p, p, sz, p]
         lib.affine_qmm_ex.restype = i32
+        lib.qsw_mlp_forward_ex.argtypes = [p, p, i64, i64, i64, i64, p, p, p, i32, i32, p, p, p, i32, i32,
+                                           p, p, p, i32, i32, i32, i32, p, p, p, sz, p]
+        lib.qsw_mlp_forward_ex.restype = i32
         lib.qsw_silu_mul_ex.argtypes = [p, p, i64, i32, i32, p, p]
         lib.qsw_silu_mul_ex.restype = i32
         lib.qsw_set_stream_k.argtypes = [i32]
@@ -252,10 +255,12 @@ def qswiglu_forward_noalloc(x, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_
     return out.view(*x.shape[:-1], I)
 
 
-def affine_qmm(x, w, s, b, gs, bits, y=None, stream=None, workspace="auto") -> torch.Tensor:
-    """y = bf16(x . W^T) with W affine-quantised; returns bf16 [..., N].
+def affine_qmm(x, w, s, b, gs, bits, y=None, stream=None, workspace="auto", residual=None) -> torch.Tensor:
+    """y = T(x . W^T + residual) with W affine-quantised, T = x's dtype; returns [..., N].
 
-    workspace: as for qswiglu_forward; x may be bfloat16 or float16.
+    workspace: as for qswiglu_forward; x may be bfloat16 or float16.  residual:
+    None, or an [..., N] tensor of x's dtype added before the one rounding (it
+    may be y itself).
     """
     lib = load_library()
     _need(x, "x", tuple(_ACT))
@@ -270,11 +275,63 @@ def affine_qmm(x, w, s, b, gs, bits, y=None, stream=None, workspace="auto") -> t
         _need(y, "y", (dt,), x.device)
         if y.numel() != M * N:
             raise ValueError("y has the wrong size")
+    r_ptr = None
+    if residual is not None:
+        _need(residual, "residual", (dt,), x.device)
+        if residual.numel() != M * N:
+            raise ValueError("residual has the wrong size")
+        r_ptr = residual.data_ptr()
     ws_ptr, ws_bytes = _workspace_arg(workspace, x.device, stream)
     code = lib.affine_qmm_ex(x2.data_ptr(), M, K, N, w.data_ptr(), s.data_ptr(), b.data_ptr(),
-                             int(gs), int(bits), _ACT[dt], y.data_ptr(), ws_ptr, ws_bytes, _stream_ptr(stream))
+                             int(gs), int(bits), _ACT[dt], r_ptr, y.data_ptr(), ws_ptr, ws_bytes,
+                             _stream_ptr(stream))
     _check("affine_qmm_ex", code)
     return y.view(*x.shape[:-1], N)
+
+
+def mlp_forward(x, h, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, wd, sd, bd, gs_d, bits_d,
+                variant=MATCH, out=None, hidden=None, stream=None, workspace="auto") -> torch.Tensor:
+    """The whole MLP block: y = T(h + (silu(x . Wg^T) * (x . Wu^T)) . Wd^T).
+
+    h: the residual [..., Ho] (x's dtype) or None; it may be `out`.  hidden: an
+    [M, I] buffer for the intermediate (allocated when None).  Returns y [..., Ho].
+    """
+    lib = load_library()
+    _need(x, "x", tuple(_ACT))
+    dt = x.dtype
+    H = x.shape[-1]
+    x2 = x.reshape(-1, H)
+    M = x2.shape[0]
+    I = _operand(wg, sg, bg, "gate", x.device, H, bits_g, gs_g, dt)
+    if _operand(wu, su, bu, "up", x.device, H, bits_u, gs_u, dt) != I:
+        raise ValueError("gate and up must have the same number of rows")
+    Ho = _operand(wd, sd, bd, "down", x.device, I, bits_d, gs_d, dt)
+    if hidden is None:
+        hidden = torch.empty((M, I), dtype=dt, device=x.device)
+    else:
+        _need(hidden, "hidden", (dt,), x.device)
+        if hidden.numel() != M * I:
+            raise ValueError("hidden has the wrong size")
+    if out is None:
+        out = torch.empty((M, Ho), dtype=dt, device=x.device)
+    else:
+        _need(out, "out", (dt,), x.device)
+        if out.numel() != M * Ho:
+            raise ValueError("out has the wrong size")
+    h_ptr = None
+    if h is not None:
+        _need(h, "h", (dt,), x.device)
+        if h.numel() != M * Ho:
+            raise ValueError("h has the wrong size")
+        h_ptr = h.data_ptr()
+    ws_ptr, ws_bytes = _workspace_arg(workspace, x.device, stream)
+    code = lib.qsw_mlp_forward_ex(x2.data_ptr(), h_ptr, M, H, I, Ho, wg.data_ptr(), sg.data_ptr(), bg.data_ptr(),
+                                  int(gs_g), int(bits_g), wu.data_ptr(), su.data_ptr(), bu.data_ptr(), int(gs_u),
+                                  int(bits_u), wd.data_ptr(), sd.data_ptr(), bd.data_ptr(), int(gs_d), int(bits_d),
+                                  int(variant), _ACT[dt], hidden.data_ptr(), out.data_ptr(), ws_ptr, ws_bytes,
+                                  _stream_ptr(stream))
+    _check("qsw_mlp_forward_ex", code)
+    return out.view(*x.shape[:-1], Ho)
 
 
 def qsw_silu_mul(g, u, variant=MATCH, out=None, stream=None) -> torch.Tensor:

@@ -438,8 +438,64 @@ def pin_f16_silu_exhaustive(orc):
             assert got_f[j] == ref_f16(gv * ub / (1.0 + math.exp(-gv))), (gv, uval)
 
 
+# ------------------------------------------------- whole MLP, residual -----
+
+def _mlp_case(M, H, I, Ho, dtype, seed):
+    case = inputs.make_case(M, H, I, bits_g=4, gs_g=32, bits_u=8, gs_u=32, seed=seed, dtype=dtype)
+    down = inputs.make_case(1, I, Ho, bits_g=4, gs_g=32, seed=seed + 100, dtype=dtype).gate
+    h = inputs.make_x(M, Ho, seed=seed + 200, dtype=dtype)
+    return case, down, h
+
+
+def _brute_down(hidden_bits, down, h_bits, dtype):
+    """y = T(h + hidden . Wd^T) with exact rational sums."""
+    to_bits, val = REF[dtype]
+    M, I = hidden_bits.shape
+    Ho = down.packed.shape[0]
+    codes = [ref_codes_from_words(r, I, down.bits) for r in down.packed]
+    W = [[Fraction(val(to_bits(float(Fraction(val(int(down.scales[o, k // down.gs]))) * codes[o][k]
+                                      + Fraction(val(int(down.biases[o, k // down.gs]))))))) for k in range(I)]
+         for o in range(Ho)]
+    y = np.zeros((M, Ho), dtype=np.uint16)
+    for m in range(M):
+        hid = [Fraction(val(int(t))) for t in hidden_bits[m]]
+        for o in range(Ho):
+            acc = sum(hid[k] * W[o][k] for k in range(I))
+            if h_bits is not None:
+                acc += Fraction(val(int(h_bits[m, o])))
+            y[m, o] = to_bits(float(acc))
+    return y
+
+
+def pin_mlp_brute_force(orc):
+    """The whole block against exact rational sums (bf16 and f16): hidden is
+    the fused expansion, y = T(h + hidden . Wd^T) with one rounding."""
+    for dtype, seed in (("bf16", 21), ("f16", 22)):
+        case, down, h = _mlp_case(2, 64, 32, 5, dtype, seed)
+        for v in (MATCH, F32):
+            y, hidden = orc.mlp(case.x, h, *case.oracle_args()[1:], down.packed, down.scales, down.biases,
+                                down.gs, down.bits, variant=v, dtype=dtype)
+            assert np.array_equal(hidden, brute_force(case, v)), (dtype, v)
+            assert np.array_equal(y, _brute_down(hidden, down, h, dtype)), (dtype, v)
+        y0 = orc.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, case.gate.gs,
+                     case.gate.bits, dtype=dtype, residual=None)
+        assert np.array_equal(y0, brute_force(case, DEBUG_GATE))
+
+
+def pin_mlp_zero_input(orc):
+    """x = 0 gives hidden = 0 and y = h exactly; with no residual y = +0."""
+    for dtype in ("bf16", "f16"):
+        case, down, h = _mlp_case(3, 96, 64, 7, dtype, 23)
+        case.x[:] = 0
+        args = (*case.oracle_args()[1:], down.packed, down.scales, down.biases, down.gs, down.bits)
+        y, hidden = orc.mlp(case.x, h, *args, variant=MATCH, dtype=dtype)
+        assert np.all(hidden == 0) and np.array_equal(y, h)
+        y, _ = orc.mlp(case.x, None, *args, variant=F32, dtype=dtype)
+        assert np.all(y == 0)
+
+
 ALL_PINS = [pin_bf16_binary32, pin_bf16_double, pin_unpack, pin_hand_example,
             pin_zero_input, pin_integer_case, pin_brute_force, pin_k_permutation,
             pin_silu_values, pin_silu_exhaustive, pin_match_is_unfused, pin_sampled_pairs,
             pin_f16_decode, pin_f16_double, pin_f16_hand_example, pin_f16_brute_force,
-            pin_f16_silu_exhaustive]
+            pin_f16_silu_exhaustive, pin_mlp_brute_force, pin_mlp_zero_input]

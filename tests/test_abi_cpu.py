@@ -180,3 +180,18 @@ def test_noalloc_entry_point_validates_on_the_host(lib):
     assert call(-1, 0) == INVALID
     assert call(4, 7) == INVALID
     assert call(4, 0, x=FAKE + 8) == UNSUPPORTED
+
+
+def test_mlp_entry_point_validates_on_the_host(lib):
+    """The whole-MLP entry point checks both stages' arguments first."""
+    def mlp(M=4, variant=0, act=0, h=None, hidden=FAKE, I=64, gs_d=32, bits_d=4):
+        return lib.qsw_mlp_forward_ex(FAKE, h, M, 256, I, 96, FAKE, FAKE, FAKE, 64, 4, FAKE, FAKE, FAKE, 64, 4,
+                                      FAKE, FAKE, FAKE, gs_d, bits_d, variant, act, hidden, FAKE, None, 0, None)
+    assert mlp(M=0) == OK
+    assert mlp(variant=2) == INVALID            # debug variants have no whole-block meaning
+    assert mlp(act=3) == INVALID
+    assert mlp(hidden=None) == INVALID
+    assert mlp(h=FAKE + 2) == UNSUPPORTED        # residual alignment
+    assert mlp(gs_d=48) == UNSUPPORTED           # down group size
+    assert mlp(I=48) == UNSUPPORTED              # I is the down projection's K
+    assert mlp(bits_d=3) == UNSUPPORTED

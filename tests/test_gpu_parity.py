@@ -13,7 +13,7 @@ import torch
 import oracle
 from quantized_swiglu_mlp_gb300 import inputs, ops
 from tests.gpu_util import device_args, to_bits
-from tests.tolerances import check_f32, check_match, check_match_with_projections, check_projection
+from tests.tolerances import TO_F64, check_f32, check_match, check_match_with_projections, check_projection
 
 pytestmark = pytest.mark.gpu
 
@@ -659,3 +659,96 @@ def test_plain_bf16_entry_points(dev, gemv_limit):
         want = oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gsg, btg)
         ok, info = check_projection(to_bits(y), want)
         assert ok, info
+
+
+# ---------------------------------------------- residual and whole MLP ----
+
+def _mlp_inputs(M, H, I, Ho, dtype, seed):
+    case = inputs.make_case(M, H, I, bits_g=4, gs_g=64, bits_u=8, gs_u=32, seed=seed, dtype=dtype)
+    down = inputs.make_case(1, I, Ho, bits_g=4, gs_g=64, seed=seed + 1, dtype=dtype).gate
+    h = inputs.make_x(M, Ho, seed=seed + 2, dtype=dtype)
+    return case, down, h
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
+def test_affine_qmm_residual(dev, gemv_limit, dtype, limit):
+    """y = T(x . W^T + r): the residual joins the f32 accumulator before the
+    one rounding, also when y is r itself."""
+    M, K, N = (5, 1024, 300) if limit else (140, 640, 300)
+    case = inputs.make_case(M, K, N, bits_g=4, gs_g=64, seed=71, dtype=dtype)
+    r = inputs.make_x(M, N, seed=72, x_std=3.0, dtype=dtype)
+    gemv_limit(limit)
+    x, w, s, b, gs, bits = device_args(case, dev)[:6]
+    rd = inputs.bits_to_device(r, dev, dtype)
+    got = to_bits(ops.affine_qmm(x, w, s, b, gs, bits, residual=rd))
+    inplace = rd.clone()
+    ops.affine_qmm(x, w, s, b, gs, bits, y=inplace, residual=inplace)
+    ops.qsw_check_device_errors()
+    want = oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gs, bits, dtype=dtype,
+                      residual=r)
+    ok, info = check_projection(got, want, dtype)
+    assert ok, info
+    assert np.array_equal(to_bits(inplace), got)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
+@pytest.mark.parametrize("variant", [ops.MATCH, ops.F32], ids=["match", "f32"])
+def test_mlp_forward(dev, gemv_limit, dtype, limit, variant):
+    """The whole block: hidden is exactly the fused expansion's output, and y
+    is the down projection of that hidden plus the residual (checked against
+    the oracle fed the GPU's hidden, and end to end against the oracle's block)."""
+    M = 5 if limit else 130
+    case, down, h = _mlp_inputs(M, 512, 256, 200, dtype, 31)
+    gemv_limit(limit)
+    a = device_args(case, dev)
+    d = inputs.operand_to_device(down, dev, dtype)
+    hd = inputs.bits_to_device(h, dev, dtype)
+    hidden = torch.empty((M, 256), dtype=inputs.TORCH_DTYPES[dtype], device=dev)
+    y = to_bits(ops.mlp_forward(a[0], hd, *a[1:], *d, variant=variant, hidden=hidden))
+    fused = to_bits(ops.qswiglu_forward(*a, variant=variant))
+    ops.qsw_check_device_errors()
+    hid = to_bits(hidden)
+    assert np.array_equal(hid, fused)
+    want = oracle.qmm(hid, down.packed, down.scales, down.biases, down.gs, down.bits, dtype=dtype, residual=h)
+    ok, info = check_projection(y, want, dtype)
+    assert ok, info
+    y_ref, _ = oracle.mlp(case.x, h, *case.oracle_args()[1:], down.packed, down.scales, down.biases, down.gs,
+                          down.bits, variant=variant, dtype=dtype)
+    yg, yr = TO_F64[dtype](y), TO_F64[dtype](y_ref)
+    assert np.linalg.norm(yg - yr) <= 1e-2 * np.linalg.norm(yr)
+
+
+def test_mlp_forward_in_place_and_no_residual(dev, gemv_limit):
+    case, down, h = _mlp_inputs(40, 512, 128, 96, "bf16", 41)
+    gemv_limit(0)
+    a = device_args(case, dev)
+    d = inputs.operand_to_device(down, dev)
+    hd = inputs.bits_to_device(h, dev)
+    ref = to_bits(ops.mlp_forward(a[0], hd, *a[1:], *d))
+    inplace = hd.clone()
+    ops.mlp_forward(a[0], inplace, *a[1:], *d, out=inplace)
+    none = to_bits(ops.mlp_forward(a[0], None, *a[1:], *d))
+    ops.qsw_check_device_errors()
+    assert np.array_equal(to_bits(inplace), ref)
+    hid = to_bits(ops.qswiglu_forward(*a))
+    want = oracle.qmm(hid, down.packed, down.scales, down.biases, down.gs, down.bits)
+    ok, info = check_projection(none, want)
+    assert ok, info
+
+
+def test_full_mlp_decode(dev, gemv_limit):
+    """The decode shape as a whole block: H = Ho = 2048, I = 8192, 4-bit gs 64."""
+    case = inputs.workload_case("decode")
+    down = inputs.make_case(1, 8192, 2048, bits_g=4, gs_g=64, seed=5).gate
+    h = inputs.make_x(1, 2048, seed=6)
+    gemv_limit(16)
+    a = device_args(case, dev)
+    d = inputs.operand_to_device(down, dev)
+    hidden = torch.empty((1, 8192), dtype=torch.bfloat16, device=dev)
+    y = to_bits(ops.mlp_forward(a[0], inputs.bits_to_device(h, dev), *a[1:], *d, hidden=hidden))
+    ops.qsw_check_device_errors()
+    want = oracle.qmm(to_bits(hidden), down.packed, down.scales, down.biases, 64, 4, residual=h)
+    ok, info = check_projection(y, want)
+    assert ok, info

@@ -24,14 +24,19 @@ MUTANTS = {
     "dropped_term": ("for (int64_t k = 0; k < K; ++k) acc += xr[k] * wr[k];",
                      "for (int64_t k = 1; k < K; ++k) acc += xr[k] * wr[k];"),
     "silu_uses_up": ("return ract(silu * ub, dt);", "return ract(silu * gb, dt);"),
-    "qmm_transposed": ("y[m * N + n] = f64_to_act(dot_f64(xd + m * K, wr, K), dt);",
-                       "y[(n % M) * N + (m + n / M) % N] = f64_to_act(dot_f64(xd + m * K, wr, K), dt);"),
+    "qmm_transposed": ("y[m * N + n] = f64_to_act(acc, dt);",
+                       "y[(n % M) * N + (m + n / M) % N] = f64_to_act(acc, dt);"),
     "subnormal_spacing": ("if (ulp_exp < -133) ulp_exp = -133;", "if (ulp_exp < -126) ulp_exp = -126;"),
     "f16_one_bit_short": ("int ulp_exp = e - 10;", "int ulp_exp = e - 9;"),
     "f16_subnormal_spacing": ("if (ulp_exp < -24) ulp_exp = -24;", "if (ulp_exp < -14) ulp_exp = -14;"),
     "f16_exponent_bias": ("(uint16_t)((e + 15) << 10)", "(uint16_t)((e + 16) << 10)"),
     "f16_overflow_early": ("if (r >= 65536.0) return", "if (r >= 32768.0) return"),
     "f16_decode_bias": ("else a = ldexp((double)(1024 + fr), ex - 25);", "else a = ldexp((double)(1024 + fr), ex - 24);"),
+    "residual_dropped": ("if (r) acc += act_to_f64(r[m * N + n], dt);", "(void)r;"),
+    "residual_rounded_first": ("y[m * N + n] = f64_to_act(acc, dt);",
+                               "y[m * N + n] = f64_to_act(r ? act_to_f64(f64_to_act(acc - act_to_f64(r[m * N + n], dt), dt), dt) + act_to_f64(r[m * N + n], dt) : acc, dt);"),
+    "mlp_skips_silu": ("int rc = orc_qswiglu(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, variant, dt, hidden);",
+                       "int rc = orc_qswiglu(x, M, H, I, wg, sg, bg, gs_g, bits_g, wu, su, bu, gs_u, bits_u, ORC_DEBUG_UP, dt, hidden);"),
     "dequant_ignores_dtype": ("out[r * K + k] = act_to_f64(f64_to_act(sc * q + bi, dt), dt);",
                               "out[r * K + k] = orc_bf16_to_f64(orc_f64_to_bf16(sc * q + bi));"),
 }
