@@ -328,6 +328,54 @@ def bench_prefill(args, dev, stream, peaks, peak_src):
         res.update(_bench_mixed_sweep(args, dev, stream))
     if args.only in ("all", "f16"):
         res.update(_bench_f16(args, dev, stream))
+    if args.only in ("all", "mlp"):
+        res.update(_bench_mlp(args, dev, stream))
+    return res
+
+
+def _bench_mlp(args, dev, stream):
+    """The whole MLP block y = h + (silu(x.Wg^T)*(x.Wu^T)).Wd^T (Ho = H, down
+    4-bit gs 64) at the decode and mid shapes, MATCH, bf16: decode as weight
+    GB/s over the three matrices (replicas > 3x L2, early weight stream on, as
+    in a decode loop), mid as TFLOP/s of the three projections."""
+    import torch
+    from quantized_swiglu_mlp_gb300 import inputs, ops
+
+    res = {}
+    saved = ops.qsw_get_early_weight_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    try:
+        for name in ("decode", "mid_prefill"):
+            case = inputs.workload_case(name)
+            down = inputs.make_case(1, case.I, case.H, bits_g=4, gs_g=64, seed=1).gate
+            wbytes = weight_bytes(case) + down.packed.nbytes + down.scales.nbytes + down.biases.nbytes
+            a = to_device(case, dev)
+            d = inputs.operand_to_device(down, dev)
+            h = inputs.bits_to_device(inputs.make_x(case.M, case.H, seed=2), dev)
+            reps = max(1, int(np.ceil(3.2 * l2 / wbytes))) if case.M == 1 else 1
+            sets = [(a[1:], d)] + [(tuple(t.clone() if isinstance(t, torch.Tensor) else t for t in a[1:]),
+                                    tuple(t.clone() if isinstance(t, torch.Tensor) else t for t in d))
+                                   for _ in range(reps - 1)]
+            hidden = torch.empty((case.M, case.I), dtype=torch.bfloat16, device=dev)
+            out = torch.empty((case.M, case.H), dtype=torch.bfloat16, device=dev)
+            ops.qsw_set_early_weight_stream(case.M == 1)
+            steps = 200 if case.M == 1 else args.prefill_steps
+
+            def step(i):
+                gu, dd = sets[i % len(sets)]
+                ops.mlp_forward(a[0], h, *gu, *dd, hidden=hidden, out=out, stream=stream)
+
+            ms = time_graph(step, steps, 3, stream)
+            us = ms * 1e3 / steps
+            flops = 6.0 * case.M * case.H * case.I
+            key = "mlp_decode" if case.M == 1 else "mlp_mid"
+            res[key] = {"us_per_block": round(us, 2), "weight_GBps": round(wbytes / us / 1e3, 1),
+                        "tflops": round(flops / us / 1e6, 1)}
+            del a, d, sets, hidden, out
+            torch.cuda.empty_cache()
+    finally:
+        ops.qsw_set_early_weight_stream(saved)
+    ops.qsw_check_device_errors(stream)
     return res
 
 
@@ -636,7 +684,7 @@ def main(argv=None):
                     help="stream-K scheduling of the tensor-core kernel (library switch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--only", choices=["all", "decode", "large", "mid", "sweep", "f16"], default="all",
+    ap.add_argument("--only", choices=["all", "decode", "large", "mid", "sweep", "f16", "mlp"], default="all",
                     help="run one workload only (profiling); the JSON line then carries what ran")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="untimed load before the timed region, so the clock sampler sees it")

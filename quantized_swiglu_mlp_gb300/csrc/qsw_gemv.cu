@@ -6,8 +6,10 @@
 // streams the packed rows from HBM exactly once, as early and as deep as
 // possible, and keeps everything but the dequantisation off the critical path:
 //
-//  * unit of work: 8 output rows (fused: rows r..r+7 of Wg AND of Wu) or 16
-//    rows (single linear).  One persistent CTA per SM takes units round-robin.
+//  * unit of work: 8 output rows (fused: rows r..r+7 of Wg AND of Wu; single
+//    linear: rows r..r+7 of W, A rows 8..15 of the MMA left zero, so that a
+//    unit stays small at large K).  One persistent CTA per SM takes units
+//    round-robin.
 //  * a unit's rows are contiguous in HBM: ONE 1-D bulk (TMA) copy per array
 //    (codes of each operand, each scale and bias array) lands it in a
 //    shared-memory ring slot, completing on the slot's mbarrier.  At kernel
@@ -17,7 +19,9 @@
 //    blocks per unit and the per-unit bookkeeping stays small.  One warp of the
 //    group adds the 4 partial sums in a fixed order and applies the epilogue.
 //  * x is the same for every unit: it is staged once per CTA in shared memory,
-//    already permuted into MMA B-fragment order (bank-conflict-free reads).
+//    already permuted into MMA B-fragment order (bank-conflict-free reads);
+//    only its M real rows are stored (the padding rows of the 8-row fragment
+//    are zeros made at the read), so K = 8192 fits at small M.
 //  * a lane (g = lane/4, c = lane%4) dequantises 32 codes of gate row g and of
 //    up row g to the activation dtype T (bf16 or f16) in registers
 //    (w = T(s*q + b), one rounding) and feeds
@@ -45,7 +49,7 @@ constexpr int kBlockK = 128;                    // codes per K block
 constexpr int kChunk = 32;                      // codes per lane per block
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kMaxSlots = 16;
-constexpr int kXBlockBytes = 4 * 32 * 16;       // B fragments of one block, one x row group (2 KB)
+constexpr int kXBlockBytes = 4 * 32 * 16;       // B fragments of one block, one full x row group (2 KB)
 constexpr int kXPre = 4;                        // x pieces per thread requested ahead of the weights
 
 __device__ unsigned int g_gemv_error;
@@ -57,6 +61,7 @@ struct GemvParams {
   const uint16_t *s0, *b0, *s1, *b1;
   GroupDiv gd0, gd1;
   uint32_t ng0, ng1;      // groups per row (K / gs)
+  int x_rows;             // x rows staged per row group: min(8, M) (the others are zero fragments)
   int variant;
   uint16_t *out;
   const uint16_t *res;    // single-operand form: [M, N] added before the rounding (or null)
@@ -150,7 +155,7 @@ struct Chunk {
 template <int BITS0, int BB, bool DUAL>
 __device__ __forceinline__ void issue_unit(const GemvParams &p, uint8_t *base, uint64_t *bar, unsigned int *issued,
                                            int u, int lane) {
-  constexpr int R = DUAL ? 8 : 16;
+  constexpr int R = 8;
   const uint32_t r0 = static_cast<uint32_t>(u) * R;
   const uint32_t rows = static_cast<uint32_t>(p.N) - r0 < static_cast<uint32_t>(R) ? static_cast<uint32_t>(p.N) - r0
                                                                                      : static_cast<uint32_t>(R);
@@ -176,7 +181,7 @@ __device__ __forceinline__ void issue_unit(const GemvParams &p, uint8_t *base, u
 
 template <int BITS0, int BITS1, bool DUAL, int NG, class A>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
-  constexpr int R = DUAL ? 8 : 16;          // output rows per unit
+  constexpr int R = 8;                      // output rows per unit
   constexpr int BB = DUAL ? BITS1 : BITS0;
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);               // [kMaxSlots]
@@ -220,9 +225,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
   // the weight stream of all SMs, x would only arrive microseconds later.  The
   // last warp issues the copies and stages no x: issuing stalls while the copy
   // engine is saturated, and no other warp should wait for that.
-  const int x_total = static_cast<int>(nkb) * NG * 32;   // (kb, G, lane) triples
+  // Only the lanes of real x rows are staged: lane L = 4n + c carries row n
+  // of a group, so rows n >= x_rows (padding when M < 8) are zero fragments
+  // synthesised at the read, and a block of one group takes x_rows * 64 bytes.
+  const int x_lanes = 4 * p.x_rows;                        // staged lanes per (block, group)
+  const uint32_t x_piece = static_cast<uint32_t>(p.x_rows) * 64;   // bytes per (block, group, j)
+  const int x_total = static_cast<int>(nkb) * NG * x_lanes;   // (kb, G, lane) triples
   auto load_x = [&](int e, uint4 (&xv)[4]) {
-    const int L = e & 31, G = (e >> 5) % NG, kb = (e >> 5) / NG;
+    const int L = e % x_lanes, G = (e / x_lanes) % NG, kb = (e / x_lanes) / NG;
     const int m = 8 * G + (L >> 2);
     const uint32_t k = static_cast<uint32_t>(kb) * kBlockK + (L & 3) * kChunk;
     if (k < K && m < p.M) {
@@ -235,15 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     }
   };
   auto store_x = [&](int e, const uint4 (&xv)[4]) {
-    const int L = e & 31, G = (e >> 5) % NG, kb = (e >> 5) / NG;
-    uint8_t *dst = smem + p.x_off + static_cast<size_t>(kb * NG + G) * kXBlockBytes + L * 16;
+    const int L = e % x_lanes, G = (e / x_lanes) % NG, kb = (e / x_lanes) / NG;
+    uint8_t *dst = smem + p.x_off + static_cast<size_t>(kb * NG + G) * 4 * x_piece + L * 16;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {   // x values 8j..8j+7: (x0,x1) (x2,x3) (x4,x5) (x6,x7)
       const uint4 f = make_uint4(prmt(xv[j].x, xv[j].z, 0x5410u),    // h=0: (x0, x4)
                                  prmt(xv[j].x, xv[j].z, 0x7632u),    //      (x1, x5)
                                  prmt(xv[j].y, xv[j].w, 0x5410u),    // h=1: (x2, x6)
                                  prmt(xv[j].y, xv[j].w, 0x7632u));   //      (x3, x7)
-      *reinterpret_cast<uint4 *>(dst + j * 512) = f;
+      *reinterpret_cast<uint4 *>(dst + j * x_piece) = f;
     }
   };
   constexpr int kStageThreads = kThreads - 32;
@@ -311,20 +321,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
   const int grp = warp / kGroupWarps, gw = warp % kGroupWarps;
   const int g = lane >> 2, c = lane & 3;
   const uint32_t sb0 = R * p.ng0 * 2, sb1 = DUAL ? R * p.ng1 * 2 : 0;
-  const uint32_t xbase = smem_u32(smem + p.x_off) + lane * 16;
+  // lanes past the staged rows read lane 0's piece and zero it (rows >= M)
+  const bool x_live = lane < x_lanes;
+  const uint32_t xbase = smem_u32(smem + p.x_off) + (x_live ? lane : 0) * 16;
   for (int ig = 0; x_ok; ++ig) {
     const int i = grp + ig * kGroups;
     if (i >= my_units) break;
     const int slot = grp * spg + ig % spg, round = ig / spg;
     if (!warp_wait_lazy(&full[slot], round & 1, abort_flag, p.timeout_ns, err, 2000)) break;
     const uint32_t base = smem_u32(smem + slot * p.slot_bytes);
-    const int ga = g, gb = DUAL ? g : g + 8;   // unit rows fed to A rows g and g+8
+    // A rows g (gate, or the single operand) and g+8 (up; zero in the
+    // single-operand form, whose units are 8 rows of one matrix)
+    const int ga = g, gb = g;
     const uint32_t rowa = base + ga * p.pitch0 + c * (kChunk * BITS0 / 8);
-    const uint32_t rowb = (DUAL ? base + R * p.pitch0 + gb * p.pitch1 : base + gb * p.pitch0) + c * (kChunk * BB / 8);
+    const uint32_t rowb = base + R * p.pitch0 + gb * p.pitch1 + c * (kChunk * BB / 8);
     const uint32_t sbase = base + p.sb_off;
     const uint32_t s_a = sbase + ga * p.ng0 * 2, b_a = s_a + sb0;
-    const uint32_t s_b = DUAL ? sbase + 2 * sb0 + gb * p.ng1 * 2 : sbase + gb * p.ng0 * 2;
-    const uint32_t b_b = s_b + (DUAL ? sb1 : sb0);
+    const uint32_t s_b = sbase + 2 * sb0 + gb * p.ng1 * 2;
+    const uint32_t b_b = s_b + sb1;
     float sum[NG][4];
 #pragma unroll
     for (int G = 0; G < NG; ++G)
@@ -342,12 +356,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
       uint32_t sa = 0, ba = 0, sb = 0, bb = 0;
       if (kval) {
         ca.load(rowa + kb * (kBlockK * BITS0 / 8));
-        cb.load(rowb + kb * (kBlockK * BB / 8));
-        const uint32_t ia = p.gd0(k) * 2, ib = (DUAL ? p.gd1 : p.gd0)(k) * 2;
+        const uint32_t ia = p.gd0(k) * 2;
         sa = lds_u16(s_a + ia);
         ba = lds_u16(b_a + ia);
-        sb = lds_u16(s_b + ib);
-        bb = lds_u16(b_b + ib);
+        if (DUAL) {
+          cb.load(rowb + kb * (kBlockK * BB / 8));
+          const uint32_t ib = p.gd1(k) * 2;
+          sb = lds_u16(s_b + ib);
+          bb = lds_u16(b_b + ib);
+        } else {
+#pragma unroll
+          for (int q = 0; q < Chunk<BB, A>::kWords; ++q) cb.w[q] = 0;
+        }
       } else {
 #pragma unroll
         for (int q = 0; q < Chunk<BITS0, A>::kWords; ++q) ca.w[q] = 0;
@@ -364,12 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
         for (int q = 0; q < 4; ++q) acc[G][q] = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint32_t pa[4], pb[4];
+        uint32_t pa[4], pb[4] = {0u, 0u, 0u, 0u};
         ca.dequant(j, sa2, ba2, pa);
-        cb.dequant(j, sb2, bb2, pb);
+        if (DUAL) cb.dequant(j, sb2, bb2, pb);
 #pragma unroll
         for (int G = 0; G < NG; ++G) {
-          const uint4 xf = lds128(xbase + ((kb * NG + G) * 4 + j) * 512);
+          uint4 xf = lds128(xbase + ((kb * NG + G) * 4 + j) * x_piece);
+          if (!x_live) xf = make_uint4(0u, 0u, 0u, 0u);
           // A rows g (operand a) and g+8 (operand b); k_local 2c,2c+1 <- pair 2h,
           // k_local 2c+8,2c+9 <- pair 2h+1
           const uint32_t a0[4] = {pa[0], pb[0], pa[1], pb[1]};
@@ -461,7 +482,7 @@ struct Layout {
 
 // Shared-memory layout for the given shape; slots == 0 when it does not fit.
 Layout plan(int64_t K, int64_t N, int M, int gs0, int gs1, int bits0, int bits1, bool dual, int num_sms) {
-  const int64_t R = dual ? 8 : 16;
+  const int64_t R = 8;
   const int NG = M <= 8 ? 1 : M <= 16 ? 2 : 4;
   const int64_t pitch0 = K * bits0 / 8, pitch1 = dual ? K * bits1 / 8 : 0;
   const int64_t ng = K / gs0 + (dual ? K / gs1 : 0);
@@ -469,7 +490,8 @@ Layout plan(int64_t K, int64_t N, int M, int gs0, int gs1, int bits0, int bits1,
   l.sb_off = static_cast<int>(R * (pitch0 + pitch1));
   l.slot_bytes = static_cast<int>((l.sb_off + R * 4 * ng + 127) / 128 * 128);
   const int64_t nkb = (K + kBlockK - 1) / kBlockK;
-  const int64_t x_bytes = nkb * NG * kXBlockBytes;
+  const int64_t x_rows = M < 8 ? M : 8;
+  const int64_t x_bytes = nkb * NG * kXBlockBytes * x_rows / 8;
   const int64_t red_bytes = static_cast<int64_t>(kGroups) * 2 * kGroupWarps * NG * 128 * 4;
   const int64_t bar_bytes = (kMaxSlots + 4 * kGroups + 2) * 8 + 2 * kMaxSlots * 4 + 16;
   const int64_t fixed = x_bytes + red_bytes + bar_bytes;
@@ -495,7 +517,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 template <int BITS0, int BITS1, bool DUAL, int NG, class A>
 cudaError_t launch_cfg(GemvParams p, const Layout &l, cudaStream_t stream, int num_sms) {
-  constexpr int R = DUAL ? 8 : 16;
+  constexpr int R = 8;
   p.pitch0 = p.K * BITS0 / 8;
   p.pitch1 = DUAL ? p.K * BITS1 / 8 : 0;
   p.units = (p.N + R - 1) / R;
@@ -598,6 +620,7 @@ cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   p.gd1 = GroupDiv::make(o1.gs);
   p.ng0 = static_cast<uint32_t>(K / op0.gs);
   p.ng1 = static_cast<uint32_t>(K / o1.gs);
+  p.x_rows = M < 8 ? static_cast<int>(M) : 8;
   p.variant = variant;
   p.out = static_cast<uint16_t *>(out);
   p.res = op1 ? nullptr : static_cast<const uint16_t *>(residual);

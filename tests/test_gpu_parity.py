@@ -752,3 +752,19 @@ def test_full_mlp_decode(dev, gemv_limit):
     want = oracle.qmm(to_bits(hidden), down.packed, down.scales, down.biases, 64, 4, residual=h)
     ok, info = check_projection(y, want)
     assert ok, info
+
+
+@pytest.mark.parametrize("M", [1, 2])
+def test_small_m_large_k_single_operand(dev, gemv_limit, M):
+    """The decode-size down projection (K = 8192, N = 2048) runs on the small-M
+    kernel: x is staged with its real rows only and units are 8 rows."""
+    case = inputs.make_case(M, 8192, 2048, bits_g=4, gs_g=64, seed=90 + M)
+    gemv_limit(16)
+    x, w, s, b, gs, bits = device_args(case, dev)[:6]
+    before = ops.qsw_get_counters()[ops.CNT_QMM_GEMV]
+    got = to_bits(ops.affine_qmm(x, w, s, b, gs, bits))
+    ops.qsw_check_device_errors()
+    assert ops.qsw_get_counters()[ops.CNT_QMM_GEMV] == before + 1
+    want = oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gs, bits)
+    ok, info = check_projection(got, want)
+    assert ok, info
