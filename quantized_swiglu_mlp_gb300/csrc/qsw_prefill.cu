@@ -10,16 +10,19 @@
 //
 // GB300 design (sm_103a), one persistent CTA per SM, warp-specialised, three
 // shared-memory rings filled by TMA and one filled by the dequantisers:
-//   x ring      x tile [256 x 64] bf16, 128-byte swizzle     TMA    -> MMA
-//   codes ring  packed codes of the tile's 128 B rows          TMA    -> dequant
-//   scale ring  per operand: scales and biases of 8 groups     TMA    -> dequant
-//   B ring      dequantised bf16 B tile [128 x 64], swizzled   dequant -> MMA
+//   x ring      stages of 2 x tiles [256 x 64], 128-byte swizzle   TMA -> MMA
+//   codes ring  packed codes of the tile's 128 B rows, per K step  TMA -> dequant
+//   scale ring  per operand: scales and biases of 8 groups         TMA -> dequant
+//   B ring      stages of 2 dequantised B tiles [128 x 64]         dequant -> MMA
+// (a stage is two 64-wide K steps: the MMA issuer pays one barrier wait and
+// one commit per 16 UMMAs instead of per 8, and those shared-memory round
+// trips are what its loop spends beyond the tensor core's own time).
 // Roles:
 //   warp 0      producer of the codes and scale rings;
 //   warp 1      TMEM owner and MMA issuer: per 64-wide K step, 2 x 4
 //               tcgen05.mma kind::f16 M=128 N=128 K=16, one per 128-row half of
 //               the x tile, both against the same B tile (every dequantised
-//               weight serves 256 rows of x);
+//               weight serves 256 rows of x), two K steps per ring stage;
 //   warp 2      producer of the x ring (two producers, so that neither stream
 //               waits behind the other's ring);
 //   warps 3-18  dequantisers: each thread turns 16 codes of one B row into bf16
@@ -57,7 +60,8 @@ constexpr int kXBytes = BM * BK * 2;                      // 32 KB
 constexpr int kBBytes = BN * BK * 2;                      // 16 KB
 constexpr int kGroupsPerEntry = 8;                        // scale groups per ring entry (16 bytes)
 constexpr int kBarBytes = 512;
-constexpr int kChainSteps = 22;                          // K steps per accumulation chain, at most
+constexpr int kSub = 2;                                   // K steps (64 wide) per x/B ring stage
+constexpr int kChainStages = 11;                          // ring stages per accumulation chain, at most (22 K steps)
 constexpr int kPartFloats = 2 * UM * BN;                  // f32 partial accumulator of one split tile (128 KB)
 
 __device__ unsigned int g_prefill_error;
@@ -83,20 +87,26 @@ struct Cfg {
   static constexpr int kS0Bytes = kRows0 * 2 * kGroupsPerEntry;
   static constexpr int kS1Bytes = kRows1 * 2 * kGroupsPerEntry;
   static constexpr int kEntryBytes = 2 * kS0Bytes + 2 * kS1Bytes;
-  static constexpr int kSb = 4;   // B ring
-  static constexpr int kSx = 4;   // x ring (advances with the B ring: same depth)
+  // The x and B rings hold stages of kSub consecutive K steps (one barrier
+  // wait and one commit per stage for the MMA issuer); codes and scales keep
+  // rings of single K steps.
+  static constexpr int kSb = 2;   // B ring, stages
+  static constexpr int kSx = 2;   // x ring, stages (advances with the B ring: same depth)
+  static constexpr int kXStage = kSub * kXBytes;
+  static constexpr int kBStage = kSub * kBBytes;
   static constexpr int kBudget = kMaxSmem - 1024 - kBarBytes;
-  static constexpr int kFixed = kSx * kXBytes + kSb * kBBytes + 2 * kEntryBytes;
+  static constexpr int kFixed = kSx * kXStage + kSb * kBStage + 2 * kEntryBytes;
   static constexpr int kScFit = (kBudget - kFixed) / kCodesBytes;
-  static constexpr int kSc = kScFit > 4 ? 4 : kScFit;   // codes ring
+  static constexpr int kSc = kScFit > 4 ? 4 : kScFit;   // codes ring, K steps
   static constexpr int kXOff = 0;
-  static constexpr int kBOff = kXOff + kSx * kXBytes;
-  static constexpr int kCOff = kBOff + kSb * kBBytes;
+  static constexpr int kBOff = kXOff + kSx * kXStage;
+  static constexpr int kCOff = kBOff + kSb * kBStage;
   static constexpr int kSOff = kCOff + kSc * kCodesBytes;
   static constexpr int kBarOff = kSOff + 2 * kEntryBytes;
   static constexpr int kSmemBytes = kBarOff + kBarBytes + 1024;
   static_assert(kSc >= 2, "codes ring too small");
   static_assert(kSx == kSb, "the x and B rings share their barriers' slot index");
+  static_assert(kSc >= kSub, "the codes ring must hold a stage");
   static_assert(kCodesBytes % 1024 == 0 && kC0Bytes % 128 == 0, "codes ring alignment");
   static_assert(kEntryBytes % 128 == 0 && kS0Bytes % 128 == 0, "scale ring alignment");
   static_assert(kSmemBytes <= kMaxSmem, "shared memory budget");
@@ -303,20 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOff);
-  // The x and B rings advance together (slot k of both holds K step k mod 4):
-  // one dequantiser also waits for the x tile before its arrival on b_full, so
-  // the MMA issuer waits on b_full alone, and one commit to b_empty releases
-  // both slots (the x producer waits on it too).  Every barrier wait in the
-  // issuer's loop is shared-memory latency on the tensor core's critical path.
-  uint64_t *x_full = bars;              // x tile landed (TMA bytes)
-  uint64_t *b_full = x_full + Sx;       // B tile written by all dequantisers, x tile landed
+  // The x and B rings advance together (slot k of both holds stage k mod 2):
+  // one commit to b_empty releases both slots (the x producer waits on it
+  // too).  Every barrier wait in the issuer's loop is shared-memory latency on
+  // the tensor core's critical path, hence stages of two K steps.
+  uint64_t *x_full = bars;              // x tiles of a stage landed (TMA bytes)
+  uint64_t *b_full = x_full + Sx;       // B tiles of a stage written by all dequantisers
   uint64_t *b_empty = b_full + Sb;      // MMAs reading the x and B tiles completed
   uint64_t *c_full = b_empty + Sb;      // codes landed
   uint64_t *c_empty = c_full + Sc;      // codes consumed by all dequantisers
   uint64_t *s_full = c_empty + Sc;      // [op][2] scale entry landed
   uint64_t *s_empty = s_full + 4;       // [op][2] scale entry consumed
-  // Accumulation: each tile's K range is split into chains of at most
-  // kChainSteps K steps.  Chain 0 accumulates in TMEM buffer X, every later
+  // Accumulation: each segment's K range is split into chains of at most
+  // kChainStages ring stages.  Chain 0 accumulates in TMEM buffer X, every later
   // chain in buffer Y, and the epilogue adds Y into X with f32 adds after each
   // of them.  Short tensor-core accumulation chains keep the rounding of the
   // stored projections close to a correctly rounded sum.  X of tile t is
@@ -486,14 +495,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ls = 0; ls < S.n_seg && ok; ++ls) {
         const Seg sg = S.seg(ls, p);
         const int m0 = (sg.tile % p.m_tiles) * BM;
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+        for (int kb = sg.kb0; kb < sg.kb1; kb += kSub) {   // one stage: kSub K steps (fewer at the end)
           const int xs = n_x % Sx;
+          const int nsub = sg.kb1 - kb < kSub ? sg.kb1 - kb : kSub;
           if (!mbar_wait(&b_empty[xs], ((n_x / Sx) & 1) ^ 1u, abort_flag, p.timeout_ns, err)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&x_full[xs], kXBytes);
-          tma_load_2d(smem + C::kXOff + xs * kXBytes, &tm_x, &x_full[xs], kb * BK, m0);
+          mbar_arrive_expect_tx(&x_full[xs], nsub * kXBytes);
+          for (int j = 0; j < nsub; ++j)
+            tma_load_2d(smem + C::kXOff + xs * C::kXStage + j * kXBytes, &tm_x, &x_full[xs], (kb + j) * BK, m0);
           ++n_x;
         }
       }
@@ -512,22 +523,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdesc = umma_idesc_f16kind(UM, BN, A::kUmmaFormat);
       int n_x = 0, n_b = 0;
       bool ok = true;
-      // Chains of at most kChainSteps K steps (see the accumulation note at the
-      // barriers): chain 0 accumulates in X, chains 1.. in Y, and the epilogue
-      // adds Y into X after each of them.  Completions per segment: y_free and
-      // acc_full P each, xacc_free 1; y_base counts the y_free completions of
-      // the earlier segments.
+      // Chains of at most kChainStages ring stages (see the accumulation note at
+      // the barriers): chain 0 accumulates in X, chains 1.. in Y, and the
+      // epilogue adds Y into X after each of them.  Completions per segment:
+      // y_free and acc_full P each, xacc_free 1; y_base counts the y_free
+      // completions of the earlier segments.
       int y_base = 0;
       for (int ls = 0; ls < S.n_seg && ok; ++ls) {
         const Seg sg = S.seg(ls, p);
-        const int L = sg.kb1 - sg.kb0;
-        const int nc = (L + kChainSteps - 1) / kChainSteps;
-        const int clen = (L + nc - 1) / nc;   // K steps per chain (the last may be shorter)
+        const int nst = (sg.kb1 - sg.kb0 + kSub - 1) / kSub;   // ring stages of this segment
+        const int nc = (nst + kChainStages - 1) / kChainStages;
+        const int clen = (nst + nc - 1) / nc;   // stages per chain (the last may be shorter)
         const int P = nc > 1 ? nc - 1 : 1;
         const uint32_t x_tmem = tmem_base + static_cast<uint32_t>((ls & 1) * kAccCols);
         const uint32_t y_tmem = tmem_base + static_cast<uint32_t>(((ls + 1) & 1) * kAccCols);
-        int c = 0, cpos = 0;   // chain and K step within it
-        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+        int c = 0, cpos = 0;   // chain and stage within it
+        for (int st = 0; st < nst; ++st) {
+          const int kb = sg.kb0 + st * kSub;
+          const int nsub = sg.kb1 - kb < kSub ? sg.kb1 - kb : kSub;
           if (cpos == 0) {
             // X of this segment was Y of the previous one, and Y was its X:
             // chain 0 needs the previous segment's last X += Y done, chain 1
@@ -555,28 +568,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t d_tmem = c == 0 ? x_tmem : y_tmem;
           const bool chain_start = cpos == 0;
-          const int xs = n_x % Sx, bs = n_b % Sb;
-          // b_full also covers the x tile (see the barrier note)
-          if (!mbar_wait(&b_full[bs], (n_b / Sb) & 1, abort_flag, p.timeout_ns, err)) {
+          const int bs = n_b % Sb;
+          if (!mbar_wait(&x_full[bs], (n_b / Sb) & 1, abort_flag, p.timeout_ns, err) ||
+              !mbar_wait(&b_full[bs], (n_b / Sb) & 1, abort_flag, p.timeout_ns, err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // the x tile's two 128-row halves (16 KB apart) against the same B tile
-          const uint64_t adesc0 = umma_desc_sw128(smem_u32(smem + C::kXOff + xs * kXBytes));
-          const uint64_t adesc1 = umma_desc_sw128(smem_u32(smem + C::kXOff + xs * kXBytes + UM * 128));
-          const uint64_t bdesc = umma_desc_sw128(smem_u32(smem + C::kBOff + bs * kBBytes));
+          for (int j = 0; j < nsub; ++j) {
+            // K step j of the stage: the x tile's two 128-row halves (16 KB
+            // apart) against the same B tile
+            const uint32_t xa = smem_u32(smem + C::kXOff + bs * C::kXStage + j * kXBytes);
+            const uint64_t adesc0 = umma_desc_sw128(xa);
+            const uint64_t adesc1 = umma_desc_sw128(xa + UM * 128);
+            const uint64_t bdesc = umma_desc_sw128(smem_u32(smem + C::kBOff + bs * C::kBStage + j * kBBytes));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // +32 bytes of K per step inside the 128-byte swizzle atom
-            const uint32_t acc = (chain_start && kk == 0) ? 0u : 1u;
-            umma_bf16(d_tmem, adesc0 + 2 * kk, bdesc + 2 * kk, kIdesc, acc);
-            umma_bf16(d_tmem + BN, adesc1 + 2 * kk, bdesc + 2 * kk, kIdesc, acc);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // +32 bytes of K per step inside the 128-byte swizzle atom
+              const uint32_t acc = (chain_start && j == 0 && kk == 0) ? 0u : 1u;
+              umma_bf16(d_tmem, adesc0 + 2 * kk, bdesc + 2 * kk, kIdesc, acc);
+              umma_bf16(d_tmem + BN, adesc1 + 2 * kk, bdesc + 2 * kk, kIdesc, acc);
+            }
           }
           umma_commit(&b_empty[bs]);
           ++n_x;
           ++n_b;
-          if (++cpos == clen || kb + 1 == sg.kb1) {   // chain c complete
+          if (++cpos == clen || st + 1 == nst) {   // chain c complete
             if (c >= 1 || nc == 1) umma_commit(acc_full);
             ++c;
             cpos = 0;
@@ -613,43 +630,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int ls = 0; ls < S.n_seg && ok; ++ls) {
       const Seg sg = S.seg(ls, p);
       int epos = sg.kb0 % kpe;   // K step within the current scale entry
-      for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-        const int es = n_e & 1;
-        // a scale entry starts at an entry boundary or at the segment's first K step
-        if ((epos == 0 || kb == sg.kb0) &&
-            !(ok = warp_wait(&s_full[op * 2 + es], (n_e >> 1) & 1, abort_flag, p.timeout_ns, err)))
-          break;
-        const int cs = n_c % Sc, bs = n_b % Sb;
-        if (!(ok = warp_wait(&c_full[cs], (n_c / Sc) & 1, abort_flag, p.timeout_ns, err))) break;
-        // dequantiser 0 vouches for the x tile of this K step as well; the x
-        // tile lands long before the B slot frees up, so this wait hides in
-        // the next one
-        if (dw == 0 && !(ok = warp_wait(&x_full[bs], (n_b / Sb) & 1, abort_flag, p.timeout_ns, err))) break;
-        if (!(ok = warp_wait(&b_empty[bs], ((n_b / Sb) & 1) ^ 1u, abort_flag, p.timeout_ns, err))) break;
-        // scale and bias of this thread's 16 codes (one group: gs is a multiple of 32)
-        const uint32_t gi = gd(static_cast<uint32_t>(epos * BK + 16 * q));
-        const uint32_t eoff = static_cast<uint32_t>(es * C::kEntryBytes) + gi * 2;
-        const uint32_t s2 = splat_bf16(static_cast<uint16_t>(ld_shared_u16(sbase + s_row + eoff)));
-        const uint32_t b2 = splat_bf16(static_cast<uint16_t>(ld_shared_u16(sbase + b_row + eoff)));
-        const uint32_t caddr = sbase + c_row + static_cast<uint32_t>(cs * C::kCodesBytes);
-        const uint32_t baddr = sbase + static_cast<uint32_t>(C::kBOff + bs * kBBytes + row * 128);
-        if (op == 0)
-          dequant16<BITS0, A>(caddr, s2, b2, baddr, row, q);
-        else
-          dequant16<BITS1, A>(caddr, s2, b2, baddr, row, q);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&b_full[bs]);
-          mbar_arrive(&c_empty[cs]);
+      for (int kb = sg.kb0; kb < sg.kb1 && ok; kb += kSub) {   // one B stage
+        const int nsub = sg.kb1 - kb < kSub ? sg.kb1 - kb : kSub;
+        const int bs = n_b % Sb;
+        for (int j = 0; j < nsub; ++j) {
+          const int kbj = kb + j;
+          const int es = n_e & 1;
+          // a scale entry starts at an entry boundary or at the segment's first K step
+          if ((epos == 0 || kbj == sg.kb0) &&
+              !(ok = warp_wait(&s_full[op * 2 + es], (n_e >> 1) & 1, abort_flag, p.timeout_ns, err)))
+            break;
+          const int cs = n_c % Sc;
+          if (!(ok = warp_wait(&c_full[cs], (n_c / Sc) & 1, abort_flag, p.timeout_ns, err))) break;
+          if (j == 0 && !(ok = warp_wait(&b_empty[bs], ((n_b / Sb) & 1) ^ 1u, abort_flag, p.timeout_ns, err)))
+            break;
+          // scale and bias of this thread's 16 codes (one group: gs is a multiple of 32)
+          const uint32_t gi = gd(static_cast<uint32_t>(epos * BK + 16 * q));
+          const uint32_t eoff = static_cast<uint32_t>(es * C::kEntryBytes) + gi * 2;
+          const uint32_t s2 = splat_bf16(static_cast<uint16_t>(ld_shared_u16(sbase + s_row + eoff)));
+          const uint32_t b2 = splat_bf16(static_cast<uint16_t>(ld_shared_u16(sbase + b_row + eoff)));
+          const uint32_t caddr = sbase + c_row + static_cast<uint32_t>(cs * C::kCodesBytes);
+          const uint32_t baddr =
+              sbase + static_cast<uint32_t>(C::kBOff + bs * C::kBStage + j * kBBytes + row * 128);
+          if (op == 0)
+            dequant16<BITS0, A>(caddr, s2, b2, baddr, row, q);
+          else
+            dequant16<BITS1, A>(caddr, s2, b2, baddr, row, q);
+          // B stores visible to the tensor core, code reads done before the
+          // codes slot is refilled (both proxies)
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&c_empty[cs]);
+          ++n_c;
+          if (++epos == kpe || kbj + 1 == sg.kb1) {
+            if (lane == 0) mbar_arrive(&s_empty[op * 2 + es]);
+            ++n_e;
+            epos = 0;
+          }
         }
-        ++n_c;
+        if (!ok) break;
+        if (lane == 0) mbar_arrive(&b_full[bs]);
         ++n_b;
-        if (++epos == kpe || kb + 1 == sg.kb1) {
-          if (lane == 0) mbar_arrive(&s_empty[op * 2 + es]);
-          ++n_e;
-          epos = 0;
-        }
       }
     }
   } else {
@@ -663,8 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int ls = 0; ls < S.n_seg && ok; ++ls) {
       const Seg sg = S.seg(ls, p);
       const int t = sg.tile;
-      const int L = sg.kb1 - sg.kb0;
-      const int nc = (L + kChainSteps - 1) / kChainSteps;
+      const int nst = (sg.kb1 - sg.kb0 + kSub - 1) / kSub;   // ring stages of this segment
+      const int nc = (nst + kChainStages - 1) / kChainStages;
       const int P = nc > 1 ? nc - 1 : 1;   // acc_full completions of this segment
       const uint32_t tbase = lane_base + static_cast<uint32_t>((ls & 1) * kAccCols);          // X
       const uint32_t ybase = lane_base + static_cast<uint32_t>(((ls + 1) & 1) * kAccCols);    // Y
