@@ -102,6 +102,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
       : "memory");
 }
 
+// Bring [src, src + bytes) into L2; no data returns to the SM.  Both the
+// address and the size are multiples of 16 bytes.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -289,6 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     __syncthreads();
     if (!stager) issue_round(0);
     first_round = 1;
+    // Start x's way into L2 while that work finishes (a cold x would otherwise
+    // be read from HBM behind the weight stream, after the wait).  A prefetch
+    // changes no value: if that work is still writing x, its writes land in
+    // L2 all the same, and x is read only after the wait.
+    if (warp == 0 && lane < p.M) prefetch_l2_bulk(p.x + static_cast<int64_t>(lane) * p.K, static_cast<uint32_t>(p.K) * 2);
     griddep_wait();
     preload_x();
     if (stager) {
