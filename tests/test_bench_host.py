@@ -79,3 +79,17 @@ def test_peaks_fallback_or_measured():
     peaks, src = bench.load_peaks()
     assert src in ("measured", "fallback")
     assert peaks["hbm_gbs"] > 1000 and peaks["bf16_tflops"] > 100
+
+
+def test_peaks_per_key(tmp_path):
+    f = tmp_path / "peaks.json"
+    f.write_text('{"hbm_gbs": 7100.5, "bf16_tflops": {"value": 2010}}')
+    peaks, src = bench.load_peaks(str(f))
+    assert src == "measured"
+    assert peaks["hbm_gbs"] == 7100.5 and peaks["bf16_tflops"] == 2010.0
+    assert peaks["bf16_tflops_sustained"] == bench.FALLBACK_PEAKS["bf16_tflops_sustained"]
+    f.write_text('{"hbm_gbs": 7100.5}')
+    peaks, src = bench.load_peaks(str(f))
+    assert src == "fallback" and peaks["hbm_gbs"] == 7100.5
+    peaks, src = bench.load_peaks(str(tmp_path / "missing.json"))
+    assert src == "fallback" and peaks == bench.FALLBACK_PEAKS
