@@ -305,6 +305,13 @@ def bench_decode(args, dev, stream, peaks, peak_src):
             e2e_graphs[i % replicas].replay()
 
     e2e_ms = time_calls(e2e_step, args.steps, args.warmup, stream)
+
+    # the same loop with every call launched on its own (no early weight
+    # stream): each call waits for the previous one to finish before it
+    # requests any weight
+    ops.qsw_set_early_weight_stream(False)
+    iso_ms = time_graph(step, args.steps, args.warmup, stream)
+    ops.qsw_set_early_weight_stream(args.early_weights)
     world, rank, _ = dist_info()
     max_ms, total_bytes = reduce_timing(ms, wbytes * args.steps)
     e2e_max_ms, e2e_bytes = reduce_timing(e2e_ms, wbytes * args.steps)
@@ -318,7 +325,10 @@ def bench_decode(args, dev, stream, peaks, peak_src):
                   "traffic": read_traffic("gemv", "decode"), "peak_source": peak_src,
                   "kernel": "gemv_kernel (small-M, mma.sync reduction)",
                   "algorithmic_bytes_per_launch": algo_bytes},
-        l2_bytes=l2)
+        l2_bytes=l2,
+        isolated={"us_per_call": round(iso_ms * 1e3 / args.steps, 3),
+                  "weight_GBps": round(wbytes * args.steps / (iso_ms / 1e3) / 1e9, 1),
+                  "mode": "early weight stream off: each call starts after the previous one ends"})
 
 
 def bench_prefill(args, dev, stream, peaks, peak_src):
@@ -599,6 +609,7 @@ def run_ours(args):
                 "mode": "per step one CUDA-graph replay: pinned H2D copy of x, qswiglu_forward, "
                         "D2H copy of hidden to pinned memory; no host sync between steps",
                 "d2h_bytes_per_step": 2 * 8192},
+        "decode_isolated": d["isolated"],
         "gpu_launches": d["launches"] * world,
         "clocks": d["clocks"],
     }

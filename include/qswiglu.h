@@ -267,6 +267,15 @@ QSW_API int qsw_get_early_weight_stream(void);
 /* Per-wait limit for device-side waits, in nanoseconds (default 4e9). */
 QSW_API void qsw_set_wait_timeout_ns(uint64_t ns);
 
+/* Test hook, not for production use: the next call served by the small-M
+ * kernel never requests the first unit of each of its CTAs, so every wait on
+ * that unit's shared-memory slot runs out after the qsw_set_wait_timeout_ns
+ * limit.  The kernel then lets its other copies land and returns without
+ * writing its output, and the next qsw_check_device_errors() returns
+ * QSW_ERR_TIMEOUT.  Later calls are unaffected.  Nothing traps and nothing
+ * waits without a limit. */
+QSW_API void qsw_debug_withhold_next_fill(void);
+
 /* Dispatch counters (process-wide, monotonically increasing). `out` receives
  * min(n, QSW_NUM_COUNTERS) values. */
 QSW_API void qsw_get_counters(uint64_t *out, int n);

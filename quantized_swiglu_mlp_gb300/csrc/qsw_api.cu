@@ -272,6 +272,8 @@ int qsw_get_gemv_max_m(void) { return gemv_max_m(); }
 
 void qsw_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
 
+void qsw_debug_withhold_next_fill(void) { qsw::gemv_withhold_next(); }
+
 void qsw_set_early_weight_stream(int on) { g_early_weights.store(on ? 1 : 0); }
 
 int qsw_get_early_weight_stream(void) { return g_early_weights.load(); }
@@ -296,6 +298,6 @@ const char *qsw_status_string(qsw_status s) {
   }
 }
 
-int qsw_version(void) { return 103; }
+int qsw_version(void) { return 104; }
 
 }  // extern "C"

@@ -38,8 +38,8 @@
 // own copies land and returns, and the host reads the device error word.
 #include <atomic>
 
-#include "qsw_device.cuh"
 #include "qsw_internal.h"
+#include "qsw_smallm.cuh"
 
 namespace qsw {
 namespace {
@@ -48,8 +48,8 @@ constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kWideGroup = 4;                   // warps sharing one unit (default)
 constexpr int kNarrowGroup = 2;                 // ... when every unit of a CTA fits in its slots at once
-constexpr int kBlockK = 128;                    // codes per K block
-constexpr int kChunk = 32;                      // codes per lane per block
+constexpr int kBlockK = kSmallBlockK;           // codes per K block
+constexpr int kChunk = kSmallChunk;             // codes per lane per block
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kMaxSlots = 16;
 constexpr int kXBlockBytes = 4 * 32 * 16;       // B fragments of one block, one full x row group (2 KB)
@@ -76,88 +76,8 @@ struct GemvParams {
   int red_off;            // byte offset of the partial sums
   int bar_off;            // byte offset of the barriers
   int early;              // launched as a programmatic dependent (early weight stream)
+  int withhold;           // test only: the first fill of slot 0 is never issued (1) or as usual (0)
   uint64_t timeout_ns;
-};
-
-// D += A . B, m16n8k16, f32 accumulators, A and B in the activation dtype.
-template <class A>
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  if constexpr (A::kId == ActF16::kId) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-}
-
-__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Bring [src, src + bytes) into L2; no data returns to the SM.  Both the
-// address and the size are multiples of 16 bytes.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint2 lds64(uint32_t addr) {
-  uint2 v;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
-  return v;
-}
-
-// 32 codes of one row (the lane's chunk of a 128-code block), from shared memory.
-template <int BITS, class A>
-struct Chunk {
-  static constexpr int kWords = kChunk * BITS / 32;   // 4, 8 or 2
-  uint32_t w[kWords];
-  __device__ __forceinline__ void load(uint32_t addr) {
-    if constexpr (BITS == 2) {
-      const uint2 v = lds64(addr);
-      w[0] = v.x;
-      w[1] = v.y;
-    } else {
-#pragma unroll
-      for (int i = 0; i < kWords / 4; ++i) {
-        const uint4 v = lds128(addr + 16 * i);
-        w[4 * i + 0] = v.x;
-        w[4 * i + 1] = v.y;
-        w[4 * i + 2] = v.z;
-        w[4 * i + 3] = v.w;
-      }
-    }
-  }
-  // eight codes (sub-chunk j), interleaved pairing (codes p, p+4 in word p)
-  __device__ __forceinline__ void dequant(int j, uint32_t s2, uint32_t b2, uint32_t (&o)[4]) const {
-    if constexpr (BITS == 4) {
-      Dequant8<4, A>::interleaved(w[j], s2, b2, o);
-    } else if constexpr (BITS == 8) {
-      Dequant8<8, A>::interleaved(w[2 * j], w[2 * j + 1], s2, b2, o);
-    } else {
-      Dequant8<2, A>::interleaved(w[j >> 1] >> (16 * (j & 1)), s2, b2, o);
-    }
-  }
 };
 
 // Issue the bulk copies of unit u into a slot (lanes 0..5 of the calling warp).
@@ -260,11 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     uint8_t *dst = smem + p.x_off + static_cast<size_t>(kb * NG + G) * 4 * x_piece + L * 16;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {   // x values 8j..8j+7: (x0,x1) (x2,x3) (x4,x5) (x6,x7)
-      const uint4 f = make_uint4(prmt(xv[j].x, xv[j].z, 0x5410u),    // h=0: (x0, x4)
-                                 prmt(xv[j].x, xv[j].z, 0x7632u),    //      (x1, x5)
-                                 prmt(xv[j].y, xv[j].w, 0x5410u),    // h=1: (x2, x6)
-                                 prmt(xv[j].y, xv[j].w, 0x7632u));   //      (x3, x7)
-      *reinterpret_cast<uint4 *>(dst + j * x_piece) = f;
+      *reinterpret_cast<uint4 *>(dst + j * x_piece) = x_fragment(xv[j]);
     }
   };
   constexpr int kStageThreads = kThreads - 32;
@@ -278,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
   auto issue_round = [&](int s) {
     for (int q = 0; q < kGroups; ++q) {
       const int i = q + s * kGroups;
-      if (i < my_units)
+      // (the test hook leaves slot 0 without its first fill: waits on it run out)
+      if (i < my_units && !(p.withhold && i == 0))
         issue_unit<BITS0, BB, DUAL>(p, smem + (q * spg + s) * p.slot_bytes, &full[q * spg + s],
                                     &issued_cnt[q * spg + s], unit_of(i), lane);
     }
@@ -610,7 +527,11 @@ cudaError_t launch_act(const GemvParams &p, const Layout &l, int bits0, int bits
   }
 }
 
+std::atomic<int> g_withhold{0};
+
 }  // namespace
+
+void gemv_withhold_next() { g_withhold.store(1); }
 
 bool gemv_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const QuantOperand *op1, int num_sms) {
   const bool dual = op1 != nullptr;
@@ -658,6 +579,7 @@ cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const Qu
   p.res = op1 ? nullptr : static_cast<const uint16_t *>(residual);
   p.timeout_ns = timeout_ns;
   p.early = early_weights ? 1 : 0;
+  p.withhold = g_withhold.exchange(0);
   if (act == ActF16::kId) return launch_act<ActF16>(p, l, op0.bits, o1.bits, op1 != nullptr, stream, num_sms);
   if (act == ActBf16::kId) return launch_act<ActBf16>(p, l, op0.bits, o1.bits, op1 != nullptr, stream, num_sms);
   return cudaErrorInvalidValue;

@@ -34,6 +34,10 @@ cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const Qu
                         const QuantOperand *op1, int variant, int act, void *out, const void *residual,
                         cudaStream_t stream, uint64_t timeout_ns, int num_sms, bool early_weights);
 
+// Test hook: the next small-M launch never fills its CTAs' first slot, so
+// that the waits on it run out.
+void gemv_withhold_next();
+
 // Whether the small-M kernel can stage rows of length K (else the tensor-core
 // kernel serves every M).
 bool gemv_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const QuantOperand *op1, int num_sms);

@@ -36,7 +36,7 @@ EXPORTED = ("qswiglu_forward", "affine_qmm", "qswiglu_forward_ws", "affine_qmm_w
             "qswiglu_forward_ex", "affine_qmm_ex", "qsw_silu_mul_ex", "qsw_mlp_forward_ex", "qsw_workspace_bytes",
             "qsw_set_stream_k", "qsw_get_stream_k", "qsw_silu_mul", "qsw_check_device_errors",
             "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_early_weight_stream",
-            "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns",
+            "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns", "qsw_debug_withhold_next_fill",
             "qsw_get_counters", "qsw_reset_counters", "qsw_status_string", "qsw_version")
 
 _lock = threading.Lock()
@@ -374,6 +374,12 @@ def qsw_get_gemv_max_m() -> int:
 
 def qsw_set_wait_timeout_ns(ns: int) -> None:
     load_library().qsw_set_wait_timeout_ns(int(ns))
+
+
+def qsw_debug_withhold_next_fill() -> None:
+    """Test hook: the next small-M call leaves its first units unrequested, so
+    its waits run out (see include/qswiglu.h)."""
+    load_library().qsw_debug_withhold_next_fill()
 
 
 def qsw_get_counters() -> list[int]:

@@ -142,6 +142,73 @@ def test_small_m_kernel(dev, gemv_limit, shape, variant):
     assert ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] > before
 
 
+# More small-M shapes: many slot refills per CTA, odd M, 2- and 8-bit
+# operands, K blocks fewer than warps, the mixed-spec workload's specs.
+MORE_SMALL_M_SHAPES = [
+    (1, 2048, 30000, 4, 64, 4, 64),    # 30000 rows: each CTA's slots are refilled many times
+    (7, 1024, 1203, 4, 64, 8, 32),     # M odd, ragged last unit
+    (2, 4096, 3000, 2, 64, 4, 128),    # 2-bit gate, 32 K blocks per unit
+    (5, 256, 17, 8, 32, 8, 32),        # 3 units, 2 K blocks: most warps idle
+    (3, 2560, 10240, 4, 64, 8, 32),    # the mixed-spec workload's specs
+]
+
+
+@pytest.mark.parametrize("shape", MORE_SMALL_M_SHAPES, ids=_ids(MORE_SMALL_M_SHAPES))
+@pytest.mark.parametrize("variant", [ops.MATCH, ops.F32], ids=["match", "f32"])
+def test_small_m_kernel_more_shapes(dev, gemv_limit, shape, variant):
+    M, H, I, bg, gg, bu, gu = shape
+    case = inputs.make_case(M, H, I, bits_g=bg, gs_g=gg, bits_u=bu, gs_u=gu, seed=M * 13 + I)
+    gemv_limit(16)
+    before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
+    check_fused(case, dev, variant, rows=list(range(M)))
+    assert ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] > before
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 2048, 1000), (3, 1024, 203), (8, 512, 40), (2, 8192, 2048)])
+@pytest.mark.parametrize("with_residual", [False, True], ids=["plain", "residual"])
+def test_small_m_single_operand(dev, gemv_limit, M, K, N, with_residual):
+    """affine_qmm on the small-M kernel (ragged units), with and without a
+    residual."""
+    case = inputs.make_case(M, K, N, bits_g=4, gs_g=64, seed=M + K + N)
+    gemv_limit(16)
+    x, w, s, b, gs, bits = device_args(case, dev)[:6]
+    h = inputs.make_x(M, N, seed=K) if with_residual else None
+    before = ops.qsw_get_counters()[ops.CNT_QMM_GEMV]
+    y = ops.affine_qmm(x, w, s, b, gs, bits, residual=None if h is None else inputs.bits_to_device(h, dev))
+    got = to_bits(y)
+    ops.qsw_check_device_errors()
+    assert ops.qsw_get_counters()[ops.CNT_QMM_GEMV] == before + 1
+    want = oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gs, bits, residual=h)
+    ok, info = check_projection(got, want)
+    assert ok, info
+
+
+@pytest.mark.parametrize("early", [False, True], ids=["plain", "early_weights"])
+def test_small_m_wait_runs_out(dev, gemv_limit, early_weights, early):
+    """A fill that never comes: with the test hook, the next small-M call never
+    requests its CTAs' first units.  Every wait on them gives up after the
+    (short) limit, the kernel returns without trapping, the error word reports
+    QSW_ERR_TIMEOUT, and the next call on the same stream is correct again."""
+    case = inputs.workload_case("decode")
+    gemv_limit(16)
+    early_weights(early)
+    a = device_args(case, dev)
+    want = oracle.qswiglu(*case.oracle_args(), variant=ops.MATCH)
+    ops.qsw_set_wait_timeout_ns(20_000_000)
+    try:
+        ops.qsw_debug_withhold_next_fill()
+        ops.qswiglu_forward(*a, variant=ops.MATCH)
+        with pytest.raises(ops.QswError) as e:
+            ops.qsw_check_device_errors()
+        assert e.value.code == 4   # QSW_ERR_TIMEOUT
+        got = to_bits(ops.qswiglu_forward(*a, variant=ops.MATCH))
+        ops.qsw_check_device_errors()
+    finally:
+        ops.qsw_set_wait_timeout_ns(4_000_000_000)
+    ok, info = check_match(got, want)
+    assert ok, info
+
+
 @pytest.mark.parametrize("shape", [(2, 96, 40, 4, 32, 4, 32), (3, 2080, 64, 4, 32, 8, 32)],
                          ids=["groups_per_row_12", "k_tail"])
 def test_small_m_routes_unstageable_shapes(dev, gemv_limit, shape):
@@ -317,6 +384,26 @@ def _sampled(case, dev, variant, rows, limit, gemv_limit):
 def test_full_decode(dev, gemv_limit, variant):
     case = inputs.workload_case("decode")
     _sampled(case, dev, variant, [0], 16, gemv_limit)
+
+
+def test_decode_projection_rate(dev, gemv_limit):
+    """The exact-projection rate at the decode workload, in the benchmark's
+    launch configuration: every output of three x seeds (24,576 elements per
+    projection), so the 99.9 % bar is enforced, not only reported."""
+    gemv_limit(16)
+    got = {ops.DEBUG_GATE: [], ops.DEBUG_UP: []}
+    want = {ops.DEBUG_GATE: [], ops.DEBUG_UP: []}
+    for seed in (0, 1, 2):
+        case = inputs.workload_case("decode", seed=seed)
+        a = device_args(case, dev)
+        _, g64, u64 = oracle.qswiglu(*case.oracle_args(), variant=ops.MATCH, return_acc=True)
+        for v, ref in ((ops.DEBUG_GATE, g64), (ops.DEBUG_UP, u64)):
+            got[v].append(run_fused(case, dev, v, a))
+            want[v].append(oracle.bf16_round_array(ref))
+    for v in (ops.DEBUG_GATE, ops.DEBUG_UP):
+        g, w = np.concatenate(got[v], axis=None), np.concatenate(want[v], axis=None)
+        ok, info = check_projection(g, w)
+        assert ok and g.size >= 20_000, info
 
 
 def test_full_tiny_prefill(dev, gemv_limit):
