@@ -12,6 +12,7 @@ import torch
 
 import oracle
 from quantized_swiglu_mlp_gb300 import inputs, ops
+from tests.exact_sums import projection_context
 from tests.gpu_util import device_args, to_bits
 from tests.tolerances import TO_F64, check_f32, check_match, check_match_with_projections, check_projection
 
@@ -59,9 +60,13 @@ def match_epilogue(g, u, dtype="bf16"):
 
 def check_fused(case, dev, variant, rows=None, pairs=None):
     """Run `variant` on the GPU and compare with the oracle on all rows, the
-    listed rows, or the listed (m, i) pairs.  Returns the GPU result."""
+    listed rows, or the listed (m, i) pairs.  Returns the GPU result.  MATCH
+    is checked with the stored projections, the exact f64 sums and the
+    accumulation bound of the kernel that ran."""
     a = device_args(case, dev)
+    before = ops.qsw_get_counters()[ops.CNT_FUSED_TC]
     got = run_fused(case, dev, variant, a)
+    kernel = "tensor_core" if ops.qsw_get_counters()[ops.CNT_FUSED_TC] > before else "small_m"
     if rows is not None:
         sel = (np.asarray(rows),)
     elif pairs is not None:
@@ -73,17 +78,21 @@ def check_fused(case, dev, variant, rows=None, pairs=None):
         want = {v: oracle.qswiglu_pairs(*case.oracle_args(), v, pairs, dtype=dt)
                 for v in (variant, ops.DEBUG_GATE, ops.DEBUG_UP)}
         h_ref, g_ref, u_ref = want[variant], want[ops.DEBUG_GATE], want[ops.DEBUG_UP]
+        if variant == ops.MATCH:
+            g64, u64, bnd_g, bnd_u = projection_context(case, kernel, pairs=pairs)
     elif variant == ops.MATCH:
         h_ref, g64, u64 = oracle.qswiglu(*case.oracle_args(), variant=variant, rows=rows, return_acc=True,
                                          dtype=dt)
         g_ref, u_ref = oracle.round_array(g64, dt), oracle.round_array(u64, dt)
+        _, _, bnd_g, bnd_u = projection_context(case, kernel, rows=rows)
     else:
         h_ref = oracle.qswiglu(*case.oracle_args(), variant=variant, rows=rows, dtype=dt)
     if variant == ops.MATCH:
         g_gpu = run_fused(case, dev, ops.DEBUG_GATE, a)[sel]
         u_gpu = run_fused(case, dev, ops.DEBUG_UP, a)[sel]
         ok, info = check_match_with_projections(got[sel], g_gpu, u_gpu, h_ref, g_ref, u_ref,
-                                                lambda g, u: match_epilogue(g, u, dt), dt)
+                                                lambda g, u: match_epilogue(g, u, dt), dt,
+                                                exact=(g64, u64), bounds=(bnd_g, bnd_u))
         assert ok, info
     else:
         check(variant, got[sel], h_ref, dt)
@@ -240,9 +249,12 @@ def test_small_m_projection_rate(dev, gemv_limit, M):
 
 @pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
 def test_fused_match_equals_unfused(dev, gemv_limit, limit):
-    """MATCH is the unfused composition op for op: on the tensor-core kernel
-    (same K order, gate/up differ only in their N position) the fused and
-    unfused GPU paths agree bit for bit."""
+    """MATCH is the unfused composition op for op, and both kernels compute it
+    bit for bit: each kernel folds every K block into the f32 accumulator the
+    same way in its fused and single-operand forms (same K split; an MMA's
+    result for one A row does not depend on the other rows -- measured: the
+    fused gate/up projections equal affine_qmm's bit for bit), and the MATCH
+    epilogue rounds at the same points as the elementwise kernel."""
     case = inputs.make_case(24, 1024, 264, bits_g=4, gs_g=64, bits_u=8, gs_u=32, seed=3)
     gemv_limit(limit)
     a = device_args(case, dev)
@@ -250,17 +262,14 @@ def test_fused_match_equals_unfused(dev, gemv_limit, limit):
     # under stream-K scheduling, which changes the f32 summation order
     fused = to_bits(ops.qswiglu_forward(*a, variant=ops.MATCH, workspace=None))
     unfused = to_bits(ops.unfused_swiglu(*a, variant=ops.MATCH, workspace=None))
+    x, wg, sg, bg, gsg, btg, wu, su, bu, gsu, btu = a
+    pg = to_bits(ops.qswiglu_forward(*a, variant=ops.DEBUG_GATE, workspace=None))
+    pu = to_bits(ops.qswiglu_forward(*a, variant=ops.DEBUG_UP, workspace=None))
+    sg_ = to_bits(ops.affine_qmm(x, wg, sg, bg, gsg, btg, workspace=None))
+    su_ = to_bits(ops.affine_qmm(x, wu, su, bu, gsu, btu, workspace=None))
     ops.qsw_check_device_errors()
-    if limit == 0:
-        assert np.array_equal(fused, unfused)
-    else:
-        # The small-M kernel feeds gate/up rows to the lower/upper half of the
-        # mma.sync A operand while the single-operand form uses both halves for
-        # one matrix; the legacy MMA's rounding can differ between halves, so
-        # a few projections round the other way: same MATCH bound, >= 99 % equal.
-        ok, info = check_match(fused, unfused)
-        assert ok, info
-        assert (fused == unfused).mean() >= 0.99
+    assert np.array_equal(pg, sg_) and np.array_equal(pu, su_)
+    assert np.array_equal(fused, unfused)
 
 
 @pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
@@ -584,9 +593,11 @@ def test_stream_k_graph_replays(dev, gemv_limit, stream_k):
         assert _epoch(ws) == e0 + len(outs)
         step = inputs.Case(x=xb, gate=base.gate, up=base.up)
         h_ref, g64, u64 = oracle.qswiglu(*step.oracle_args(), variant=oracle.MATCH, return_acc=True)
+        _, _, bnd_g, bnd_u = projection_context(step, "tensor_core")
         ok, info = check_match_with_projections(
             to_bits(outs[ops.MATCH]), to_bits(outs[ops.DEBUG_GATE]), to_bits(outs[ops.DEBUG_UP]), h_ref,
-            oracle.bf16_round_array(g64), oracle.bf16_round_array(u64), match_epilogue)
+            oracle.bf16_round_array(g64), oracle.bf16_round_array(u64), match_epilogue,
+            exact=(g64, u64), bounds=(bnd_g, bnd_u))
         assert ok, info
 
 

@@ -10,6 +10,7 @@ import torch
 
 import oracle
 from quantized_swiglu_mlp_gb300 import inputs, ops
+from tests.exact_sums import projection_context
 from tests.gpu_util import device_args, to_bits
 from tests.tolerances import check_f32, check_match_with_projections
 
@@ -35,10 +36,12 @@ def forced_split():
 
 def _match_ok(case, outs):
     h_ref, g64, u64 = oracle.qswiglu(*case.oracle_args(), variant=oracle.MATCH, return_acc=True)
+    _, _, bnd_g, bnd_u = projection_context(case, "tensor_core")
     return check_match_with_projections(
         to_bits(outs[ops.MATCH]), to_bits(outs[ops.DEBUG_GATE]), to_bits(outs[ops.DEBUG_UP]), h_ref,
         oracle.bf16_round_array(g64), oracle.bf16_round_array(u64),
-        lambda g, u: oracle.silu_mul(np.ascontiguousarray(g), np.ascontiguousarray(u), oracle.MATCH))
+        lambda g, u: oracle.silu_mul(np.ascontiguousarray(g), np.ascontiguousarray(u), oracle.MATCH),
+        exact=(g64, u64), bounds=(bnd_g, bnd_u))
 
 
 @pytest.mark.parametrize("shape", [(300, 512, 1536, 4, 64, 4, 64), (257, 2080, 384, 4, 32, 8, 32)],
