@@ -37,6 +37,9 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# M values of the mixed-spec sweep: the workload's own (1, 2, 3, 4, 8, 64, 2048)
+# and more around the small-M / tensor-core cut-over
+SWEEP_M = (1, 2, 3, 4, 8, 16, 24, 32, 48, 64, 128, 256, 2048)
 
 
 # ------------------------------------------------------------ helpers -------
@@ -312,6 +315,12 @@ def bench_decode(args, dev, stream, peaks, peak_src):
     ops.qsw_set_early_weight_stream(False)
     iso_ms = time_graph(step, args.steps, args.warmup, stream)
     ops.qsw_set_early_weight_stream(args.early_weights)
+
+    # the other variant of the same loop (F32 when the headline is MATCH)
+    other = "f32" if args.variant == "match" else "match"
+    ov = ops.VARIANTS[other]
+    other_ms = time_graph(lambda i: ops.qswiglu_forward(x, *reps[i % replicas], variant=ov, out=out, stream=stream),
+                          args.steps, args.warmup, stream)
     world, rank, _ = dist_info()
     max_ms, total_bytes = reduce_timing(ms, wbytes * args.steps)
     e2e_max_ms, e2e_bytes = reduce_timing(e2e_ms, wbytes * args.steps)
@@ -328,7 +337,9 @@ def bench_decode(args, dev, stream, peaks, peak_src):
         l2_bytes=l2,
         isolated={"us_per_call": round(iso_ms * 1e3 / args.steps, 3),
                   "weight_GBps": round(wbytes * args.steps / (iso_ms / 1e3) / 1e9, 1),
-                  "mode": "early weight stream off: each call starts after the previous one ends"})
+                  "mode": "early weight stream off: each call starts after the previous one ends"},
+        other_variant={"variant": other, "us_per_call": round(other_ms * 1e3 / args.steps, 3),
+                       "weight_GBps": round(wbytes * args.steps / (other_ms / 1e3) / 1e9, 1)})
 
 
 def bench_prefill(args, dev, stream, peaks, peak_src):
@@ -340,6 +351,8 @@ def bench_prefill(args, dev, stream, peaks, peak_src):
     res = {"stream_k": args.stream_k}
     if args.only in ("all", "large"):
         res.update(_bench_large(args, dev, stream, peaks, peak_src))
+    if args.only in ("all", "tiny"):
+        res.update(_bench_tiny(args, dev, stream))
     if args.only in ("all", "mid"):
         res.update(_bench_mid(args, dev, stream))
     if args.only in ("all", "sweep"):
@@ -461,6 +474,45 @@ def _bench_large(args, dev, stream, peaks, peak_src):
     return res
 
 
+def _bench_tiny(args, dev, stream):
+    """The tiny prefill (a 6-token prompt: M=6, H=512, I=1536, MATCH): the fused
+    call on the small-M kernel (its default route) and on the tensor-core
+    kernel, and the unfused path (2x affine_qmm + silu*mul), in us per call.
+    The weights (0.9 MB) stay in L2, as they would between layers of a real
+    prompt's first pass only if nothing else ran; the figure is latency."""
+    import torch
+    from quantized_swiglu_mlp_gb300 import inputs, ops
+
+    case = inputs.workload_case("tiny_prefill")
+    a = to_device(case, dev)
+    out = torch.empty((case.M, case.I), dtype=torch.bfloat16, device=dev)
+    g = torch.empty_like(out)
+    u = torch.empty_like(out)
+    x, wg, sg, bg, gsg, btg, wu, su, bu, gsu, btu = a
+    saved = ops.qsw_get_gemv_max_m()
+    res = {}
+    steps = 200
+    try:
+        for name, limit in (("tiny_fused_small_m", 16), ("tiny_fused_tensor_core", 0)):
+            ops.qsw_set_gemv_max_m(limit)
+            ms = time_graph(lambda i: ops.qswiglu_forward(*a, variant=ops.MATCH, out=out, stream=stream), steps, 3,
+                            stream)
+            res[name] = {"us_per_call": round(ms * 1e3 / steps, 2)}
+        ops.qsw_set_gemv_max_m(saved)
+
+        def unfused(i):
+            ops.affine_qmm(x, wg, sg, bg, gsg, btg, y=g, stream=stream)
+            ops.affine_qmm(x, wu, su, bu, gsu, btu, y=u, stream=stream)
+            ops.qsw_silu_mul(g, u, ops.MATCH, out=out, stream=stream)
+
+        ms = time_graph(unfused, steps, 3, stream)
+        res["tiny_unfused"] = {"us_per_call": round(ms * 1e3 / steps, 2)}
+    finally:
+        ops.qsw_set_gemv_max_m(saved)
+    ops.qsw_check_device_errors(stream)
+    return res
+
+
 def _bench_mid(args, dev, stream):
     import torch
     from quantized_swiglu_mlp_gb300 import inputs, ops
@@ -506,11 +558,11 @@ def _bench_mixed_sweep(args, dev, stream):
     rows = []
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     try:
-        for M in inputs.MIXED_M_SWEEP:
+        for M in SWEEP_M:
             case = inputs.workload_case("mixed", M=M)
             base = to_device(case, dev)
             wbytes = weight_bytes(case)
-            reps = max(1, int(np.ceil(3.2 * l2 / wbytes))) if M <= 64 else 1
+            reps = max(1, int(np.ceil(3.2 * l2 / wbytes))) if M <= 256 else 1
             sets = [base[1:]] + [tuple(t.clone() if isinstance(t, torch.Tensor) else t for t in base[1:])
                                  for _ in range(reps - 1)]
             out = torch.empty((M, case.I), dtype=torch.bfloat16, device=dev)
@@ -519,13 +571,17 @@ def _bench_mixed_sweep(args, dev, stream):
                 if name == "small_m" and M > 32:
                     continue
                 ops.qsw_set_gemv_max_m(limit)
-                steps = 200 if M <= 64 else 10
+                steps = 200 if M <= 256 else 10
+                before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
                 ms = time_graph(lambda i: ops.qswiglu_forward(base[0], *sets[i % len(sets)], variant=ops.MATCH,
                                                               out=out, stream=stream), steps, 3, stream)
+                if name == "small_m" and ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] == before:
+                    entry["small_m"] = "does not fit this shape's rows in shared memory (tensor-core kernel ran)"
+                    continue
                 us = ms * 1e3 / steps
                 entry[name] = {"us": round(us, 2), "weight_GBps": round(wbytes / us / 1e3, 1),
                                "tflops": round(4.0 * M * case.H * case.I / us / 1e6, 1)}
-            if "small_m" in entry:
+            if isinstance(entry.get("small_m"), dict):
                 entry["faster"] = "small_m" if entry["small_m"]["us"] < entry["tensor_core"]["us"] else "tensor_core"
             rows.append(entry)
             del base, sets, out
@@ -536,6 +592,50 @@ def _bench_mixed_sweep(args, dev, stream):
     small = [r["M"] for r in rows if r.get("faster") == "small_m"]
     return {"mixed_sweep": rows, "mixed_small_m_faster_up_to": max(small) if small else 0,
             "default_small_m_limit": saved}
+
+
+def _time_oracle(case, rows, threads):
+    """Seconds for the oracle (as it stands) to compute `rows` of x of `case`
+    (MATCH) with `threads` OpenMP threads."""
+    import oracle
+    saved = oracle.num_threads()
+    oracle.set_num_threads(threads)
+    try:
+        t0 = time.perf_counter()
+        oracle.qswiglu(*case.oracle_args(), variant=oracle.MATCH, rows=rows)
+        return time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(saved)
+
+
+def cpu_baseline_configs(full: bool):
+    """The oracle on every workload, single-threaded and on all host cores, on
+    the stated sample of rows of x (all I outputs of each row): by default a
+    few seconds in all; with `full`, the tiny, mid and mixed workloads whole
+    and 256 rows of the large one.  Rates use the workload's own metric (4*H*I
+    FLOP per row; weight bytes for the decode call)."""
+    import oracle
+    from quantized_swiglu_mlp_gb300 import inputs
+    cores = os.cpu_count() or 1
+    plan = [("tiny_prefill", None, None), ("decode", None, None),
+            ("mid_prefill", None if full else 16, None), ("large_prefill", 256 if full else 4, None),
+            ("mixed", None if full else 8, 2048)]
+    out = {}
+    for name, n_rows, m in plan:
+        case = inputs.workload_case(name, M=m) if m else inputs.workload_case(name)
+        rows = None if n_rows is None else [int(r) for r in np.linspace(0, case.M - 1, n_rows)]
+        n = case.M if rows is None else len(rows)
+        entry = {"rows": f"{n} of {case.M}", "M": case.M, "H": case.H, "I": case.I}
+        for label, threads in (("single_thread", 1), ("all_cores", cores)):
+            sec = _time_oracle(case, rows, threads)
+            if name == "decode":
+                entry[label] = {"s": round(sec, 4), "GBps": round(weight_bytes(case) / sec / 1e9, 4)}
+            else:
+                entry[label] = {"s": round(sec, 4), "GFLOPs": round(4.0 * n * case.H * case.I / sec / 1e9, 3)}
+        entry["cores"] = cores
+        entry["note"] = "each oracle call dequantises both whole weight matrices first (f64), so small row samples are dominated by it"
+        out[name if m is None else f"{name}_M{m}"] = entry
+    return out
 
 
 def cpu_baseline_decode(budget_s: float):
@@ -610,6 +710,7 @@ def run_ours(args):
                         "D2H copy of hidden to pinned memory; no host sync between steps",
                 "d2h_bytes_per_step": 2 * 8192},
         "decode_isolated": d["isolated"],
+        "decode_other_variant": d["other_variant"],
         "gpu_launches": d["launches"] * world,
         "clocks": d["clocks"],
     }
@@ -619,6 +720,7 @@ def run_ours(args):
         v, cores, sample = cpu_baseline_decode(args.cpu_budget)
         line["cpu_baseline"] = {"value": round(v, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
                                 "sample": sample}
+        line["cpu_baseline_configs"] = cpu_baseline_configs(args.oracle_full)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -703,7 +805,10 @@ def main(argv=None):
                     help="stream-K scheduling of the tensor-core kernel (library switch)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--only", choices=["all", "decode", "large", "mid", "sweep", "f16", "mlp"], default="all",
+    ap.add_argument("--oracle-full", action="store_true",
+                    help="time the oracle on the tiny, mid and mixed workloads whole and 256 large-prefill rows "
+                         "(minutes) instead of the default few-second samples")
+    ap.add_argument("--only", choices=["all", "decode", "tiny", "large", "mid", "sweep", "f16", "mlp"], default="all",
                     help="run one workload only (profiling); the JSON line then carries what ran")
     ap.add_argument("--soak-seconds", type=float, default=1.0,
                     help="untimed load before the timed region, so the clock sampler sees it")

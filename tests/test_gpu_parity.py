@@ -443,6 +443,18 @@ def test_full_mixed_sweep(dev, gemv_limit, M):
         check_fused(case, dev, ops.MATCH, rows=rows)
 
 
+@pytest.mark.parametrize("M", [16, 24, 32, 48, 128, 256])
+def test_mixed_sweep_more_m(dev, gemv_limit, M):
+    """The mixed-spec workload at the M values the benchmark adds around the
+    small-M / tensor-core cut-over: both kernels where both apply (M <= 32)."""
+    case = inputs.workload_case("mixed", M=M)
+    rows = [0, M // 2, M - 1]
+    _sampled(case, dev, ops.MATCH, rows, 32 if M <= 32 else 16, gemv_limit)
+    if M <= 32:
+        gemv_limit(0)
+        check_fused(case, dev, ops.MATCH, rows=rows)
+
+
 @pytest.fixture
 def early_weights():
     saved = ops.qsw_get_early_weight_stream()
