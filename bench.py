@@ -590,8 +590,36 @@ def _bench_mixed_sweep(args, dev, stream):
         ops.qsw_set_gemv_max_m(saved)
     ops.qsw_check_device_errors(stream)
     small = [r["M"] for r in rows if r.get("faster") == "small_m"]
+    # the same comparison on the decode workload's shapes (H=2048, I=8192,
+    # 4-bit gs 64), where the small-M kernel fits up to M = 32
+    cut = []
+    try:
+        for M in (1, 8, 16, 24, 32):
+            case = inputs.workload_case("decode", M=M)
+            base = to_device(case, dev)
+            wbytes = weight_bytes(case)
+            reps = max(1, int(np.ceil(3.2 * l2 / wbytes)))
+            sets = [base[1:]] + [tuple(t.clone() if isinstance(t, torch.Tensor) else t for t in base[1:])
+                                 for _ in range(reps - 1)]
+            out = torch.empty((M, case.I), dtype=torch.bfloat16, device=dev)
+            entry = {"M": M}
+            for name, limit in (("small_m", 32), ("tensor_core", 0)):
+                ops.qsw_set_gemv_max_m(limit)
+                before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
+                ms = time_graph(lambda i: ops.qswiglu_forward(base[0], *sets[i % len(sets)], variant=ops.MATCH,
+                                                              out=out, stream=stream), 200, 3, stream)
+                if name == "small_m" and ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] == before:
+                    entry["small_m"] = "does not fit"
+                    continue
+                entry[name] = {"us": round(ms * 1e3 / 200, 2)}
+            cut.append(entry)
+            del base, sets, out
+            torch.cuda.empty_cache()
+    finally:
+        ops.qsw_set_gemv_max_m(saved)
+    ops.qsw_check_device_errors(stream)
     return {"mixed_sweep": rows, "mixed_small_m_faster_up_to": max(small) if small else 0,
-            "default_small_m_limit": saved}
+            "decode_shape_cutover": cut, "default_small_m_limit": saved}
 
 
 def _time_oracle(case, rows, threads):

@@ -171,8 +171,12 @@ QSW_API qsw_status affine_qmm_ws(const void *x, int64_t M, int64_t K, int64_t N,
  * and takes no workspace argument.  The array is one per device: calls through
  * this entry point must not run concurrently with each other (use one stream,
  * or the *_ws form with one workspace per stream).  The first call on a device
- * also enqueues a 4 KB memset of the array's header on `stream`.  Arguments,
- * results and errors as for qswiglu_forward.
+ * also resolves the array's address and enqueues a 4 KB memset of its header
+ * on `stream`; made inside a CUDA-graph capture, that memset becomes part of
+ * the graph (every replay re-zeroes the header, which is harmless: the header
+ * only needs to start at zero).  Should that first set-up fail, the call
+ * returns QSW_ERR_CUDA and the next call tries again.  Arguments, results and
+ * errors as for qswiglu_forward.
  */
 QSW_API qsw_status qswiglu_forward_noalloc(const void *x, int64_t M, int64_t H, int64_t I,
                            const uint32_t *wg, const void *sg, const void *bg,

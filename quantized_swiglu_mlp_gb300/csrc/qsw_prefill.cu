@@ -1087,16 +1087,25 @@ cudaError_t prefill_static_workspace(int num_sms, cudaStream_t stream, void **pt
   if (num_sms <= 0 || num_sms > kStaticScratchSms || prefill_workspace_bytes(num_sms) > kStaticScratchBytes)
     return cudaSuccess;   // whole tiles only
   static void *addr[64];
-  static cudaError_t status[64];
-  static std::once_flag once[64];
+  static std::atomic<bool> ready[64];
+  static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::call_once(once[dev], [&] {
-    status[dev] = cudaGetSymbolAddress(&addr[dev], g_static_scratch);
-    // epoch, done count and flags start at zero, on the stream of the first call
-    if (status[dev] == cudaSuccess) status[dev] = cudaMemsetAsync(addr[dev], 0, header_bytes(num_sms), stream);
-  });
-  if (status[dev] != cudaSuccess) return status[dev];
+  if (!ready[dev].load(std::memory_order_acquire)) {
+    // First use on this device: resolve the array's device address and zero
+    // its header (epoch, done count, flags) on the caller's stream.  A failure
+    // leaves the device unset, so the next call tries again.
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev].load(std::memory_order_relaxed)) {
+      void *a = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&a, g_static_scratch);
+      if (e != cudaSuccess) return e;
+      e = cudaMemsetAsync(a, 0, header_bytes(num_sms), stream);
+      if (e != cudaSuccess) return e;
+      addr[dev] = a;
+      ready[dev].store(true, std::memory_order_release);
+    }
+  }
   *ptr = addr[dev];
   *bytes = kStaticScratchBytes;
   return cudaSuccess;

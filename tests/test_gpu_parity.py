@@ -443,6 +443,25 @@ def test_full_mixed_sweep(dev, gemv_limit, M):
         check_fused(case, dev, ops.MATCH, rows=rows)
 
 
+@pytest.mark.parametrize("mode", [ops.STREAM_K_ALWAYS, ops.STREAM_K_AUTO], ids=["always", "auto"])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_large_prefill_projection_rate(dev, gemv_limit, stream_k, mode, seed):
+    """The exact-projection rate at H = 4096 (three accumulation chains per
+    tile) on 8 rows that include the last row tile, whose tiles the ragged
+    wave splits between SMs (stream-K): 114,688 values per projection."""
+    case = inputs.workload_case("large_prefill", seed=seed)
+    gemv_limit(0)
+    stream_k(mode)
+    rows = [0, 1, 2047, 2048, 3839, 3840, 4094, 4095]
+    a = device_args(case, dev)
+    _, g64, u64 = oracle.qswiglu(*case.oracle_args(), variant=ops.MATCH, rows=rows, return_acc=True)
+    _, _, bnd_g, bnd_u = projection_context(case, "tensor_core", rows=rows)
+    for v, ref, bnd in ((ops.DEBUG_GATE, g64, bnd_g), (ops.DEBUG_UP, u64, bnd_u)):
+        got = run_fused(case, dev, v, a)[np.asarray(rows)]
+        ok, info = check_projection(got, oracle.bf16_round_array(ref), exact=ref, bound=bnd)
+        assert ok and got.size >= 100_000, info
+
+
 @pytest.mark.parametrize("M", [16, 24, 32, 48, 128, 256])
 def test_mixed_sweep_more_m(dev, gemv_limit, M):
     """The mixed-spec workload at the M values the benchmark adds around the

@@ -98,3 +98,53 @@ def test_noalloc_graph_replays_and_takes_no_memory(dev, forced_split):
         ops.qsw_check_device_errors()
         ok, info = _match_ok(inputs.Case(x=xb, gate=base.gate, up=base.up), outs)
         assert ok, info
+
+
+_FIRST_USE_IN_CAPTURE = r"""
+import sys
+import torch
+sys.path.insert(0, {root!r})
+import oracle
+from quantized_swiglu_mlp_gb300 import inputs, ops
+from tests.gpu_util import device_args, to_bits
+from tests.tolerances import check_match
+ops.load_library()
+torch.cuda.set_device(0)
+dev = torch.device("cuda:0")
+ops.qsw_set_stream_k(ops.STREAM_K_ALWAYS)
+ops.qsw_set_gemv_max_m(0)
+case = inputs.make_case(300, 512, 1536, seed=11)
+a = device_args(case, dev)
+want = oracle.qswiglu(*case.oracle_args(), variant=oracle.MATCH)
+out = torch.empty((300, 1536), dtype=torch.bfloat16, device=dev)
+s = torch.cuda.Stream()
+g = torch.cuda.CUDAGraph()
+with torch.cuda.graph(g, stream=s):   # the process's first no-alloc call
+    ops.qswiglu_forward_noalloc(*a, variant=ops.MATCH, out=out, stream=s)
+for _ in range(2):
+    out.fill_(0)
+    with torch.cuda.stream(s):
+        g.replay()
+    torch.cuda.synchronize()
+    ops.qsw_check_device_errors(s)
+    assert check_match(to_bits(out), want)[0], "replay"
+    e = ops.qswiglu_forward_noalloc(*a, variant=ops.MATCH, stream=s)
+    torch.cuda.synchronize()
+    ops.qsw_check_device_errors(s)
+    assert check_match(to_bits(e), want)[0], "eager"
+print("OK")
+"""
+
+
+def test_noalloc_first_use_inside_capture(dev):
+    """In a fresh process the first no-alloc call is made inside a CUDA-graph
+    capture (so the scratch header's zeroing is recorded into the graph); two
+    replays interleaved with eager calls on the same stream all match the
+    oracle."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FIRST_USE_IN_CAPTURE.format(root=root)], capture_output=True,
+                       text=True, timeout=600, cwd=root)
+    assert r.returncode == 0 and r.stdout.strip().endswith("OK"), r.stdout[-2000:] + r.stderr[-2000:]
