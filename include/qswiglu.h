@@ -59,7 +59,8 @@ typedef enum {
     QSW_ERR_INVALID_ARG = 1,   /* null pointer, negative size, shape inconsistency */
     QSW_ERR_UNSUPPORTED = 2,   /* valid but not handled: bits, gs, H, alignment, size */
     QSW_ERR_CUDA = 3,          /* a CUDA runtime/driver call or launch failed */
-    QSW_ERR_TIMEOUT = 4        /* a kernel gave up on a device-side wait */
+    QSW_ERR_TIMEOUT = 4,       /* a kernel gave up on a device-side wait */
+    QSW_ERR_BOUNDS = 5         /* debug build only: a device-side address or copy check failed */
 } qsw_status;
 
 /* Rounding variants of the fused expansion (fused-swiglu-kernel.ts, header
@@ -248,9 +249,19 @@ QSW_API qsw_status qsw_silu_mul(const void *g, const void *u, int64_t n, int var
                         void *out, void *stream);
 
 /* Synchronise `stream`, then read and clear the device error word.
- * Returns QSW_ERR_TIMEOUT if any kernel gave up on a wait since the last call,
- * QSW_ERR_CUDA if synchronisation failed, else QSW_OK. */
+ * Returns QSW_ERR_BOUNDS if a debug-build check failed (libqswiglu_debug.so
+ * only), else QSW_ERR_TIMEOUT if any kernel gave up on a wait since the last
+ * call, QSW_ERR_CUDA if synchronisation failed, else QSW_OK. */
 QSW_API qsw_status qsw_check_device_errors(void *stream);
+
+/* 1 in the debug build (libqswiglu_debug.so, compiled with QSW_DEBUG_BOUNDS):
+ * every kernel fills its shared-memory staging areas -- and the tensor-core
+ * kernel its TMEM accumulators -- with NaN bit patterns at start, so a read of
+ * staging data that was never written shows up as NaN in the results, and
+ * checks TMA copy coordinates (16-byte innermost offsets), shared-memory
+ * ranges and output indices, reporting a failure as QSW_ERR_BOUNDS through
+ * qsw_check_device_errors() without trapping.  0 in the regular build. */
+QSW_API int qsw_debug_build(void);
 
 /* Largest M routed to the small-M kernel (default 16; 0 sends every M to the
  * tensor-core kernel).  Values above 32 are clamped to 32.  Process-wide. */

@@ -48,25 +48,36 @@ def source_hash() -> str:
     return h.hexdigest()[:12]
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+DEBUG_LIB_PATH = os.path.join(OUT_DIR, "libqswiglu_debug.so")
+# (library, object folder, extra nvcc flags): the regular build and the debug
+# build (device-side address/copy checks and NaN-filled staging, QSW_DEBUG_BOUNDS)
+VARIANTS = ((LIB_PATH, "obj", []), (DEBUG_LIB_PATH, "obj_debug", ["-DQSW_DEBUG_BOUNDS"]))
+
+
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, s) for s in SOURCES + HEADERS]
     deps.append(os.path.join(ROOT, "include", "qswiglu.h"))
     return any(os.path.getmtime(d) > t for d in deps)
 
 
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not _stale():
+    """Compile both libraries (every translation unit of both at once) and
+    return the regular one's path."""
+    todo = [v for v in VARIANTS if force or _stale(v[0])]
+    if not todo:
         return LIB_PATH
-    os.makedirs(os.path.join(OUT_DIR, "obj"), exist_ok=True)
     cc = nvcc()
     flags = _flags(verbose_ptxas)
+    for _, objdir, _ in todo:
+        os.makedirs(os.path.join(OUT_DIR, objdir), exist_ok=True)
 
-    def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, "obj", src.replace(".cu", ".o"))
-        cmd = [cc, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job) -> str:
+        src, objdir, extra = job
+        obj = os.path.join(OUT_DIR, objdir, src.replace(".cu", ".o"))
+        cmd = [cc, *flags, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -74,13 +85,17 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
             sys.stderr.write(r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    r = subprocess.run([cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs], capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    jobs = [(src, objdir, extra) for _, objdir, extra in todo for src in SOURCES]
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    for n, (lib, _, _) in enumerate(todo):
+        tmp = lib + f".tmp{os.getpid()}"
+        mine = objs[n * len(SOURCES):(n + 1) * len(SOURCES)]
+        r = subprocess.run([cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *mine], capture_output=True,
+                           text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
     return LIB_PATH
 
 

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "qswiglu.h"
+#include "qsw_device.cuh"
 #include "qsw_internal.h"
 
 namespace qsw {
@@ -259,6 +260,7 @@ qsw_status qsw_check_device_errors(void *stream) {
   unsigned int a = 0, b = 0;
   if (qsw::prefill_take_errors(&a) != cudaSuccess) return QSW_ERR_CUDA;
   if (qsw::gemv_take_errors(&b) != cudaSuccess) return QSW_ERR_CUDA;
+  if ((a | b) & qsw::DEVERR_BOUNDS) return QSW_ERR_BOUNDS;
   return (a | b) ? QSW_ERR_TIMEOUT : QSW_OK;
 }
 
@@ -273,6 +275,14 @@ int qsw_get_gemv_max_m(void) { return gemv_max_m(); }
 void qsw_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
 
 void qsw_debug_withhold_next_fill(void) { qsw::gemv_withhold_next(); }
+
+int qsw_debug_build(void) {
+#ifdef QSW_DEBUG_BOUNDS
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 void qsw_set_early_weight_stream(int on) { g_early_weights.store(on ? 1 : 0); }
 
@@ -294,6 +304,7 @@ const char *qsw_status_string(qsw_status s) {
     case QSW_ERR_UNSUPPORTED: return "unsupported shape, spec or alignment";
     case QSW_ERR_CUDA: return "CUDA error";
     case QSW_ERR_TIMEOUT: return "device-side wait timed out";
+    case QSW_ERR_BOUNDS: return "device-side address or copy check failed (debug build)";
     default: return "unknown status";
   }
 }

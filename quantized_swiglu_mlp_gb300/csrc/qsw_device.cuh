@@ -20,8 +20,35 @@ namespace qsw {
 
 // ------------------------------------------------------------------ errors --
 
-// Device error word bits, set by kernels that gave up on a wait.
-enum : unsigned { DEVERR_TIMEOUT = 1u };
+// Device error word bits: a kernel gave up on a wait; a debug-build check of
+// an address or a copy coordinate failed.
+enum : unsigned { DEVERR_TIMEOUT = 1u, DEVERR_BOUNDS = 2u };
+
+// ------------------------------------------------------------ debug build --
+// Built with QSW_DEBUG_BOUNDS, the kernels (1) fill their shared-memory
+// staging areas (and the tensor-core kernel its TMEM accumulators) with 0xFF
+// bytes at start -- a NaN in bf16, f16 and f32 -- so that a read of staging
+// data that was never written shows up as NaN in the results, and (2) check
+// copy coordinates and address ranges, recording a failure in the device
+// error word (DEVERR_BOUNDS) and going on: nothing traps.  Both compile to
+// nothing in the regular build.
+#ifdef QSW_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
+__device__ __forceinline__ void debug_check(bool ok, unsigned int *err) {
+  if (kDebugBounds && !ok) atomicOr(err, DEVERR_BOUNDS);
+}
+
+// Every thread of the CTA: [p, p + bytes) of shared memory (16-byte aligned;
+// a partial last 16 bytes is left) := 0xFF.  The caller synchronises.
+__device__ __forceinline__ void debug_poison_smem(uint8_t *p, uint32_t bytes) {
+  if (kDebugBounds)
+    for (uint32_t i = threadIdx.x * 16; i + 16 <= bytes; i += blockDim.x * 16)
+      *reinterpret_cast<uint4 *>(p + i) = make_uint4(~0u, ~0u, ~0u, ~0u);
+}
 
 // ----------------------------------------------------------------- helpers --
 

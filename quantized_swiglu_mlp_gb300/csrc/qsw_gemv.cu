@@ -90,6 +90,8 @@ __device__ __forceinline__ void issue_unit(const GemvParams &p, uint8_t *base, u
                                                                                      : static_cast<uint32_t>(R);
   const uint32_t sb0 = R * p.ng0 * 2, sb1 = DUAL ? R * p.ng1 * 2 : 0;   // bytes of one s/b array region
   if (lane == 0) {
+    debug_check(r0 + rows <= static_cast<uint32_t>(p.N) && rows >= 1, &g_gemv_error);
+    debug_check(p.sb_off + 2 * sb0 + 2 * sb1 <= static_cast<uint32_t>(p.slot_bytes), &g_gemv_error);
     const uint32_t bytes = rows * (p.pitch0 + (DUAL ? p.pitch1 : 0)) + rows * 4 * (p.ng0 + (DUAL ? p.ng1 : 0));
     mbar_arrive_expect_tx(bar, bytes);
     *issued += 1;   // fills of this slot so far (for draining after an abort)
@@ -134,6 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
                        static_cast<int>(gridDim.x);
   auto unit_of = [&](int i) { return static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x); };
 
+  if constexpr (kDebugBounds) {
+    debug_poison_smem(smem, static_cast<uint32_t>(p.bar_off));   // slots, x, partial sums
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.slots; ++s) {
       mbar_init(&full[s], 1);
@@ -288,6 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
       Chunk<BB, A> cb;
       uint32_t sa = 0, ba = 0, sb = 0, bb = 0;
       if (kval) {
+        debug_check((kb * kBlockK + (c + 1) * kChunk) * BITS0 / 8 <= static_cast<uint32_t>(p.pitch0) &&
+                        (!DUAL || (kb * kBlockK + (c + 1) * kChunk) * BB / 8 <= static_cast<uint32_t>(p.pitch1)) &&
+                        p.gd0(k) < p.ng0 && (!DUAL || p.gd1(k) < p.ng1),
+                    err);
         ca.load(rowa + kb * (kBlockK * BITS0 / 8));
         const uint32_t ia = p.gd0(k) * 2;
         sa = lds_u16(s_a + ia);

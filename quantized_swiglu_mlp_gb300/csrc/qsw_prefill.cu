@@ -347,6 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kpe0 = kGroupsPerEntry * p.gd0.gs / BK;
   const int kpe1 = kGroupsPerEntry * p.gd1.gs / BK;
 
+  if constexpr (kDebugBounds) {
+    debug_poison_smem(smem, C::kBarOff);   // every staging ring, before any copy lands
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < Sx; ++s) mbar_init(&x_full[s], 1);
     for (int s = 0; s < Sb; ++s) {
@@ -401,6 +405,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const unsigned int sk_tag = *sk_tag_slot;
+  if constexpr (kDebugBounds) {
+    // every accumulator column := NaN before the first MMA (each epilogue warp
+    // writes the 32 TMEM lanes of its quarter)
+    if (warp >= kWarpEpi0) {
+      const uint32_t q = static_cast<uint32_t>(warp & 3) * 32u;
+      uint32_t nan16[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) nan16[e] = ~0u;
+      for (uint32_t col = 0; col < kTmemCols; col += 16) tmem_st16(tmem_base + (q << 16) + col, nan16);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
 
   if (warp == kWarpTma) {
     // ------------------------------------------- codes and scale producer --
@@ -427,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           uint8_t *dst = smem + C::kCOff + cs * C::kCodesBytes;
           mbar_arrive_expect_tx(&c_full[cs], C::kCodesBytes);
+          debug_check((kb * BK * BITS0 / 32) % 4 == 0 && (kb * BK * BITS1 / 32) % 4 == 0, err);   // 16-byte x
           tma_load_2d(dst, &tm_c0, &c_full[cs], kb * BK * BITS0 / 32, n0_c);
           if (DUAL) tma_load_2d(dst + C::kC0Bytes, &tm_c1, &c_full[cs], kb * BK * BITS1 / 32, n0_c);
         }
@@ -448,6 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (op ? p.sb_tma1 : p.sb_tma0) {
             if (lane == 0) {
               mbar_arrive_expect_tx(&s_full[op * 2 + es], 2 * rows * 2 * kGroupsPerEntry);
+              debug_check(g0 % 8 == 0, err);   // 16-byte x (8 scales)
               tma_load_2d(sdst, op ? &tm_s1 : &tm_s0, &s_full[op * 2 + es], g0, n0_c);
               tma_load_2d(bdst, op ? &tm_b1 : &tm_b0, &s_full[op * 2 + es], g0, n0_c);
             }
@@ -503,8 +524,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&x_full[xs], nsub * kXBytes);
-          for (int j = 0; j < nsub; ++j)
+          for (int j = 0; j < nsub; ++j) {
+            debug_check(((kb + j) * BK) % 8 == 0, err);   // 16-byte x (8 activations)
             tma_load_2d(smem + C::kXOff + xs * C::kXStage + j * kXBytes, &tm_x, &x_full[xs], (kb + j) * BK, m0);
+          }
           ++n_x;
         }
       }
@@ -743,6 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             if (live) {
               float *dst = part + (static_cast<size_t>(h * (BN / 16) + j) * 4 * UM + row) * 4;
+              debug_check(static_cast<size_t>(dst - part) + 3 * UM * 4 + 4 <= static_cast<size_t>(kPartFloats), err);
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 st_global_v4(dst + i * UM * 4, make_uint4(ra[4 * i], ra[4 * i + 1], ra[4 * i + 2], ra[4 * i + 3]));
@@ -842,6 +866,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            __uint_as_float(ra[e + 1]) + A::hi(r2[e / 2]));
               }
               const int64_t col = n0 + c0;
+              // columns past N (a ragged last tile) are skipped element by element below
+              debug_check(m < p.M && col % 16 == 0, err);
               if (vec_ok && col + 16 <= p.N) {
                 st_global_v4(orow + col, make_uint4(packed[0], packed[1], packed[2], packed[3]));
                 st_global_v4(orow + col + 8, make_uint4(packed[4], packed[5], packed[6], packed[7]));

@@ -23,20 +23,21 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "lib", "libqswiglu.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "lib", "libqswiglu_debug.so")   # built with QSW_DEBUG_BOUNDS
 
 MATCH, F32, DEBUG_GATE, DEBUG_UP = 0, 1, 2, 3
 VARIANTS = {"match": MATCH, "f32": F32, "debug_gate": DEBUG_GATE, "debug_up": DEBUG_UP}
 CNT_FUSED_TC, CNT_FUSED_GEMV, CNT_QMM_TC, CNT_QMM_GEMV, CNT_SILU_MUL = range(5)
 NUM_COUNTERS = 5
 STATUS = {0: "QSW_OK", 1: "QSW_ERR_INVALID_ARG", 2: "QSW_ERR_UNSUPPORTED", 3: "QSW_ERR_CUDA",
-          4: "QSW_ERR_TIMEOUT"}
+          4: "QSW_ERR_TIMEOUT", 5: "QSW_ERR_BOUNDS"}
 STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS = 0, 1, 2
 ACT_BF16, ACT_F16 = 0, 1
 EXPORTED = ("qswiglu_forward", "affine_qmm", "qswiglu_forward_ws", "affine_qmm_ws", "qswiglu_forward_noalloc",
             "qswiglu_forward_ex", "affine_qmm_ex", "qsw_silu_mul_ex", "qsw_mlp_forward_ex", "qsw_workspace_bytes",
             "qsw_set_stream_k", "qsw_get_stream_k", "qsw_silu_mul", "qsw_check_device_errors",
             "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_early_weight_stream",
-            "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns", "qsw_debug_withhold_next_fill",
+            "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns", "qsw_debug_withhold_next_fill", "qsw_debug_build",
             "qsw_get_counters", "qsw_reset_counters", "qsw_status_string", "qsw_version")
 
 _lock = threading.Lock()
@@ -380,6 +381,13 @@ def qsw_debug_withhold_next_fill() -> None:
     """Test hook: the next small-M call leaves its first units unrequested, so
     its waits run out (see include/qswiglu.h)."""
     load_library().qsw_debug_withhold_next_fill()
+
+
+def qsw_debug_build() -> bool:
+    """Whether the loaded library is the debug build (QSW_DEBUG_BOUNDS)."""
+    lib = load_library()
+    lib.qsw_debug_build.restype = ctypes.c_int
+    return bool(lib.qsw_debug_build())
 
 
 def qsw_get_counters() -> list[int]:

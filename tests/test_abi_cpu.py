@@ -195,3 +195,16 @@ def test_mlp_entry_point_validates_on_the_host(lib):
     assert mlp(gs_d=48) == UNSUPPORTED           # down group size
     assert mlp(I=48) == UNSUPPORTED              # I is the down projection's K
     assert mlp(bits_d=3) == UNSUPPORTED
+
+
+def test_debug_build_is_built_and_exports_the_same_abi(lib):
+    """The debug build (QSW_DEBUG_BOUNDS) is built beside the regular one,
+    exports every declared symbol and says which build it is."""
+    dbg = ctypes.CDLL(qbuild.DEBUG_LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    dbg.qsw_debug_build.restype = ctypes.c_int
+    lib.qsw_debug_build.restype = ctypes.c_int
+    assert dbg.qsw_debug_build() == 1 and lib.qsw_debug_build() == 0
+    dbg.qsw_status_string.restype = ctypes.c_char_p
+    assert b"debug" in dbg.qsw_status_string(5)
