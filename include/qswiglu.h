@@ -89,7 +89,8 @@ enum {
     QSW_CNT_QMM_TC = 2,       /* affine_qmm, tensor-core kernel */
     QSW_CNT_QMM_GEMV = 3,     /* affine_qmm, small-M kernel */
     QSW_CNT_SILU_MUL = 4,     /* elementwise silu*mul */
-    QSW_NUM_COUNTERS = 5
+    QSW_CNT_GEMV_STREAM = 5,  /* small-M calls (fused or affine_qmm) served by the warp-streamed kernel */
+    QSW_NUM_COUNTERS = 6
 };
 
 /*
@@ -268,6 +269,23 @@ QSW_API int qsw_debug_build(void);
 QSW_API void qsw_set_gemv_max_m(int m);
 QSW_API int qsw_get_gemv_max_m(void);
 
+/* Which small-M kernel serves a call routed to the small-M path. */
+typedef enum {
+    QSW_SMALL_M_AUTO = 0,   /* the warp-streamed kernel where it applies (M <= 8, H <= 16384 and its
+                               staging fits in shared memory), else the slot-ring kernel (default) */
+    QSW_SMALL_M_RING = 1,   /* always the slot-ring kernel (bulk copies into shared-memory slots
+                               shared by a CTA's warps) */
+    QSW_SMALL_M_STREAM = 2  /* the warp-streamed kernel where it applies (each warp copies its own
+                               blocks into a private ring), else the slot-ring one */
+} qsw_small_m_kernel;
+
+/* Selects the small-M kernel (qsw_small_m_kernel; other values are ignored).
+ * Both compute the same function; the choice changes only which one runs and,
+ * within the f32 accumulation bound, the order of the additions.
+ * Process-wide. */
+QSW_API void qsw_set_small_m_kernel(int kernel);
+QSW_API int qsw_get_small_m_kernel(void);
+
 /* Early weight stream (default off).  When on, the small-M kernel is launched
  * as a programmatic dependent of the work before it on the stream: it may start
  * while the previous kernel is still running and streams the packed weights,
@@ -282,8 +300,8 @@ QSW_API int qsw_get_early_weight_stream(void);
 /* Per-wait limit for device-side waits, in nanoseconds (default 4e9). */
 QSW_API void qsw_set_wait_timeout_ns(uint64_t ns);
 
-/* Test hook, not for production use: the next call served by the small-M
- * kernel never requests the first unit of each of its CTAs, so every wait on
+/* Test hook, not for production use: the next call served by the slot-ring
+ * small-M kernel (the warp-streamed kernel has no spin waits) never requests the first unit of each of its CTAs, so every wait on
  * that unit's shared-memory slot runs out after the qsw_set_wait_timeout_ns
  * limit.  The kernel then lets its other copies land and returns without
  * writing its output, and the next qsw_check_device_errors() returns

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "lib")
 LIB_PATH = os.path.join(OUT_DIR, "libqswiglu.so")
-SOURCES = ["qsw_api.cu", "qsw_gemv.cu", "qsw_prefill.cu", "qsw_elementwise.cu"]
+SOURCES = ["qsw_api.cu", "qsw_gemv.cu", "qsw_gemv_stream.cu", "qsw_prefill.cu", "qsw_elementwise.cu"]
 HEADERS = ["qsw_device.cuh", "qsw_smallm.cuh", "qsw_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

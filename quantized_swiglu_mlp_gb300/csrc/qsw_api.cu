@@ -16,6 +16,7 @@
 namespace qsw {
 cudaError_t prefill_take_errors(unsigned int *out);
 cudaError_t gemv_take_errors(unsigned int *out);
+cudaError_t gemv_stream_take_errors(unsigned int *out);
 }
 
 namespace {
@@ -25,6 +26,7 @@ std::atomic<int> g_gemv_max_m{-1};   // -1: not yet initialised
 std::atomic<uint64_t> g_timeout_ns{4000000000ull};
 std::atomic<int> g_early_weights{0};
 std::atomic<int> g_stream_k{QSW_STREAM_K_AUTO};
+std::atomic<int> g_small_m_kernel{QSW_SMALL_M_AUTO};
 
 int gemv_max_m() {
   int v = g_gemv_max_m.load(std::memory_order_relaxed);
@@ -54,6 +56,35 @@ int sm_count() {
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+enum Route { ROUTE_TC = 0, ROUTE_RING = 1, ROUTE_STREAM = 2 };
+
+// Which kernel serves M rows: the small-M path up to the small-M limit (the
+// warp-streamed kernel unless the slot-ring one is selected, where it
+// applies), else -- or where neither small-M kernel applies -- the tensor-core
+// kernel.
+Route route(int64_t M, int64_t K, int64_t N, const qsw::QuantOperand &op0, const qsw::QuantOperand *op1) {
+  if (M > gemv_max_m()) return ROUTE_TC;
+  if (g_small_m_kernel.load(std::memory_order_relaxed) != QSW_SMALL_M_RING &&
+      qsw::gemv_stream_fits(M, K, N, op0, op1, sm_count()))
+    return ROUTE_STREAM;
+  if (qsw::gemv_fits(M, K, N, op0, op1, sm_count())) return ROUTE_RING;
+  return ROUTE_TC;
+}
+
+// The small-M kernel `r` (ROUTE_RING or ROUTE_STREAM).
+cudaError_t launch_small_m(Route r, const void *x, int64_t M, int64_t K, int64_t N, const qsw::QuantOperand &op0,
+                           const qsw::QuantOperand *op1, int variant, int act, void *out, const void *residual,
+                           cudaStream_t s) {
+  const bool early = g_early_weights.load(std::memory_order_relaxed) != 0;
+  if (r == ROUTE_STREAM) {
+    const cudaError_t e =
+        qsw::launch_gemv_stream(x, M, K, N, op0, op1, variant, act, out, residual, s, sm_count(), early);
+    if (e == cudaSuccess) g_counters[QSW_CNT_GEMV_STREAM].fetch_add(1, std::memory_order_relaxed);
+    return e;
+  }
+  return qsw::launch_gemv(x, M, K, N, op0, op1, variant, act, out, residual, s, g_timeout_ns.load(), sm_count(), early);
+}
 
 qsw_status check_spec(int64_t K, int gs, int bits) {
   if (gs <= 0 || K <= 0) return QSW_ERR_INVALID_ARG;
@@ -116,9 +147,9 @@ qsw_status fused_forward(const void *x, int64_t M, int64_t H, int64_t I, const u
   const qsw::QuantOperand g{wg, static_cast<const uint16_t *>(sg), static_cast<const uint16_t *>(bg), gs_g, bits_g};
   const qsw::QuantOperand u{wu, static_cast<const uint16_t *>(su), static_cast<const uint16_t *>(bu), gs_u, bits_u};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (M <= gemv_max_m() && qsw::gemv_fits(M, H, I, g, &u, sm_count())) {
-    st = from_cuda(qsw::launch_gemv(x, M, H, I, g, &u, variant, act, out, nullptr, s, g_timeout_ns.load(), sm_count(),
-                                    g_early_weights.load(std::memory_order_relaxed) != 0));
+  const Route r = route(M, H, I, g, &u);
+  if (r != ROUTE_TC) {
+    st = from_cuda(launch_small_m(r, x, M, H, I, g, &u, variant, act, out, nullptr, s));
     if (st == QSW_OK) g_counters[QSW_CNT_FUSED_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
     if (static_scratch && qsw::prefill_static_workspace(sm_count(), s, &ws.ptr, &ws.bytes) != cudaSuccess)
@@ -172,9 +203,9 @@ qsw_status affine_qmm_ex(const void *x, int64_t M, int64_t K, int64_t N, const u
 
   const qsw::QuantOperand op{w, static_cast<const uint16_t *>(s), static_cast<const uint16_t *>(b), gs, bits};
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (M <= gemv_max_m() && qsw::gemv_fits(M, K, N, op, nullptr, sm_count())) {
-    st = from_cuda(qsw::launch_gemv(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, act_dtype, y, residual, cs, g_timeout_ns.load(),
-                                    sm_count(), g_early_weights.load(std::memory_order_relaxed) != 0));
+  const Route r = route(M, K, N, op, nullptr);
+  if (r != ROUTE_TC) {
+    st = from_cuda(launch_small_m(r, x, M, K, N, op, nullptr, QSW_DEBUG_GATE, act_dtype, y, residual, cs));
     if (st == QSW_OK) g_counters[QSW_CNT_QMM_GEMV].fetch_add(1, std::memory_order_relaxed);
   } else {
     st = from_cuda(qsw::launch_prefill(x, M, K, N, op, nullptr, QSW_DEBUG_GATE, act_dtype, y, residual, cs,
@@ -257,11 +288,12 @@ qsw_status qsw_silu_mul(const void *g, const void *u, int64_t n, int variant, vo
 
 qsw_status qsw_check_device_errors(void *stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return QSW_ERR_CUDA;
-  unsigned int a = 0, b = 0;
+  unsigned int a = 0, b = 0, c = 0;
   if (qsw::prefill_take_errors(&a) != cudaSuccess) return QSW_ERR_CUDA;
   if (qsw::gemv_take_errors(&b) != cudaSuccess) return QSW_ERR_CUDA;
-  if ((a | b) & qsw::DEVERR_BOUNDS) return QSW_ERR_BOUNDS;
-  return (a | b) ? QSW_ERR_TIMEOUT : QSW_OK;
+  if (qsw::gemv_stream_take_errors(&c) != cudaSuccess) return QSW_ERR_CUDA;
+  if ((a | b | c) & qsw::DEVERR_BOUNDS) return QSW_ERR_BOUNDS;
+  return (a | b | c) ? QSW_ERR_TIMEOUT : QSW_OK;
 }
 
 void qsw_set_gemv_max_m(int m) {
@@ -283,6 +315,12 @@ int qsw_debug_build(void) {
   return 0;
 #endif
 }
+
+void qsw_set_small_m_kernel(int kernel) {
+  if (kernel >= QSW_SMALL_M_AUTO && kernel <= QSW_SMALL_M_STREAM) g_small_m_kernel.store(kernel);
+}
+
+int qsw_get_small_m_kernel(void) { return g_small_m_kernel.load(); }
 
 void qsw_set_early_weight_stream(int on) { g_early_weights.store(on ? 1 : 0); }
 
@@ -309,6 +347,6 @@ const char *qsw_status_string(qsw_status s) {
   }
 }
 
-int qsw_version(void) { return 104; }
+int qsw_version(void) { return 105; }
 
 }  // extern "C"

@@ -1,0 +1,545 @@
+// Warp-streamed small-M kernel (M <= 8): the fused SwiGLU expansion and the
+// single quantised linear, for decode-sized batches.
+//
+// Method: mlx-bun pages, src/model/fused-swiglu-kernel.ts -- at decode the two
+// projections are weight-streaming GEMVs.  Measured on this GPU, such a call
+// spends as much time in per-call fixed costs (launch, staging x, the final
+// reduction) as in its weight stream or its dequantisation, so the design
+// keeps every step outside the block loop short and division-free:
+//
+//  * unit of work: 8 output features.  Fused: A rows 0..7 of mma.sync
+//    m16n8k16 are gate rows, rows 8..15 the up rows of the same features, so
+//    one MMA yields both projections; single linear: rows 8..15 are zero.
+//    CTA b takes a contiguous range of units (sizes differ by at most one);
+//    the CTA's (unit, 128-code K block) items, unit-major, are cut into one
+//    contiguous range per warp, so a warp runs many consecutive blocks between
+//    synchronisations and the only CTA barriers are "x staged" and "partials
+//    written";
+//  * every warp streams its own blocks: each lane copies its 32 codes of A
+//    rows g and g+8 (g = lane/4) per block with 16-byte cp.async copies into
+//    a private ring of kDepth stages in shared memory, kDepth blocks ahead of
+//    the block it computes, and waits only for its own copies
+//    (cp.async.wait_group) -- no barrier, no copy engine, no slot bookkeeping;
+//  * the lane dequantises its codes to the activation dtype T (w = T(s*q + b),
+//    one rounding) with the K order inside each 8-code group interleaved
+//    (codes j, j+4 paired); x is staged once per CTA in shared memory in the
+//    matching B-fragment order, all 8 fragment rows (rows >= M zero);
+//  * scales and biases are read per block through L1; each warp requests the
+//    scale rows of its units into L1 when it starts;
+//  * each block accumulates in a fresh fragment that is added to the warp's
+//    running f32 sum; at a unit boundary the sum goes to a shared-memory
+//    partial, and after one barrier the CTA adds each unit's partials in warp
+//    order (deterministic) using per-unit warp ranges the warps recorded, and
+//    applies the epilogue.
+//
+// Two CTAs fit on an SM (at most 64 registers per thread, about 100 KB of
+// shared memory at decode sizes), so with the early weight stream the next
+// call's CTAs start and request their first blocks while this call computes.
+// The kernel has no spin waits: cp.async.wait_group waits for the thread's own
+// copies, which always complete.
+#include <atomic>
+
+#include "qsw_internal.h"
+#include "qsw_smallm.cuh"
+
+namespace qsw {
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kDepth = 3;                     // ring stages per warp
+constexpr int kBlockK = kSmallBlockK;         // codes per K block
+constexpr int kChunk = kSmallChunk;           // codes per lane per block
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kXBlockBytes = 4 * 32 * 16;     // B fragments of one block: 4 pieces x 32 lanes x 16 bytes
+constexpr int64_t kMaxK = 16384;              // the group-index multiply below is exact up to here
+
+__device__ unsigned int g_gemv_stream_error;
+
+struct StreamParams {
+  const uint16_t *x;
+  int M, K, N;
+  const uint32_t *w0, *w1;
+  const uint16_t *s0, *b0, *s1, *b1;
+  uint32_t gm0, gm1;      // group index of code k: umulhi(k >> 4, gm) (gm = ceil(2^31 / (gs / 32)))
+  uint32_t ng0, ng1;      // groups per row (K / gs)
+  int variant;
+  uint16_t *out;
+  const uint16_t *res;    // single-operand form: [M, N] added before the rounding (or null)
+  int nkb;                // K blocks per row
+  int uq, ur;             // CTA b has uq + (b < ur) units, starting at b * uq + min(b, ur)
+  int slots;              // partial-sum slots per warp
+  int red_off, ring_off, tab_off;   // byte offsets of the partial sums, the rings, the warp tables
+  int early;
+};
+
+// 16- or 8-byte asynchronous copy global -> shared, tracked per thread.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// One bf16/f16 value, zero-extended into 32 bits (through L1).
+__device__ __forceinline__ uint32_t ldg_u16(const uint16_t *p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void prefetch_l1(const void *p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
+
+// Layout of one operand's codes in a ring stage: piece q (16 bytes) of lane L
+// at q * 512 + L * 16 (2-bit: the lane's 8 bytes at L * 8), so that a warp's
+// copies and reads of one piece are 512 consecutive bytes.
+template <int BITS>
+__host__ __device__ constexpr int chunk_bytes() {
+  return BITS == 2 ? 256 : BITS / 4 * 512;
+}
+template <int BITS>
+__host__ __device__ constexpr int lane_bytes() {
+  return BITS == 2 ? 8 : 16;
+}
+template <int BITS0, int BITS1, bool DUAL>
+__host__ __device__ constexpr int stage_bytes() {
+  return chunk_bytes<BITS0>() + (DUAL ? chunk_bytes<BITS1>() : 0);
+}
+
+template <int BITS>
+__device__ __forceinline__ void copy_chunk(uint32_t dst, const uint32_t *src) {
+  if constexpr (BITS == 2) {
+    cp_async8(dst, src);
+  } else {
+#pragma unroll
+    for (int q = 0; q < BITS / 4; ++q) cp_async16(dst + q * 512, src + 4 * q);
+  }
+}
+template <int BITS>
+__device__ __forceinline__ void read_chunk(uint32_t (&w)[BITS], uint32_t src) {
+  if constexpr (BITS == 2) {
+    const uint2 v = lds64(src);
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int q = 0; q < BITS / 4; ++q) {
+      const uint4 v = lds128(src + q * 512);
+      w[4 * q + 0] = v.x;
+      w[4 * q + 1] = v.y;
+      w[4 * q + 2] = v.z;
+      w[4 * q + 3] = v.w;
+    }
+  }
+}
+
+template <int BITS0, int BITS1, bool DUAL, class A>
+__global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamParams p) {
+  constexpr int BB = DUAL ? BITS1 : BITS0;
+  constexpr int SB = stage_bytes<BITS0, BITS1, DUAL>();
+  extern __shared__ __align__(128) uint8_t smem[];
+  float *red = reinterpret_cast<float *>(smem + p.red_off);   // [kWarps][slots][32][4]
+  int *ufirst_tab = reinterpret_cast<int *>(smem + p.tab_off);  // [kWarps]: CTA-local unit of a warp's first item
+  int *wfirst_tab = ufirst_tab + kWarps;                         // [units of the CTA]: first warp of a unit
+  int *wlast_tab = wfirst_tab + p.uq + 1;                        // [units of the CTA]: last warp of a unit
+  unsigned int *err = &g_gemv_stream_error;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const uint32_t K = static_cast<uint32_t>(p.K);
+  const int nkb = p.nkb;
+  const int b = static_cast<int>(blockIdx.x);
+  const int u_begin = b * p.uq + (b < p.ur ? b : p.ur);
+  const int ucount = p.uq + (b < p.ur ? 1 : 0);
+  const int items = ucount * nkb;
+  const int i_begin = static_cast<int>(static_cast<int64_t>(warp) * items / kWarps);
+  const int i_end = static_cast<int>(static_cast<int64_t>(warp + 1) * items / kWarps);
+  const int u_first = i_begin / nkb;
+  const uint32_t ring = smem_u32(smem + p.ring_off) + warp * (kDepth * SB);
+
+  if constexpr (kDebugBounds) {   // x, partial sums, rings, warp tables
+    debug_poison_smem(smem, static_cast<uint32_t>(p.tab_off + (kWarps + 2 * (p.uq + 1)) * 4));
+    __syncthreads();
+  }
+
+  // x of a non-dependent launch is requested first: behind the weight stream
+  // it would arrive microseconds later
+  const int x_total = nkb * 32;   // (block, lane) pieces of 64 bytes
+  auto load_x = [&](int e, uint4 (&xv)[4]) {
+    const int L = e & 31, kb = e >> 5;
+    const int m = L >> 2;
+    const uint32_t k = static_cast<uint32_t>(kb) * kBlockK + (L & 3) * kChunk;
+    if (k < K && m < p.M) {
+      const uint4 *xp = reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(m) * p.K + k);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xv[q] = __ldg(xp + q);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xv[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+  // For block kb and fragment piece j (x values 8j..8j+7 of each lane's chunk),
+  // lane L = 4n + c's 16 bytes sit at (kb*4 + j)*512 + L*16: row n of x (zero
+  // for n >= M), codes kb*128 + 32c + 8j ... + 7 permuted into (x0,x4)
+  // (x1,x5) (x2,x6) (x3,x7) pairs.
+  auto store_x = [&](int e, const uint4 (&xv)[4]) {
+    uint8_t *dst = smem + static_cast<size_t>(e >> 5) * kXBlockBytes + (e & 31) * 16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(dst + j * 512) = x_fragment(xv[j]);
+  };
+  uint4 x_first[4];
+  const bool has_x = static_cast<int>(threadIdx.x) < x_total;
+  if (!p.early && has_x) load_x(threadIdx.x, x_first);
+
+  // --- warp tables for the final reduction, and the scale rows into L1 ---
+  // A warp with no items (fewer items than warps) is marked -1: it may sit
+  // between a unit's first and last warp, and holds no partial sum.
+  if (lane == 0) ufirst_tab[warp] = i_begin < i_end ? u_first : -1;
+  if (i_begin < i_end) {
+    const int u_last = (i_end - 1) / nkb;
+    for (int u = u_first + lane; u <= u_last; u += 32) {
+      debug_check(u < ucount, err);
+      if (u * nkb >= i_begin) wfirst_tab[u] = warp;             // the unit's first item is the warp's
+      if ((u + 1) * nkb - 1 < i_end) wlast_tab[u] = warp;       // the unit's last item is the warp's
+    }
+    // 8 rows x ng groups x 2 bytes per array, contiguous: 128-byte lines
+    const int arrays = DUAL ? 4 : 2;
+    for (int a = 0; a < arrays; ++a) {
+      const uint16_t *base = a == 0 ? p.s0 : a == 1 ? p.b0 : a == 2 ? p.s1 : p.b1;
+      const uint32_t ng = a < 2 ? p.ng0 : p.ng1;
+      const int64_t r_end = static_cast<int64_t>(8) * (u_begin + u_last + 1) < p.N
+                                ? static_cast<int64_t>(8) * (u_begin + u_last + 1)
+                                : static_cast<int64_t>(p.N);
+      const int64_t last = r_end * ng;
+      for (int64_t e = static_cast<int64_t>(8) * (u_begin + u_first) * ng + lane * 64; e < last; e += 32 * 64)
+        prefetch_l1(base + e);
+    }
+  }
+
+  // --- the weight stream: item i (CTA-local) = (unit i / nkb, block i % nkb) ---
+  // The lane's copy cursor advances by constant strides and jumps to the next
+  // unit's rows after a unit's last block.
+  constexpr uint32_t kStep0 = kBlockK * BITS0 / 32, kStep1 = kBlockK * BB / 32;   // words per block of a row
+  const uint32_t wpr0 = K * BITS0 / 32, wpr1 = K * BB / 32;                       // words per packed row
+  const bool k_full = (K % kBlockK) == 0;
+  int ld_left = i_end - i_begin;
+  int ld_kb = i_begin - u_first * nkb;
+  int ld_row0 = 8 * (u_begin + u_first);   // first A row of the unit being requested
+  uint32_t ld_k = static_cast<uint32_t>(ld_kb) * kBlockK + c * kChunk;
+  const uint32_t *pa = p.w0 + static_cast<int64_t>(ld_row0 + g) * wpr0 + ld_k * BITS0 / 32;
+  const uint32_t *pb = p.w1 + static_cast<int64_t>(ld_row0 + g) * wpr1 + ld_k * BB / 32;
+  const uint32_t lane0 = lane * lane_bytes<BITS0>(), lane1 = chunk_bytes<BITS0>() + lane * lane_bytes<BB>();
+  uint32_t ld_stage = 0;
+  auto issue_next = [&]() {
+    if (ld_left > 0) {   // warp-uniform
+      // lanes past N or K copy nothing: their scale and bias read as 0 below, so w = 0
+      if ((ld_row0 + 8 <= p.N && (k_full || ld_kb != nkb - 1)) || (ld_row0 + g < p.N && ld_k < K)) {
+        debug_check(ld_k + kChunk <= K && ld_row0 + g < p.N, err);
+        copy_chunk<BITS0>(ring + ld_stage + lane0, pa);
+        if constexpr (DUAL) copy_chunk<BITS1>(ring + ld_stage + lane1, pb);
+      }
+      --ld_left;
+      pa += kStep0;
+      pb += kStep1;
+      ld_k += kBlockK;
+      if (++ld_kb == nkb) {
+        ld_kb = 0;
+        ld_k = c * kChunk;
+        ld_row0 += 8;
+        pa += 8 * static_cast<int64_t>(wpr0) - static_cast<int64_t>(nkb) * kStep0;
+        pb += 8 * static_cast<int64_t>(wpr1) - static_cast<int64_t>(nkb) * kStep1;
+      }
+    }
+    cp_async_commit();   // one group per item (empty past the range), so the waits count items
+    ld_stage = ld_stage + SB == kDepth * SB ? 0 : ld_stage + SB;
+  };
+
+  if (p.early && threadIdx.x == 0) griddep_launch_dependents();
+#pragma unroll
+  for (int s = 0; s < kDepth; ++s) issue_next();
+
+  // --- x -> shared memory, once per CTA ---
+  if (p.early) {
+    // programmatic dependent: x is read only after the preceding work is done
+    if (warp == 0 && lane < p.M)
+      prefetch_l2_bulk(p.x + static_cast<int64_t>(lane) * p.K, static_cast<uint32_t>(p.K) * 2);
+    griddep_wait();
+    if (has_x) load_x(threadIdx.x, x_first);
+  }
+  if (has_x) store_x(threadIdx.x, x_first);
+  for (int e = threadIdx.x + kThreads; e < x_total; e += kThreads) {
+    uint4 xv[4];
+    load_x(e, xv);
+    store_x(e, xv);
+  }
+  __syncthreads();
+
+  // --- the warp's blocks ---
+  const uint32_t xbase = smem_u32(smem) + lane * 16;
+  float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  int cu = u_first, ckb = i_begin - u_first * nkb;
+  uint32_t xb = xbase + static_cast<uint32_t>(ckb) * kXBlockBytes;
+  int c_row = 8 * (u_begin + u_first) + g;
+  uint32_t ck = static_cast<uint32_t>(ckb) * kBlockK + c * kChunk;
+  int64_t so0 = static_cast<int64_t>(c_row) * p.ng0, so1 = static_cast<int64_t>(c_row) * p.ng1;
+  uint32_t cs = 0;   // offset of the stage being computed
+  auto flush = [&]() {
+    const int t = cu - u_first;
+    debug_check(t >= 0 && t < p.slots, err);
+    *reinterpret_cast<float4 *>(red + ((warp * p.slots + t) * 32 + lane) * 4) =
+        make_float4(sum[0], sum[1], sum[2], sum[3]);
+  };
+  const int n_items = i_end - i_begin;
+#pragma unroll 1
+  for (int i = 0; i < n_items; ++i) {
+    // the block's scales and biases (L1), zero past N or K
+    uint32_t sa = 0u, ba = 0u, sb = 0u, bb = 0u;
+    if (c_row < p.N && ck < K) {
+      const uint32_t gi0 = __umulhi(ck >> 4, p.gm0);
+      debug_check(gi0 < p.ng0, err);
+      sa = ldg_u16(p.s0 + so0 + gi0);
+      ba = ldg_u16(p.b0 + so0 + gi0);
+      if constexpr (DUAL) {
+        const uint32_t gi1 = __umulhi(ck >> 4, p.gm1);
+        debug_check(gi1 < p.ng1, err);
+        sb = ldg_u16(p.s1 + so1 + gi1);
+        bb = ldg_u16(p.b1 + so1 + gi1);
+      }
+    }
+    cp_async_wait<kDepth - 1>();   // this lane's copies of the block have landed
+    Chunk<BITS0, A> ca;
+    Chunk<BB, A> cb;
+    read_chunk<BITS0>(ca.w, ring + cs + lane0);
+    if constexpr (DUAL) read_chunk<BITS1>(cb.w, ring + cs + lane1);
+    // (a lane past N or K reads stale stage bytes: with scale and bias 0 they dequantise to 0)
+    const uint32_t sa2 = sa * 0x00010001u, ba2 = ba * 0x00010001u;
+    const uint32_t sb2 = sb * 0x00010001u, bb2 = bb * 0x00010001u;
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t pa4[4], pb4[4] = {0u, 0u, 0u, 0u};
+      ca.dequant(j, sa2, ba2, pa4);
+      if constexpr (DUAL) cb.dequant(j, sb2, bb2, pb4);
+      const uint4 xf = lds128(xb + j * 512);
+      // A rows g and g+8; k_local 2c,2c+1 <- pair 2h, k_local 2c+8,2c+9 <- pair 2h+1
+      const uint32_t a0[4] = {pa4[0], pb4[0], pa4[1], pb4[1]};
+      const uint32_t a1[4] = {pa4[2], pb4[2], pa4[3], pb4[3]};
+      mma_16816<A>(acc, a0, xf.x, xf.y);
+      mma_16816<A>(acc, a1, xf.z, xf.w);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sum[q] += acc[q];
+    // the stage is read: refill it with the block kDepth items on
+    cs = cs + SB == kDepth * SB ? 0 : cs + SB;
+    issue_next();
+    xb += kXBlockBytes;
+    ck += kBlockK;
+    if (++ckb == nkb) {   // the unit's last block: its partial sum is complete
+      flush();
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sum[q] = 0.0f;
+      ckb = 0;
+      ++cu;
+      xb = xbase;
+      ck = c * kChunk;
+      c_row += 8;
+      so0 += 8 * static_cast<int64_t>(p.ng0);
+      so1 += 8 * static_cast<int64_t>(p.ng1);
+    }
+  }
+  if (ckb != 0 && n_items > 0) flush();   // the range ended inside a unit
+  cp_async_wait<0>();                     // (only empty groups remain)
+  __syncthreads();
+
+  // --- partial sums of each unit, in warp order, then the epilogue ---
+  const int M = p.M;
+  const int per_unit = 8 * M;
+  for (int e = threadIdx.x; e < ucount * per_unit; e += kThreads) {
+    const int ul = e / per_unit, rem = e - ul * per_unit;
+    const int row = rem / M, n = rem - row * M;
+    const int64_t i_out = static_cast<int64_t>(u_begin + ul) * 8 + row;
+    if (i_out >= p.N) continue;
+    // accumulator element of (A row a, x col n): lane 4*(a % 8) + n/2,
+    // register (n & 1) + 2*(a >= 8)
+    const int l = 4 * row + (n >> 1);
+    const int q0 = n & 1;
+    float s0 = 0.0f, s1 = 0.0f;
+    int w_lo = wfirst_tab[ul], w_hi = wlast_tab[ul];
+    if constexpr (kDebugBounds) {
+      const bool ok = w_lo >= 0 && w_lo <= w_hi && w_hi < kWarps;
+      debug_check(ok, err);
+      if (!ok) w_lo = 1, w_hi = 0;
+    }
+    for (int w = w_lo; w <= w_hi; ++w) {
+      const int uf = ufirst_tab[w];
+      if (uf < 0) continue;   // no items
+      const int t = ul - uf;
+      debug_check(t >= 0 && t < p.slots && w < kWarps, err);
+      const float *rw = red + ((w * p.slots + t) * 32 + l) * 4;
+      s0 += rw[q0];
+      if constexpr (DUAL) s1 += rw[q0 + 2];
+    }
+    const int64_t o = static_cast<int64_t>(n) * p.N + i_out;
+    const float v = DUAL ? swiglu_epilogue<A>(p.variant, s0, s1) : (p.res ? s0 + A::lo(p.res[o]) : s0);
+    p.out[o] = A::store(v);
+  }
+}
+
+struct StreamLayout {
+  int red_off, ring_off, tab_off, slots, total;
+};
+
+// Shared-memory layout; total == 0 when the shape does not fit.
+StreamLayout stream_plan(int64_t M, int64_t K, int64_t N, int num_sms, int stage) {
+  StreamLayout l{};
+  if (M < 1 || M > 8 || K > kMaxK || num_sms < 1) return l;
+  const int64_t nkb = (K + kBlockK - 1) / kBlockK;
+  const int64_t units = (N + 7) / 8;
+  const int64_t grid = units < num_sms ? units : num_sms;
+  const int64_t ucta = (units + grid - 1) / grid;              // most units of a CTA
+  const int64_t ipw = (ucta * nkb + kWarps - 1) / kWarps;      // most items of a warp
+  int64_t slots = (ipw + nkb - 1) / nkb + 1;                  // units a contiguous item range can touch
+  if (slots > ucta) slots = ucta;
+  const int64_t x_bytes = nkb * kXBlockBytes;
+  const int64_t red_bytes = kWarps * slots * 512;
+  const int64_t ring_bytes = static_cast<int64_t>(kWarps) * kDepth * stage;
+  const int64_t tab_bytes = (kWarps + 2 * (ucta + 1)) * 4;
+  const int64_t total = x_bytes + red_bytes + ring_bytes + tab_bytes;
+  if (total > kSmemBudget) return l;
+  l.red_off = static_cast<int>(x_bytes);
+  l.ring_off = static_cast<int>(x_bytes + red_bytes);
+  l.tab_off = static_cast<int>(x_bytes + red_bytes + ring_bytes);
+  l.slots = static_cast<int>(slots);
+  l.total = static_cast<int>(total);
+  return l;
+}
+
+int stage_of(int bits0, int bits1, bool dual) {
+  auto chunk = [](int bits) { return bits == 2 ? 256 : bits / 4 * 512; };
+  return chunk(bits0) + (dual ? chunk(bits1) : 0);
+}
+
+template <int BITS0, int BITS1, bool DUAL, class A>
+cudaError_t launch_cfg(StreamParams p, const StreamLayout &l, cudaStream_t stream, int num_sms) {
+  const int units = (p.N + 7) / 8;
+  const int grid = units < num_sms ? units : num_sms;
+  p.nkb = (p.K + kBlockK - 1) / kBlockK;
+  p.uq = units / grid;
+  p.ur = units % grid;
+  p.slots = l.slots;
+  p.red_off = l.red_off;
+  p.ring_off = l.ring_off;
+  p.tab_off = l.tab_off;
+  static std::atomic<uint64_t> attr_done{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!(attr_done.load() & (uint64_t(1) << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<BITS0, BITS1, DUAL, A>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(uint64_t(1) << dev);
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = l.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.early ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BITS0, BITS1, DUAL, A>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int BITS0, class A>
+cudaError_t launch_bits1(const StreamParams &p, const StreamLayout &l, int bits1, cudaStream_t stream, int num_sms) {
+  switch (bits1) {
+    case 2: return launch_cfg<BITS0, 2, true, A>(p, l, stream, num_sms);
+    case 4: return launch_cfg<BITS0, 4, true, A>(p, l, stream, num_sms);
+    case 8: return launch_cfg<BITS0, 8, true, A>(p, l, stream, num_sms);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class A>
+cudaError_t launch_act(const StreamParams &p, const StreamLayout &l, int bits0, int bits1, bool dual,
+                       cudaStream_t stream, int num_sms) {
+  if (dual) {
+    switch (bits0) {
+      case 2: return launch_bits1<2, A>(p, l, bits1, stream, num_sms);
+      case 4: return launch_bits1<4, A>(p, l, bits1, stream, num_sms);
+      case 8: return launch_bits1<8, A>(p, l, bits1, stream, num_sms);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (bits0) {
+    case 2: return launch_cfg<2, 2, false, A>(p, l, stream, num_sms);
+    case 4: return launch_cfg<4, 4, false, A>(p, l, stream, num_sms);
+    case 8: return launch_cfg<8, 8, false, A>(p, l, stream, num_sms);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+uint32_t group_magic(int gs) {
+  const uint64_t d = static_cast<uint64_t>(gs / 32);
+  return static_cast<uint32_t>(((uint64_t(1) << 31) + d - 1) / d);
+}
+
+}  // namespace
+
+bool gemv_stream_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const QuantOperand *op1,
+                      int num_sms) {
+  const QuantOperand &o1 = op1 ? *op1 : op0;
+  return stream_plan(M, K, N, num_sms, stage_of(op0.bits, o1.bits, op1 != nullptr)).total > 0;
+}
+
+cudaError_t launch_gemv_stream(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
+                               const QuantOperand *op1, int variant, int act, void *out, const void *residual,
+                               cudaStream_t stream, int num_sms, bool early_weights) {
+  const QuantOperand &o1 = op1 ? *op1 : op0;
+  const StreamLayout l = stream_plan(M, K, N, num_sms, stage_of(op0.bits, o1.bits, op1 != nullptr));
+  if (l.total == 0) return cudaErrorInvalidValue;
+  StreamParams p{};
+  p.x = static_cast<const uint16_t *>(x);
+  p.M = static_cast<int>(M);
+  p.K = static_cast<int>(K);
+  p.N = static_cast<int>(N);
+  p.w0 = op0.w;
+  p.s0 = op0.s;
+  p.b0 = op0.b;
+  p.gm0 = group_magic(op0.gs);
+  p.w1 = o1.w;
+  p.s1 = o1.s;
+  p.b1 = o1.b;
+  p.gm1 = group_magic(o1.gs);
+  p.ng0 = static_cast<uint32_t>(K / op0.gs);
+  p.ng1 = static_cast<uint32_t>(K / o1.gs);
+  p.variant = variant;
+  p.out = static_cast<uint16_t *>(out);
+  p.res = op1 ? nullptr : static_cast<const uint16_t *>(residual);
+  p.early = early_weights ? 1 : 0;
+  if (act == ActF16::kId) return launch_act<ActF16>(p, l, op0.bits, o1.bits, op1 != nullptr, stream, num_sms);
+  if (act == ActBf16::kId) return launch_act<ActBf16>(p, l, op0.bits, o1.bits, op1 != nullptr, stream, num_sms);
+  return cudaErrorInvalidValue;
+}
+
+// Read and clear the device error word of this translation unit's kernel.
+cudaError_t gemv_stream_take_errors(unsigned int *out) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_gemv_stream_error, sizeof v);
+  if (e != cudaSuccess) return e;
+  if (v) {
+    e = cudaMemcpyToSymbol(g_gemv_stream_error, &zero, sizeof zero);
+    if (e != cudaSuccess) return e;
+  }
+  *out = v;
+  return cudaSuccess;
+}
+
+}  // namespace qsw

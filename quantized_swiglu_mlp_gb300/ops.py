@@ -27,17 +27,18 @@ DEBUG_LIB_PATH = os.path.join(_HERE, "lib", "libqswiglu_debug.so")   # built wit
 
 MATCH, F32, DEBUG_GATE, DEBUG_UP = 0, 1, 2, 3
 VARIANTS = {"match": MATCH, "f32": F32, "debug_gate": DEBUG_GATE, "debug_up": DEBUG_UP}
-CNT_FUSED_TC, CNT_FUSED_GEMV, CNT_QMM_TC, CNT_QMM_GEMV, CNT_SILU_MUL = range(5)
-NUM_COUNTERS = 5
+CNT_FUSED_TC, CNT_FUSED_GEMV, CNT_QMM_TC, CNT_QMM_GEMV, CNT_SILU_MUL, CNT_GEMV_STREAM = range(6)
+NUM_COUNTERS = 6
 STATUS = {0: "QSW_OK", 1: "QSW_ERR_INVALID_ARG", 2: "QSW_ERR_UNSUPPORTED", 3: "QSW_ERR_CUDA",
           4: "QSW_ERR_TIMEOUT", 5: "QSW_ERR_BOUNDS"}
 STREAM_K_OFF, STREAM_K_AUTO, STREAM_K_ALWAYS = 0, 1, 2
 ACT_BF16, ACT_F16 = 0, 1
+SMALL_M_AUTO, SMALL_M_RING, SMALL_M_STREAM = 0, 1, 2
 EXPORTED = ("qswiglu_forward", "affine_qmm", "qswiglu_forward_ws", "affine_qmm_ws", "qswiglu_forward_noalloc",
             "qswiglu_forward_ex", "affine_qmm_ex", "qsw_silu_mul_ex", "qsw_mlp_forward_ex", "qsw_workspace_bytes",
             "qsw_set_stream_k", "qsw_get_stream_k", "qsw_silu_mul", "qsw_check_device_errors",
             "qsw_set_gemv_max_m", "qsw_get_gemv_max_m", "qsw_set_early_weight_stream",
-            "qsw_get_early_weight_stream", "qsw_set_wait_timeout_ns", "qsw_debug_withhold_next_fill", "qsw_debug_build",
+            "qsw_get_early_weight_stream", "qsw_set_small_m_kernel", "qsw_get_small_m_kernel", "qsw_set_wait_timeout_ns", "qsw_debug_withhold_next_fill", "qsw_debug_build",
             "qsw_get_counters", "qsw_reset_counters", "qsw_status_string", "qsw_version")
 
 _lock = threading.Lock()
@@ -94,6 +95,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.qsw_set_early_weight_stream.argtypes = [i32]
         lib.qsw_get_early_weight_stream.restype = i32
         lib.qsw_set_wait_timeout_ns.argtypes = [u64]
+        lib.qsw_set_small_m_kernel.argtypes = [i32]
+        lib.qsw_get_small_m_kernel.restype = i32
         lib.qsw_get_counters.argtypes = [ctypes.POINTER(u64), i32]
         lib.qsw_status_string.argtypes = [i32]
         lib.qsw_status_string.restype = ctypes.c_char_p
@@ -410,6 +413,15 @@ def qsw_set_early_weight_stream(on: bool) -> None:
 
 def qsw_get_early_weight_stream() -> bool:
     return bool(load_library().qsw_get_early_weight_stream())
+
+
+def qsw_set_small_m_kernel(kernel: int) -> None:
+    """SMALL_M_AUTO (default), SMALL_M_RING or SMALL_M_STREAM (include/qswiglu.h)."""
+    load_library().qsw_set_small_m_kernel(int(kernel))
+
+
+def qsw_get_small_m_kernel() -> int:
+    return int(load_library().qsw_get_small_m_kernel())
 
 
 def qsw_version() -> int:

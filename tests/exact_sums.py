@@ -22,9 +22,11 @@ the two kernels:
     then one X += Y merge per later chain (ceil(nk / 22) chains, nk = K / 64
     steps), and at most one f32 add per stream-K contributor of a split tile
     (each contributor holds at least 8 K steps: ceil(nk / 8));
-  small-M kernel: 8 chained MMAs per 128-code block into a fresh fragment, one
-    f32 add per block a warp takes (at most ceil(nkb / 2), nkb = K / 128), and
-    the adds of at most 4 warps' partial sums.
+  small-M kernels: 8 chained MMAs per 128-code block into a fresh fragment,
+    then f32 adds of the blocks' fragments and of partial sums.  Both kernels
+    cut a unit's nkb = K / 128 blocks into P contiguous or interleaved pieces,
+    one running sum each (at most nkb - P + 1 blocks, as many adds), and add
+    the P partials: at most nkb + 1 adds on any path, whatever the split.
 """
 from __future__ import annotations
 
@@ -44,7 +46,7 @@ def accumulation_steps(kernel: str, K: int) -> int:
         return 4 * 22 + math.ceil(nk / 22) + math.ceil(nk / 8)
     if kernel == "small_m":
         nkb = math.ceil(K / 128)
-        return 8 + math.ceil(nkb / 2) + 4
+        return 8 + nkb + 1
     raise ValueError(kernel)
 
 

@@ -1,5 +1,5 @@
 """The debug build (libqswiglu_debug.so, QSW_DEBUG_BOUNDS) on small cases of
-both kernels: every kernel fills its shared-memory staging (and the
+the three kernels: every kernel fills its shared-memory staging (and the
 tensor-core kernel its TMEM accumulators) with NaN patterns first, so a read
 of staging data that was never written would surface as NaN and fail the
 oracle comparison, and its address and copy checks would report
@@ -55,21 +55,25 @@ for mode in (ops.STREAM_K_OFF, ops.STREAM_K_ALWAYS):
     for M, H, I, bg_, gg, bu_, gu in shapes:
         fused(inputs.make_case(M, H, I, bits_g=bg_, gs_g=gg, bits_u=bu_, gs_u=gu, seed=M + H), "tensor_core")
 ops.qsw_set_gemv_max_m(32)
-for M, H, I, bg_, gg, bu_, gu in [(1, 512, 8, 4, 64, 4, 64), (3, 512, 203, 4, 64, 4, 64), (8, 512, 64, 2, 64, 4, 32),
-                                  (17, 1024, 100, 4, 64, 4, 64), (6, 2048, 20000, 4, 64, 4, 64)]:
-    fused(inputs.make_case(M, H, I, bits_g=bg_, gs_g=gg, bits_u=bu_, gs_u=gu, seed=M * 3 + H), "small_m")
-fused(inputs.make_case(5, 512, 136, seed=9, dtype="f16"), "small_m")
+for kernel in (ops.SMALL_M_RING, ops.SMALL_M_STREAM):
+    ops.qsw_set_small_m_kernel(kernel)
+    for M, H, I, bg_, gg, bu_, gu in [(1, 512, 8, 4, 64, 4, 64), (3, 512, 203, 4, 64, 4, 64),
+                                      (8, 512, 64, 2, 64, 4, 32), (17, 1024, 100, 4, 64, 4, 64),
+                                      (6, 2048, 20000, 4, 64, 4, 64), (2, 2080, 64, 4, 32, 8, 32)]:
+        fused(inputs.make_case(M, H, I, bits_g=bg_, gs_g=gg, bits_u=bu_, gs_u=gu, seed=M * 3 + H), "small_m")
+    fused(inputs.make_case(5, 512, 136, seed=9, dtype="f16"), "small_m")
 ops.qsw_set_gemv_max_m(0)
 fused(inputs.make_case(150, 512, 136, seed=9, dtype="f16"), "tensor_core")
-# the single-operand form on both kernels
-for limit, M in ((0, 70), (32, 3)):
+# the single-operand form on the three kernels
+for limit, M, kernel in ((0, 70, ops.SMALL_M_AUTO), (32, 3, ops.SMALL_M_RING), (32, 3, ops.SMALL_M_STREAM)):
+    ops.qsw_set_small_m_kernel(kernel)
     ops.qsw_set_gemv_max_m(limit)
     case = inputs.make_case(M, 1024, 300, bits_g=4, gs_g=64, seed=M)
     x, w, s, b, gs, bits = device_args(case, dev)[:6]
     y = to_bits(ops.affine_qmm(x, w, s, b, gs, bits))
     ops.qsw_check_device_errors()
     ok, info = check_projection(y, oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gs, bits))
-    assert ok, ("qmm", limit, info)
+    assert ok, ("qmm", limit, kernel, info)
 print("OK")
 """
 

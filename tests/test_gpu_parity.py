@@ -36,6 +36,29 @@ def gemv_limit():
     ops.qsw_set_gemv_max_m(saved)
 
 
+@pytest.fixture
+def small_m_kernel():
+    saved = ops.qsw_get_small_m_kernel()
+    yield ops.qsw_set_small_m_kernel
+    ops.qsw_set_small_m_kernel(saved)
+
+
+# the two small-M kernels: slot ring (bulk copies into CTA-shared slots) and
+# warp-streamed (M <= 8)
+SMALL_M_KERNELS = [ops.SMALL_M_RING, ops.SMALL_M_STREAM]
+KNAMES = {ops.SMALL_M_RING: "ring", ops.SMALL_M_STREAM: "stream"}
+
+
+def expect_small_m(before, kernel, M, counter=None):
+    """The call(s) since `before` ran on the small-M path, on the selected
+    kernel (the warp-streamed one serves M <= 8)."""
+    after = ops.qsw_get_counters()
+    if counter is not None:
+        assert after[counter] > before[counter]
+    reg = after[ops.CNT_GEMV_STREAM] > before[ops.CNT_GEMV_STREAM]
+    assert reg == (kernel == ops.SMALL_M_STREAM and M <= 8), (kernel, M)
+
+
 def check(variant, got, want, dtype="bf16"):
     """F32 and the stored projections against the oracle (MATCH goes through
     check_fused, which also needs the projections)."""
@@ -110,9 +133,9 @@ TC_SHAPES = [
     (128, 1024, 256, 8, 32, 8, 32),    # exact tiles, 8-bit both
 ]
 
-# The small-M kernel stages a unit's scale rows with 16-byte copies, so it
-# takes shapes with (H / gs) % 8 == 0; the others run on the tensor-core kernel
-# (test_small_m_routes_unstageable_shapes).
+# The slot-ring small-M kernel stages a unit's scale rows with 16-byte copies,
+# so it takes shapes with (H / gs) % 8 == 0; with it selected the others run on
+# the tensor-core kernel (test_small_m_routes_unstageable_shapes).
 GEMV_SHAPES = [
     (1, 512, 8, 4, 64, 4, 64),         # one partial unit
     (2, 256, 40, 4, 32, 8, 32),        # mixed specs, 5 units
@@ -140,15 +163,17 @@ def test_tensor_core_kernel(dev, gemv_limit, shape, variant):
     assert ops.qsw_get_counters()[ops.CNT_FUSED_TC] > before
 
 
+@pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
 @pytest.mark.parametrize("shape", GEMV_SHAPES, ids=_ids(GEMV_SHAPES))
 @pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAMES[v])
-def test_small_m_kernel(dev, gemv_limit, shape, variant):
+def test_small_m_kernel(dev, gemv_limit, small_m_kernel, kernel, shape, variant):
     M, H, I, bg, gg, bu, gu = shape
     case = inputs.make_case(M, H, I, bits_g=bg, gs_g=gg, bits_u=bu, gs_u=gu, seed=M * 11 + H)
     gemv_limit(32)
-    before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
+    small_m_kernel(kernel)
+    before = ops.qsw_get_counters()
     check_fused(case, dev, variant)
-    assert ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] > before
+    expect_small_m(before, kernel, M, ops.CNT_FUSED_GEMV)
 
 
 # More small-M shapes: many slot refills per CTA, odd M, 2- and 8-bit
@@ -162,44 +187,50 @@ MORE_SMALL_M_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
 @pytest.mark.parametrize("shape", MORE_SMALL_M_SHAPES, ids=_ids(MORE_SMALL_M_SHAPES))
 @pytest.mark.parametrize("variant", [ops.MATCH, ops.F32], ids=["match", "f32"])
-def test_small_m_kernel_more_shapes(dev, gemv_limit, shape, variant):
+def test_small_m_kernel_more_shapes(dev, gemv_limit, small_m_kernel, kernel, shape, variant):
     M, H, I, bg, gg, bu, gu = shape
     case = inputs.make_case(M, H, I, bits_g=bg, gs_g=gg, bits_u=bu, gs_u=gu, seed=M * 13 + I)
     gemv_limit(16)
-    before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
+    small_m_kernel(kernel)
+    before = ops.qsw_get_counters()
     check_fused(case, dev, variant, rows=list(range(M)))
-    assert ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] > before
+    expect_small_m(before, kernel, M, ops.CNT_FUSED_GEMV)
 
 
+@pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
 @pytest.mark.parametrize("M,K,N", [(1, 2048, 1000), (3, 1024, 203), (8, 512, 40), (2, 8192, 2048)])
 @pytest.mark.parametrize("with_residual", [False, True], ids=["plain", "residual"])
-def test_small_m_single_operand(dev, gemv_limit, M, K, N, with_residual):
-    """affine_qmm on the small-M kernel (ragged units), with and without a
+def test_small_m_single_operand(dev, gemv_limit, small_m_kernel, kernel, M, K, N, with_residual):
+    """affine_qmm on the small-M kernels (ragged units), with and without a
     residual."""
     case = inputs.make_case(M, K, N, bits_g=4, gs_g=64, seed=M + K + N)
     gemv_limit(16)
+    small_m_kernel(kernel)
     x, w, s, b, gs, bits = device_args(case, dev)[:6]
     h = inputs.make_x(M, N, seed=K) if with_residual else None
-    before = ops.qsw_get_counters()[ops.CNT_QMM_GEMV]
+    before = ops.qsw_get_counters()
     y = ops.affine_qmm(x, w, s, b, gs, bits, residual=None if h is None else inputs.bits_to_device(h, dev))
     got = to_bits(y)
     ops.qsw_check_device_errors()
-    assert ops.qsw_get_counters()[ops.CNT_QMM_GEMV] == before + 1
+    assert ops.qsw_get_counters()[ops.CNT_QMM_GEMV] == before[ops.CNT_QMM_GEMV] + 1
+    expect_small_m(before, kernel, M)
     want = oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gs, bits, residual=h)
     ok, info = check_projection(got, want)
     assert ok, info
 
 
 @pytest.mark.parametrize("early", [False, True], ids=["plain", "early_weights"])
-def test_small_m_wait_runs_out(dev, gemv_limit, early_weights, early):
-    """A fill that never comes: with the test hook, the next small-M call never
-    requests its CTAs' first units.  Every wait on them gives up after the
+def test_small_m_wait_runs_out(dev, gemv_limit, small_m_kernel, early_weights, early):
+    """A fill that never comes: with the test hook, the next call on the
+    slot-ring small-M kernel never requests its CTAs' first units.  Every wait on them gives up after the
     (short) limit, the kernel returns without trapping, the error word reports
     QSW_ERR_TIMEOUT, and the next call on the same stream is correct again."""
     case = inputs.workload_case("decode")
     gemv_limit(16)
+    small_m_kernel(ops.SMALL_M_RING)
     early_weights(early)
     a = device_args(case, dev)
     want = oracle.qswiglu(*case.oracle_args(), variant=ops.MATCH)
@@ -220,23 +251,33 @@ def test_small_m_wait_runs_out(dev, gemv_limit, early_weights, early):
 
 @pytest.mark.parametrize("shape", [(2, 96, 40, 4, 32, 4, 32), (3, 2080, 64, 4, 32, 8, 32)],
                          ids=["groups_per_row_12", "k_tail"])
-def test_small_m_routes_unstageable_shapes(dev, gemv_limit, shape):
+def test_small_m_routes_unstageable_shapes(dev, gemv_limit, small_m_kernel, shape):
+    """Shapes the slot-ring kernel cannot stage go to the tensor-core kernel
+    when it is selected; the warp-streamed kernel takes them."""
     M, H, I, bg, gg, bu, gu = shape
     case = inputs.make_case(M, H, I, bits_g=bg, gs_g=gg, bits_u=bu, gs_u=gu, seed=5)
     gemv_limit(32)
+    small_m_kernel(ops.SMALL_M_RING)
     before = ops.qsw_get_counters()
     check_fused(case, dev, ops.MATCH)
     after = ops.qsw_get_counters()
     assert after[ops.CNT_FUSED_TC] > before[ops.CNT_FUSED_TC]
     assert after[ops.CNT_FUSED_GEMV] == before[ops.CNT_FUSED_GEMV]
+    small_m_kernel(ops.SMALL_M_STREAM)
+    before = ops.qsw_get_counters()
+    for v in VARIANTS:
+        check_fused(case, dev, v)
+    expect_small_m(before, ops.SMALL_M_STREAM, M, ops.CNT_FUSED_GEMV)
 
 
+@pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
 @pytest.mark.parametrize("M", [1, 4, 8])
-def test_small_m_projection_rate(dev, gemv_limit, M):
-    """The exact-projection rate of the small-M kernel on a large sample
+def test_small_m_projection_rate(dev, gemv_limit, small_m_kernel, kernel, M):
+    """The exact-projection rate of the small-M kernels on a large sample
     (mixed specs, H=2560, all 10240 outputs)."""
     case = inputs.workload_case("mixed", M=M, seed=7)
     gemv_limit(32)
+    small_m_kernel(kernel)
     a = device_args(case, dev)
     _, g64, u64 = oracle.qswiglu(*case.oracle_args(), variant=ops.MATCH, return_acc=True)
     before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
@@ -247,16 +288,20 @@ def test_small_m_projection_rate(dev, gemv_limit, M):
     assert ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] == before + 2
 
 
-@pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
-def test_fused_match_equals_unfused(dev, gemv_limit, limit):
+@pytest.mark.parametrize("limit,M,kernel", [(0, 24, ops.SMALL_M_AUTO), (32, 24, ops.SMALL_M_RING),
+                                            (32, 6, ops.SMALL_M_RING), (32, 6, ops.SMALL_M_STREAM)],
+                         ids=["tensor_core", "small_m_ring_M24", "small_m_ring_M6", "small_m_stream_M6"])
+def test_fused_match_equals_unfused(dev, gemv_limit, small_m_kernel, limit, M, kernel):
     """MATCH is the unfused composition op for op, and both kernels compute it
     bit for bit: each kernel folds every K block into the f32 accumulator the
     same way in its fused and single-operand forms (same K split; an MMA's
     result for one A row does not depend on the other rows -- measured: the
     fused gate/up projections equal affine_qmm's bit for bit), and the MATCH
     epilogue rounds at the same points as the elementwise kernel."""
-    case = inputs.make_case(24, 1024, 264, bits_g=4, gs_g=64, bits_u=8, gs_u=32, seed=3)
+    case = inputs.make_case(M, 1024, 264, bits_g=4, gs_g=64, bits_u=8, gs_u=32, seed=3)
     gemv_limit(limit)
+    small_m_kernel(kernel)
+    before = ops.qsw_get_counters()
     a = device_args(case, dev)
     # whole tiles: the fused and single-operand launches split K differently
     # under stream-K scheduling, which changes the f32 summation order
@@ -268,16 +313,20 @@ def test_fused_match_equals_unfused(dev, gemv_limit, limit):
     sg_ = to_bits(ops.affine_qmm(x, wg, sg, bg, gsg, btg, workspace=None))
     su_ = to_bits(ops.affine_qmm(x, wu, su, bu, gsu, btu, workspace=None))
     ops.qsw_check_device_errors()
+    if limit:
+        expect_small_m(before, kernel, M, ops.CNT_FUSED_GEMV)
     assert np.array_equal(pg, sg_) and np.array_equal(pu, su_)
     assert np.array_equal(fused, unfused)
 
 
-@pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
+@pytest.mark.parametrize("limit,kernel", [(0, ops.SMALL_M_AUTO), (32, ops.SMALL_M_RING), (32, ops.SMALL_M_STREAM)],
+                         ids=["tensor_core", "small_m_ring", "small_m_stream"])
 @pytest.mark.parametrize("bits,gs", [(4, 64), (8, 32), (2, 64)])
-def test_affine_qmm(dev, gemv_limit, limit, bits, gs):
+def test_affine_qmm(dev, gemv_limit, small_m_kernel, limit, kernel, bits, gs):
     M, K, N = (5, 1024, 300) if limit else (140, 640, 300)
     case = inputs.make_case(M, K, N, bits_g=bits, gs_g=gs, seed=bits + gs)
     gemv_limit(limit)
+    small_m_kernel(kernel)
     x, w, s, b, _, _ = device_args(case, dev)[:6]
     got = to_bits(ops.affine_qmm(x, w, s, b, gs, bits))
     ops.qsw_check_device_errors()
@@ -389,17 +438,23 @@ def _sampled(case, dev, variant, rows, limit, gemv_limit):
     return got
 
 
+@pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
 @pytest.mark.parametrize("variant", [ops.MATCH, ops.F32], ids=["match", "f32"])
-def test_full_decode(dev, gemv_limit, variant):
+def test_full_decode(dev, gemv_limit, small_m_kernel, kernel, variant):
     case = inputs.workload_case("decode")
+    small_m_kernel(kernel)
+    before = ops.qsw_get_counters()
     _sampled(case, dev, variant, [0], 16, gemv_limit)
+    expect_small_m(before, kernel, 1, ops.CNT_FUSED_GEMV)
 
 
-def test_decode_projection_rate(dev, gemv_limit):
+@pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
+def test_decode_projection_rate(dev, gemv_limit, small_m_kernel, kernel):
     """The exact-projection rate at the decode workload, in the benchmark's
     launch configuration: every output of three x seeds (24,576 elements per
     projection), so the 99.9 % bar is enforced, not only reported."""
     gemv_limit(16)
+    small_m_kernel(kernel)
     got = {ops.DEBUG_GATE: [], ops.DEBUG_UP: []}
     want = {ops.DEBUG_GATE: [], ops.DEBUG_UP: []}
     for seed in (0, 1, 2):
@@ -481,14 +536,16 @@ def early_weights():
     ops.qsw_set_early_weight_stream(saved)
 
 
+@pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
 @pytest.mark.parametrize("graph", [False, True], ids=["stream", "graph"])
-def test_early_weight_stream_reads_previous_output(dev, gemv_limit, early_weights, graph):
+def test_early_weight_stream_reads_previous_output(dev, gemv_limit, small_m_kernel, early_weights, kernel, graph):
     """With the early weight stream on, a small-M call may start while the call
     before it runs; it must still read x only after that call wrote it.  Three
     fused calls are chained (I == H, each call's hidden is the next call's x),
     on a stream and captured in a CUDA graph, and every output is checked
     against the oracle fed the GPU's own previous output."""
     gemv_limit(16)
+    small_m_kernel(kernel)
     early_weights(True)
     cases = [inputs.make_case(2, 1024, 1024, seed=s, scale_range=(0.01, 0.03)) for s in (11, 12, 13)]
     args = [device_args(c, dev) for c in cases]
@@ -677,15 +734,17 @@ def test_f16_tensor_core_kernel(dev, gemv_limit, shape, variant):
     assert got.dtype == np.uint16
 
 
+@pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
 @pytest.mark.parametrize("shape", F16_GEMV_SHAPES, ids=_ids(F16_GEMV_SHAPES))
 @pytest.mark.parametrize("variant", VARIANTS, ids=lambda v: VNAMES[v])
-def test_f16_small_m_kernel(dev, gemv_limit, shape, variant):
+def test_f16_small_m_kernel(dev, gemv_limit, small_m_kernel, kernel, shape, variant):
     M, H, I, bg, gg, bu, gu = shape
     case = inputs.make_case(M, H, I, bits_g=bg, gs_g=gg, bits_u=bu, gs_u=gu, seed=M * 3 + H, dtype="f16")
     gemv_limit(32)
-    before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
+    small_m_kernel(kernel)
+    before = ops.qsw_get_counters()
     check_fused(case, dev, variant)
-    assert ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] > before
+    expect_small_m(before, kernel, M, ops.CNT_FUSED_GEMV)
 
 
 @pytest.mark.parametrize("limit", [0, 32], ids=["tensor_core", "small_m"])
