@@ -28,9 +28,9 @@
 //    scale rows of its units into L1 when it starts;
 //  * each block accumulates in a fresh fragment that is added to the warp's
 //    running f32 sum; at a unit boundary the sum goes to a shared-memory
-//    partial, and after one barrier the CTA adds each unit's partials in warp
-//    order (deterministic) using per-unit warp ranges the warps recorded, and
-//    applies the epilogue.
+//    partial, and after one barrier the warp holding a unit's last block adds
+//    the unit's partials in warp order (deterministic), every lane its own
+//    accumulator registers, and applies the epilogue.
 //
 // Two CTAs fit on an SM (at most 64 registers per thread, about 100 KB of
 // shared memory at decode sizes), so with the early weight stream the next
@@ -144,7 +144,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   float *red = reinterpret_cast<float *>(smem + p.red_off);   // [kWarps][slots][32][4]
   int *ufirst_tab = reinterpret_cast<int *>(smem + p.tab_off);  // [kWarps]: CTA-local unit of a warp's first item
   int *wfirst_tab = ufirst_tab + kWarps;                         // [units of the CTA]: first warp of a unit
-  int *wlast_tab = wfirst_tab + p.uq + 1;                        // [units of the CTA]: last warp of a unit
   unsigned int *err = &g_gemv_stream_error;
 
   const int warp = threadIdx.x >> 5;
@@ -162,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   const uint32_t ring = smem_u32(smem + p.ring_off) + warp * (kDepth * SB);
 
   if constexpr (kDebugBounds) {   // x, partial sums, rings, warp tables
-    debug_poison_smem(smem, static_cast<uint32_t>(p.tab_off + (kWarps + 2 * (p.uq + 1)) * 4));
+    debug_poison_smem(smem, static_cast<uint32_t>(p.tab_off + (kWarps + p.uq + 1) * 4));
     __syncthreads();
   }
 
@@ -204,7 +203,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
     for (int u = u_first + lane; u <= u_last; u += 32) {
       debug_check(u < ucount, err);
       if (u * nkb >= i_begin) wfirst_tab[u] = warp;             // the unit's first item is the warp's
-      if ((u + 1) * nkb - 1 < i_end) wlast_tab[u] = warp;       // the unit's last item is the warp's
     }
     // 8 rows x ng groups x 2 bytes per array, contiguous: 128-byte lines
     const int arrays = DUAL ? 4 : 2;
@@ -293,11 +291,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
     *reinterpret_cast<float4 *>(red + ((warp * p.slots + t) * 32 + lane) * 4) =
         make_float4(sum[0], sum[1], sum[2], sum[3]);
   };
-  const int n_items = i_end - i_begin;
-#pragma unroll 1
-  for (int i = 0; i < n_items; ++i) {
-    // the block's scales and biases (L1), zero past N or K
-    uint32_t sa = 0u, ba = 0u, sb = 0u, bb = 0u;
+  // the next block's scales and biases (through L1, one block ahead of their
+  // use), zero past N or K
+  uint32_t sa = 0u, ba = 0u, sb = 0u, bb = 0u;
+  auto load_scales = [&]() {
+    sa = ba = sb = bb = 0u;
     if (c_row < p.N && ck < K) {
       const uint32_t gi0 = __umulhi(ck >> 4, p.gm0);
       debug_check(gi0 < p.ng0, err);
@@ -310,6 +308,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
         bb = ldg_u16(p.b1 + so1 + gi1);
       }
     }
+  };
+  const int n_items = i_end - i_begin;
+  if (n_items > 0) load_scales();
+#pragma unroll 1
+  for (int i = 0; i < n_items; ++i) {
     cp_async_wait<kDepth - 1>();   // this lane's copies of the block have landed
     Chunk<BITS0, A> ca;
     Chunk<BB, A> cb;
@@ -350,42 +353,45 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
       so0 += 8 * static_cast<int64_t>(p.ng0);
       so1 += 8 * static_cast<int64_t>(p.ng1);
     }
+    if (i + 1 < n_items) load_scales();
   }
   if (ckb != 0 && n_items > 0) flush();   // the range ended inside a unit
   cp_async_wait<0>();                     // (only empty groups remain)
   __syncthreads();
 
   // --- partial sums of each unit, in warp order, then the epilogue ---
-  const int M = p.M;
-  const int per_unit = 8 * M;
-  for (int e = threadIdx.x; e < ucount * per_unit; e += kThreads) {
-    const int ul = e / per_unit, rem = e - ul * per_unit;
-    const int row = rem / M, n = rem - row * M;
-    const int64_t i_out = static_cast<int64_t>(u_begin + ul) * 8 + row;
-    if (i_out >= p.N) continue;
-    // accumulator element of (A row a, x col n): lane 4*(a % 8) + n/2,
-    // register (n & 1) + 2*(a >= 8)
-    const int l = 4 * row + (n >> 1);
-    const int q0 = n & 1;
-    float s0 = 0.0f, s1 = 0.0f;
-    int w_lo = wfirst_tab[ul], w_hi = wlast_tab[ul];
-    if constexpr (kDebugBounds) {
-      const bool ok = w_lo >= 0 && w_lo <= w_hi && w_hi < kWarps;
-      debug_check(ok, err);
-      if (!ok) w_lo = 1, w_hi = 0;
+  // The warp that holds a unit's last block finishes it: lane (g, c) adds the
+  // partials of its own accumulator registers (A rows g and g+8, x columns 2c
+  // and 2c+1) over the unit's warps in warp order and applies the epilogue to
+  // its outputs (i = 8u + g, m = 2c and 2c+1).
+  if (i_begin < i_end) {
+    const int u_last = (i_end - 1) / nkb;
+    for (int u = u_first; u <= u_last; ++u) {
+      if ((u + 1) * nkb - 1 >= i_end) continue;   // the unit ends in a later warp's range
+      float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      for (int w = wfirst_tab[u]; w <= warp; ++w) {
+        const int uf = ufirst_tab[w];
+        if (uf < 0) continue;   // no items
+        const int t = u - uf;
+        debug_check(t >= 0 && t < p.slots, err);
+        const float4 v = *reinterpret_cast<const float4 *>(red + ((w * p.slots + t) * 32 + lane) * 4);
+        s4.x += v.x;
+        s4.y += v.y;
+        s4.z += v.z;
+        s4.w += v.w;
+      }
+      const int64_t i_out = static_cast<int64_t>(u_begin + u) * 8 + g;
+      if (i_out >= p.N) continue;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int m = 2 * c + q;
+        if (m >= p.M) break;
+        const float gv = q ? s4.y : s4.x, uv = q ? s4.w : s4.z;
+        const int64_t o = static_cast<int64_t>(m) * p.N + i_out;
+        const float v = DUAL ? swiglu_epilogue<A>(p.variant, gv, uv) : (p.res ? gv + A::lo(p.res[o]) : gv);
+        p.out[o] = A::store(v);
+      }
     }
-    for (int w = w_lo; w <= w_hi; ++w) {
-      const int uf = ufirst_tab[w];
-      if (uf < 0) continue;   // no items
-      const int t = ul - uf;
-      debug_check(t >= 0 && t < p.slots && w < kWarps, err);
-      const float *rw = red + ((w * p.slots + t) * 32 + l) * 4;
-      s0 += rw[q0];
-      if constexpr (DUAL) s1 += rw[q0 + 2];
-    }
-    const int64_t o = static_cast<int64_t>(n) * p.N + i_out;
-    const float v = DUAL ? swiglu_epilogue<A>(p.variant, s0, s1) : (p.res ? s0 + A::lo(p.res[o]) : s0);
-    p.out[o] = A::store(v);
   }
 }
 
@@ -407,7 +413,7 @@ StreamLayout stream_plan(int64_t M, int64_t K, int64_t N, int num_sms, int stage
   const int64_t x_bytes = nkb * kXBlockBytes;
   const int64_t red_bytes = kWarps * slots * 512;
   const int64_t ring_bytes = static_cast<int64_t>(kWarps) * kDepth * stage;
-  const int64_t tab_bytes = (kWarps + 2 * (ucta + 1)) * 4;
+  const int64_t tab_bytes = (kWarps + ucta + 1) * 4;
   const int64_t total = x_bytes + red_bytes + ring_bytes + tab_bytes;
   if (total > kSmemBudget) return l;
   l.red_off = static_cast<int>(x_bytes);
