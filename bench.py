@@ -78,13 +78,13 @@ def weight_bytes(case) -> int:
 
 def read_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu capture, if the kernel's
-    source has not changed since (matching source hash)."""
+    sources have not changed since (matching kernel hash)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     try:
         from quantized_swiglu_mlp_gb300 import build as qbuild
-        cur = qbuild.source_hash()
+        cur = qbuild.kernel_hash(kernel)
         with open(path) as f:
             for line in f:
                 kv = dict(t.split("=", 1) for t in line.split() if "=" in t)
@@ -275,6 +275,7 @@ def bench_decode(args, dev, stream, peaks, peak_src):
     ops.qsw_check_device_errors(stream)
     launches = counters[ops.CNT_FUSED_GEMV] + counters[ops.CNT_FUSED_TC]
     timed_launches = launches - args.warmup
+    streamed = counters[ops.CNT_GEMV_STREAM] == launches   # every call on the warp-streamed kernel
 
     # end to end through the public API with pinned host buffers
     x_host = torch.empty((1, case.H), dtype=torch.bfloat16, pin_memory=True)
@@ -316,6 +317,14 @@ def bench_decode(args, dev, stream, peaks, peak_src):
     iso_ms = time_graph(step, args.steps, args.warmup, stream)
     ops.qsw_set_early_weight_stream(args.early_weights)
 
+    # the same loop on the slot-ring small-M kernel, chained and call by call
+    ops.qsw_set_small_m_kernel(ops.SMALL_M_RING)
+    ring_ms = time_graph(step, args.steps, args.warmup, stream)
+    ops.qsw_set_early_weight_stream(False)
+    ring_iso_ms = time_graph(step, args.steps, args.warmup, stream)
+    ops.qsw_set_early_weight_stream(args.early_weights)
+    ops.qsw_set_small_m_kernel(ops.SMALL_M_AUTO)
+
     # the other variant of the same loop (F32 when the headline is MATCH)
     other = "f32" if args.variant == "match" else "match"
     ov = ops.VARIANTS[other]
@@ -331,13 +340,19 @@ def bench_decode(args, dev, stream, peaks, peak_src):
         e2e_ms=e2e_max_ms, e2e_bytes=e2e_bytes, clocks=clocks, launches=timed_launches,
         roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                   "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                  "traffic": read_traffic("gemv", "decode"), "peak_source": peak_src,
-                  "kernel": "gemv_kernel (small-M, mma.sync reduction)",
+                  "traffic": read_traffic("gemv_stream" if streamed else "gemv", "decode"),
+                  "peak_source": peak_src,
+                  "kernel": ("gemv_stream_kernel (warp-streamed small-M: per-warp cp.async rings, mma.sync)"
+                             if streamed else "gemv_kernel (slot-ring small-M: bulk copies, mma.sync)"),
                   "algorithmic_bytes_per_launch": algo_bytes},
         l2_bytes=l2,
         isolated={"us_per_call": round(iso_ms * 1e3 / args.steps, 3),
                   "weight_GBps": round(wbytes * args.steps / (iso_ms / 1e3) / 1e9, 1),
                   "mode": "early weight stream off: each call starts after the previous one ends"},
+        ring={"kernel": "gemv_kernel (slot-ring small-M)",
+              "us_per_call": round(ring_ms * 1e3 / args.steps, 3),
+              "us_per_call_isolated": round(ring_iso_ms * 1e3 / args.steps, 3),
+              "weight_GBps": round(wbytes * args.steps / (ring_ms / 1e3) / 1e9, 1)},
         other_variant={"variant": other, "us_per_call": round(other_ms * 1e3 / args.steps, 3),
                        "weight_GBps": round(wbytes * args.steps / (other_ms / 1e3) / 1e9, 1)})
 
@@ -493,10 +508,14 @@ def _bench_tiny(args, dev, stream):
     res = {}
     steps = 200
     try:
-        for name, limit in (("tiny_fused_small_m", 16), ("tiny_fused_tensor_core", 0)):
+        for name, limit, kernel in (("tiny_fused_small_m", 16, ops.SMALL_M_AUTO),
+                                    ("tiny_fused_small_m_ring", 16, ops.SMALL_M_RING),
+                                    ("tiny_fused_tensor_core", 0, ops.SMALL_M_AUTO)):
             ops.qsw_set_gemv_max_m(limit)
+            ops.qsw_set_small_m_kernel(kernel)
             ms = time_graph(lambda i: ops.qswiglu_forward(*a, variant=ops.MATCH, out=out, stream=stream), steps, 3,
                             stream)
+            ops.qsw_set_small_m_kernel(ops.SMALL_M_AUTO)
             res[name] = {"us_per_call": round(ms * 1e3 / steps, 2)}
         ops.qsw_set_gemv_max_m(saved)
 
@@ -554,6 +573,11 @@ def _bench_mixed_sweep(args, dev, stream):
     import torch
     from quantized_swiglu_mlp_gb300 import inputs, ops
 
+    # (entry, small-M limit, small-M kernel): the default small-M route, the
+    # slot-ring kernel where the warp-streamed one would serve (M <= 8), the
+    # tensor-core kernel
+    kernels = (("small_m", 32, ops.SMALL_M_AUTO), ("small_m_ring", 32, ops.SMALL_M_RING),
+               ("tensor_core", 0, ops.SMALL_M_AUTO))
     saved = ops.qsw_get_gemv_max_m()
     rows = []
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -567,20 +591,26 @@ def _bench_mixed_sweep(args, dev, stream):
                                  for _ in range(reps - 1)]
             out = torch.empty((M, case.I), dtype=torch.bfloat16, device=dev)
             entry = {"M": M}
-            for name, limit in (("small_m", 32), ("tensor_core", 0)):
-                if name == "small_m" and M > 32:
+            for name, limit, kernel in kernels:
+                if name != "tensor_core" and M > (8 if name == "small_m_ring" else 32):
                     continue
                 ops.qsw_set_gemv_max_m(limit)
+                ops.qsw_set_small_m_kernel(kernel)
                 steps = 200 if M <= 256 else 10
-                before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
+                before = ops.qsw_get_counters()
                 ms = time_graph(lambda i: ops.qswiglu_forward(base[0], *sets[i % len(sets)], variant=ops.MATCH,
                                                               out=out, stream=stream), steps, 3, stream)
-                if name == "small_m" and ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] == before:
-                    entry["small_m"] = "does not fit this shape's rows in shared memory (tensor-core kernel ran)"
+                after = ops.qsw_get_counters()
+                ops.qsw_set_small_m_kernel(ops.SMALL_M_AUTO)
+                if name != "tensor_core" and after[ops.CNT_FUSED_GEMV] == before[ops.CNT_FUSED_GEMV]:
+                    entry[name] = "does not fit this shape's rows in shared memory (tensor-core kernel ran)"
                     continue
                 us = ms * 1e3 / steps
                 entry[name] = {"us": round(us, 2), "weight_GBps": round(wbytes / us / 1e3, 1),
                                "tflops": round(4.0 * M * case.H * case.I / us / 1e6, 1)}
+                if name != "tensor_core":
+                    entry[name]["kernel"] = ("warp-streamed" if after[ops.CNT_GEMV_STREAM] > before[ops.CNT_GEMV_STREAM]
+                                             else "slot-ring")
             if isinstance(entry.get("small_m"), dict):
                 entry["faster"] = "small_m" if entry["small_m"]["us"] < entry["tensor_core"]["us"] else "tensor_core"
             rows.append(entry)
@@ -603,15 +633,23 @@ def _bench_mixed_sweep(args, dev, stream):
                                  for _ in range(reps - 1)]
             out = torch.empty((M, case.I), dtype=torch.bfloat16, device=dev)
             entry = {"M": M}
-            for name, limit in (("small_m", 32), ("tensor_core", 0)):
+            for name, limit, kernel in kernels:
+                if name == "small_m_ring" and M > 8:
+                    continue
                 ops.qsw_set_gemv_max_m(limit)
-                before = ops.qsw_get_counters()[ops.CNT_FUSED_GEMV]
+                ops.qsw_set_small_m_kernel(kernel)
+                before = ops.qsw_get_counters()
                 ms = time_graph(lambda i: ops.qswiglu_forward(base[0], *sets[i % len(sets)], variant=ops.MATCH,
                                                               out=out, stream=stream), 200, 3, stream)
-                if name == "small_m" and ops.qsw_get_counters()[ops.CNT_FUSED_GEMV] == before:
-                    entry["small_m"] = "does not fit"
+                after = ops.qsw_get_counters()
+                ops.qsw_set_small_m_kernel(ops.SMALL_M_AUTO)
+                if name != "tensor_core" and after[ops.CNT_FUSED_GEMV] == before[ops.CNT_FUSED_GEMV]:
+                    entry[name] = "does not fit"
                     continue
                 entry[name] = {"us": round(ms * 1e3 / 200, 2)}
+                if name != "tensor_core":
+                    entry[name]["kernel"] = ("warp-streamed" if after[ops.CNT_GEMV_STREAM] > before[ops.CNT_GEMV_STREAM]
+                                             else "slot-ring")
             cut.append(entry)
             del base, sets, out
             torch.cuda.empty_cache()
@@ -739,6 +777,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": 2 * 8192},
         "decode_isolated": d["isolated"],
         "decode_other_variant": d["other_variant"],
+        "decode_slot_ring": d["ring"],
         "gpu_launches": d["launches"] * world,
         "clocks": d["clocks"],
     }

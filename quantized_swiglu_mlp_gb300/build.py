@@ -36,16 +36,33 @@ def _flags(verbose_ptxas: bool) -> list[str]:
     return f
 
 
-def source_hash() -> str:
-    """Short hash of every source the library is built from (used to tell
-    whether a stored profile still describes the current kernels)."""
+# The sources each kernel is compiled from (for kernel_hash).
+KERNEL_SOURCES = {
+    "gemv_stream": ["qsw_gemv_stream.cu", "qsw_smallm.cuh", "qsw_device.cuh"],
+    "gemv": ["qsw_gemv.cu", "qsw_smallm.cuh", "qsw_device.cuh"],
+    "prefill": ["qsw_prefill.cu", "qsw_device.cuh"],
+}
+
+
+def _hash(names) -> str:
     import hashlib
     h = hashlib.sha256()
-    for name in sorted(SOURCES + HEADERS):
+    for name in sorted(names):
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:12]
+
+
+def source_hash() -> str:
+    """Short hash of every source the library is built from."""
+    return _hash(SOURCES + HEADERS)
+
+
+def kernel_hash(kernel: str) -> str:
+    """Short hash of the sources one kernel is compiled from (used to tell
+    whether a stored profile still describes that kernel)."""
+    return _hash(KERNEL_SOURCES[kernel])
 
 
 DEBUG_LIB_PATH = os.path.join(OUT_DIR, "libqswiglu_debug.so")

@@ -23,7 +23,8 @@
 //  * the lane dequantises its codes to the activation dtype T (w = T(s*q + b),
 //    one rounding) with the K order inside each 8-code group interleaved
 //    (codes j, j+4 paired); x is staged once per CTA in shared memory in the
-//    matching B-fragment order, all 8 fragment rows (rows >= M zero);
+//    matching B-fragment order (all 8 fragment rows for short x, its real
+//    rows only for long x);
 //  * scales and biases are read per block through L1; each warp requests the
 //    scale rows of its units into L1 when it starts;
 //  * each block accumulates in a fresh fragment that is added to the warp's
@@ -51,7 +52,6 @@ constexpr int kDepth = 3;                     // ring stages per warp
 constexpr int kBlockK = kSmallBlockK;         // codes per K block
 constexpr int kChunk = kSmallChunk;           // codes per lane per block
 constexpr int kSmemBudget = 200 * 1024;
-constexpr int kXBlockBytes = 4 * 32 * 16;     // B fragments of one block: 4 pieces x 32 lanes x 16 bytes
 constexpr int64_t kMaxK = 16384;              // the group-index multiply below is exact up to here
 
 __device__ unsigned int g_gemv_stream_error;
@@ -67,6 +67,7 @@ struct StreamParams {
   uint16_t *out;
   const uint16_t *res;    // single-operand form: [M, N] added before the rounding (or null)
   int nkb;                // K blocks per row
+  int x_rows;             // rows of x staged per block: 8 (rows >= M as zeros) or min(M, 8)
   int uq, ur;             // CTA b has uq + (b < ur) units, starting at b * uq + min(b, ur)
   int slots;              // partial-sum slots per warp
   int red_off, ring_off, tab_off;   // byte offsets of the partial sums, the rings, the warp tables
@@ -136,7 +137,9 @@ __device__ __forceinline__ void read_chunk(uint32_t (&w)[BITS], uint32_t src) {
   }
 }
 
-template <int BITS0, int BITS1, bool DUAL, class A>
+// XF: all 8 fragment rows of x are staged (p.x_rows == 8), so the staging
+// layout is a compile-time constant.
+template <int BITS0, int BITS1, bool DUAL, bool XF, class A>
 __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamParams p) {
   constexpr int BB = DUAL ? BITS1 : BITS0;
   constexpr int SB = stage_bytes<BITS0, BITS1, DUAL>();
@@ -166,8 +169,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   }
 
   // x of a non-dependent launch is requested first: behind the weight stream
-  // it would arrive microseconds later
-  const int x_total = nkb * 32;   // (block, lane) pieces of 64 bytes
+  // it would arrive microseconds later.  Lane L = 4n + c carries row n of x.
+  // Where x is short all 8 fragment rows are staged (rows >= M as zeros: the
+  // fastest reads); for long x only its min(M, 8) real rows are, and a lane of
+  // a row n >= M reads the fragment of lane L mod (4 min(M, 8)) instead: B
+  // column n of the MMA then holds another row's values, which only affects
+  // output column n, and columns n >= M are never stored.
+  const int x_lanes = XF ? 32 : 4 * p.x_rows;
+  const uint32_t x_piece = static_cast<uint32_t>(x_lanes) * 16;   // bytes of one (block, j) piece
+  const int x_total = nkb * 32;   // (block, lane) entries of 64 bytes; lanes >= x_lanes are not staged
   auto load_x = [&](int e, uint4 (&xv)[4]) {
     const int L = e & 31, kb = e >> 5;
     const int m = L >> 2;
@@ -182,16 +192,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
     }
   };
   // For block kb and fragment piece j (x values 8j..8j+7 of each lane's chunk),
-  // lane L = 4n + c's 16 bytes sit at (kb*4 + j)*512 + L*16: row n of x (zero
-  // for n >= M), codes kb*128 + 32c + 8j ... + 7 permuted into (x0,x4)
-  // (x1,x5) (x2,x6) (x3,x7) pairs.
+  // lane L = 4n + c's 16 bytes sit at (kb*4 + j)*x_piece + L*16: row n of x,
+  // codes kb*128 + 32c + 8j ... + 7 permuted into (x0,x4) (x1,x5) (x2,x6)
+  // (x3,x7) pairs.
   auto store_x = [&](int e, const uint4 (&xv)[4]) {
-    uint8_t *dst = smem + static_cast<size_t>(e >> 5) * kXBlockBytes + (e & 31) * 16;
+    uint8_t *dst = smem + static_cast<size_t>(e >> 5) * 4 * x_piece + (e & 31) * 16;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(dst + j * 512) = x_fragment(xv[j]);
+    for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4 *>(dst + j * x_piece) = x_fragment(xv[j]);
   };
   uint4 x_first[4];
-  const bool has_x = static_cast<int>(threadIdx.x) < x_total;
+  const bool has_x = static_cast<int>(threadIdx.x) < x_total && static_cast<int>(threadIdx.x & 31) < x_lanes;
   if (!p.early && has_x) load_x(threadIdx.x, x_first);
 
   // --- warp tables for the final reduction, and the scale rows into L1 ---
@@ -270,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   }
   if (has_x) store_x(threadIdx.x, x_first);
   for (int e = threadIdx.x + kThreads; e < x_total; e += kThreads) {
+    if ((e & 31) >= x_lanes) continue;
     uint4 xv[4];
     load_x(e, xv);
     store_x(e, xv);
@@ -277,10 +288,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   __syncthreads();
 
   // --- the warp's blocks ---
-  const uint32_t xbase = smem_u32(smem) + lane * 16;
+  const uint32_t xstep = x_piece;
+  const uint32_t xbase = smem_u32(smem) + (XF ? lane : lane % x_lanes) * 16;
   float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   int cu = u_first, ckb = i_begin - u_first * nkb;
-  uint32_t xb = xbase + static_cast<uint32_t>(ckb) * kXBlockBytes;
+  uint32_t xb = xbase + static_cast<uint32_t>(ckb) * 4 * xstep;
   int c_row = 8 * (u_begin + u_first) + g;
   uint32_t ck = static_cast<uint32_t>(ckb) * kBlockK + c * kChunk;
   int64_t so0 = static_cast<int64_t>(c_row) * p.ng0, so1 = static_cast<int64_t>(c_row) * p.ng1;
@@ -327,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
       uint32_t pa4[4], pb4[4] = {0u, 0u, 0u, 0u};
       ca.dequant(j, sa2, ba2, pa4);
       if constexpr (DUAL) cb.dequant(j, sb2, bb2, pb4);
-      const uint4 xf = lds128(xb + j * 512);
+      const uint4 xf = lds128(xb + j * xstep);
       // A rows g and g+8; k_local 2c,2c+1 <- pair 2h, k_local 2c+8,2c+9 <- pair 2h+1
       const uint32_t a0[4] = {pa4[0], pb4[0], pa4[1], pb4[1]};
       const uint32_t a1[4] = {pa4[2], pb4[2], pa4[3], pb4[3]};
@@ -339,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
     // the stage is read: refill it with the block kDepth items on
     cs = cs + SB == kDepth * SB ? 0 : cs + SB;
     issue_next();
-    xb += kXBlockBytes;
+    xb += 4 * xstep;
     ck += kBlockK;
     if (++ckb == nkb) {   // the unit's last block: its partial sum is complete
       flush();
@@ -395,6 +407,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   }
 }
 
+// Rows of x staged per block: all 8 fragment rows while they take at most
+// 48 KB (K <= 3072), else only the real ones (so that two CTAs, e.g. of a
+// decode block's expansion and down projection, still fit on an SM).
+int64_t stream_x_rows(int64_t M, int64_t K) {
+  const int64_t nkb = (K + kBlockK - 1) / kBlockK;
+  return nkb * 4 * 8 * 64 <= 48 * 1024 ? 8 : (M < 8 ? M : 8);
+}
+
 struct StreamLayout {
   int red_off, ring_off, tab_off, slots, total;
 };
@@ -410,7 +430,7 @@ StreamLayout stream_plan(int64_t M, int64_t K, int64_t N, int num_sms, int stage
   const int64_t ipw = (ucta * nkb + kWarps - 1) / kWarps;      // most items of a warp
   int64_t slots = (ipw + nkb - 1) / nkb + 1;                  // units a contiguous item range can touch
   if (slots > ucta) slots = ucta;
-  const int64_t x_bytes = nkb * kXBlockBytes;
+  const int64_t x_bytes = (nkb * 4 * stream_x_rows(M, K) * 64 + 127) / 128 * 128;
   const int64_t red_bytes = kWarps * slots * 512;
   const int64_t ring_bytes = static_cast<int64_t>(kWarps) * kDepth * stage;
   const int64_t tab_bytes = (kWarps + ucta + 1) * 4;
@@ -429,22 +449,13 @@ int stage_of(int bits0, int bits1, bool dual) {
   return chunk(bits0) + (dual ? chunk(bits1) : 0);
 }
 
-template <int BITS0, int BITS1, bool DUAL, class A>
-cudaError_t launch_cfg(StreamParams p, const StreamLayout &l, cudaStream_t stream, int num_sms) {
-  const int units = (p.N + 7) / 8;
-  const int grid = units < num_sms ? units : num_sms;
-  p.nkb = (p.K + kBlockK - 1) / kBlockK;
-  p.uq = units / grid;
-  p.ur = units % grid;
-  p.slots = l.slots;
-  p.red_off = l.red_off;
-  p.ring_off = l.ring_off;
-  p.tab_off = l.tab_off;
+template <int BITS0, int BITS1, bool DUAL, bool XF, class A>
+cudaError_t launch_x(const StreamParams &p, const StreamLayout &l, int grid, cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(attr_done.load() & (uint64_t(1) << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<BITS0, BITS1, DUAL, A>,
+    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<BITS0, BITS1, DUAL, XF, A>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(uint64_t(1) << dev);
@@ -459,8 +470,24 @@ cudaError_t launch_cfg(StreamParams p, const StreamLayout &l, cudaStream_t strea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.early ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BITS0, BITS1, DUAL, A>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BITS0, BITS1, DUAL, XF, A>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int BITS0, int BITS1, bool DUAL, class A>
+cudaError_t launch_cfg(StreamParams p, const StreamLayout &l, cudaStream_t stream, int num_sms) {
+  const int units = (p.N + 7) / 8;
+  const int grid = units < num_sms ? units : num_sms;
+  p.nkb = (p.K + kBlockK - 1) / kBlockK;
+  p.x_rows = static_cast<int>(stream_x_rows(p.M, p.K));
+  p.uq = units / grid;
+  p.ur = units % grid;
+  p.slots = l.slots;
+  p.red_off = l.red_off;
+  p.ring_off = l.ring_off;
+  p.tab_off = l.tab_off;
+  return p.x_rows == 8 ? launch_x<BITS0, BITS1, DUAL, true, A>(p, l, grid, stream)
+                       : launch_x<BITS0, BITS1, DUAL, false, A>(p, l, grid, stream);
 }
 
 template <int BITS0, class A>
