@@ -574,7 +574,7 @@ def _bench_mixed_sweep(args, dev, stream):
     from quantized_swiglu_mlp_gb300 import inputs, ops
 
     # (entry, small-M limit, small-M kernel): the default small-M route, the
-    # slot-ring kernel where the warp-streamed one would serve (M <= 8), the
+    # slot-ring kernel where the warp-streamed one would serve (M <= 16), the
     # tensor-core kernel
     kernels = (("small_m", 32, ops.SMALL_M_AUTO), ("small_m_ring", 32, ops.SMALL_M_RING),
                ("tensor_core", 0, ops.SMALL_M_AUTO))
@@ -592,7 +592,7 @@ def _bench_mixed_sweep(args, dev, stream):
             out = torch.empty((M, case.I), dtype=torch.bfloat16, device=dev)
             entry = {"M": M}
             for name, limit, kernel in kernels:
-                if name != "tensor_core" and M > (8 if name == "small_m_ring" else 32):
+                if name != "tensor_core" and M > (16 if name == "small_m_ring" else 32):
                     continue
                 ops.qsw_set_gemv_max_m(limit)
                 ops.qsw_set_small_m_kernel(kernel)
@@ -634,7 +634,7 @@ def _bench_mixed_sweep(args, dev, stream):
             out = torch.empty((M, case.I), dtype=torch.bfloat16, device=dev)
             entry = {"M": M}
             for name, limit, kernel in kernels:
-                if name == "small_m_ring" and M > 8:
+                if name == "small_m_ring" and M > 16:
                     continue
                 ops.qsw_set_gemv_max_m(limit)
                 ops.qsw_set_small_m_kernel(kernel)

@@ -271,7 +271,7 @@ QSW_API int qsw_get_gemv_max_m(void);
 
 /* Which small-M kernel serves a call routed to the small-M path. */
 typedef enum {
-    QSW_SMALL_M_AUTO = 0,   /* the warp-streamed kernel where it applies (M <= 8, H <= 16384 and its
+    QSW_SMALL_M_AUTO = 0,   /* the warp-streamed kernel where it applies (M <= 16, H <= 16384 and its
                                staging fits in shared memory), else the slot-ring kernel (default) */
     QSW_SMALL_M_RING = 1,   /* always the slot-ring kernel (bulk copies into shared-memory slots
                                shared by a CTA's warps) */

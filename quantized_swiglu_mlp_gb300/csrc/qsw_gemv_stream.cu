@@ -1,4 +1,4 @@
-// Warp-streamed small-M kernel (M <= 8): the fused SwiGLU expansion and the
+// Warp-streamed small-M kernel (M <= 16): the fused SwiGLU expansion and the
 // single quantised linear, for decode-sized batches.
 //
 // Method: mlx-bun pages, src/model/fused-swiglu-kernel.ts -- at decode the two
@@ -10,7 +10,9 @@
 //  * unit of work: 8 output features.  Fused: A rows 0..7 of mma.sync
 //    m16n8k16 are gate rows, rows 8..15 the up rows of the same features, so
 //    one MMA yields both projections; single linear: rows 8..15 are zero.
-//    CTA b takes a contiguous range of units (sizes differ by at most one);
+//    With M > 8, x has two row groups of 8 and every dequantised A fragment
+//    feeds one MMA per group.  CTA b takes a contiguous range of units (sizes
+//    differ by at most one);
 //    the CTA's (unit, 128-code K block) items, unit-major, are cut into one
 //    contiguous range per warp, so a warp runs many consecutive blocks between
 //    synchronisations and the only CTA barriers are "x staged" and "partials
@@ -33,9 +35,10 @@
 //    the unit's partials in warp order (deterministic), every lane its own
 //    accumulator registers, and applies the epilogue.
 //
-// Two CTAs fit on an SM (at most 64 registers per thread, about 100 KB of
-// shared memory at decode sizes), so with the early weight stream the next
-// call's CTAs start and request their first blocks while this call computes.
+// With one row group two CTAs fit on an SM (at most 64 registers per thread,
+// about 100 KB of shared memory at decode sizes), so with the early weight
+// stream the next call's CTAs start and request their first blocks while this
+// call computes.
 // The kernel has no spin waits: cp.async.wait_group waits for the thread's own
 // copies, which always complete.
 #include <atomic>
@@ -137,10 +140,11 @@ __device__ __forceinline__ void read_chunk(uint32_t (&w)[BITS], uint32_t src) {
   }
 }
 
-// XF: all 8 fragment rows of x are staged (p.x_rows == 8), so the staging
-// layout is a compile-time constant.
-template <int BITS0, int BITS1, bool DUAL, bool XF, class A>
-__global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamParams p) {
+// XF: all 8 fragment rows of each x row group are staged (p.x_rows == 8 * NG),
+// so the staging layout is a compile-time constant.  NG: x row groups of 8
+// (M <= 8: 1; M <= 16: 2, which share every dequantised A fragment).
+template <int BITS0, int BITS1, bool DUAL, bool XF, int NG, class A>
+__global__ void __launch_bounds__(kThreads, NG == 1 ? 2 : 1) gemv_stream_kernel(const StreamParams p) {
   constexpr int BB = DUAL ? BITS1 : BITS0;
   constexpr int SB = stage_bytes<BITS0, BITS1, DUAL>();
   extern __shared__ __align__(128) uint8_t smem[];
@@ -176,11 +180,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   // column n of the MMA then holds another row's values, which only affects
   // output column n, and columns n >= M are never stored.
   const int x_lanes = XF ? 32 : 4 * p.x_rows;
-  const uint32_t x_piece = static_cast<uint32_t>(x_lanes) * 16;   // bytes of one (block, j) piece
-  const int x_total = nkb * 32;   // (block, lane) entries of 64 bytes; lanes >= x_lanes are not staged
+  const uint32_t x_piece = static_cast<uint32_t>(x_lanes) * 16;   // bytes of one (block, group, j) piece
+  const int x_total = nkb * NG * 32;   // (block, group, lane) entries of 64 bytes; lanes >= x_lanes are not staged
   auto load_x = [&](int e, uint4 (&xv)[4]) {
-    const int L = e & 31, kb = e >> 5;
-    const int m = L >> 2;
+    const int L = e & 31, kb = (e >> 5) / NG;
+    const int m = 8 * ((e >> 5) % NG) + (L >> 2);
     const uint32_t k = static_cast<uint32_t>(kb) * kBlockK + (L & 3) * kChunk;
     if (k < K && m < p.M) {
       const uint4 *xp = reinterpret_cast<const uint4 *>(p.x + static_cast<int64_t>(m) * p.K + k);
@@ -191,10 +195,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
       for (int q = 0; q < 4; ++q) xv[q] = make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  // For block kb and fragment piece j (x values 8j..8j+7 of each lane's chunk),
-  // lane L = 4n + c's 16 bytes sit at (kb*4 + j)*x_piece + L*16: row n of x,
-  // codes kb*128 + 32c + 8j ... + 7 permuted into (x0,x4) (x1,x5) (x2,x6)
-  // (x3,x7) pairs.
+  // For block kb, row group G and fragment piece j (x values 8j..8j+7 of each
+  // lane's chunk), lane L = 4n + c's 16 bytes sit at ((kb*NG + G)*4 + j)*x_piece
+  // + L*16: row 8G + n of x, codes kb*128 + 32c + 8j ... + 7 permuted into
+  // (x0,x4) (x1,x5) (x2,x6) (x3,x7) pairs.
   auto store_x = [&](int e, const uint4 (&xv)[4]) {
     uint8_t *dst = smem + static_cast<size_t>(e >> 5) * 4 * x_piece + (e & 31) * 16;
 #pragma unroll
@@ -290,9 +294,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   // --- the warp's blocks ---
   const uint32_t xstep = x_piece;
   const uint32_t xbase = smem_u32(smem) + (XF ? lane : lane % x_lanes) * 16;
-  float sum[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float sum[NG][4];
+#pragma unroll
+  for (int G = 0; G < NG; ++G)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) sum[G][q] = 0.0f;
   int cu = u_first, ckb = i_begin - u_first * nkb;
-  uint32_t xb = xbase + static_cast<uint32_t>(ckb) * 4 * xstep;
+  uint32_t xb = xbase + static_cast<uint32_t>(ckb) * NG * 4 * xstep;
   int c_row = 8 * (u_begin + u_first) + g;
   uint32_t ck = static_cast<uint32_t>(ckb) * kBlockK + c * kChunk;
   int64_t so0 = static_cast<int64_t>(c_row) * p.ng0, so1 = static_cast<int64_t>(c_row) * p.ng1;
@@ -300,8 +308,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   auto flush = [&]() {
     const int t = cu - u_first;
     debug_check(t >= 0 && t < p.slots, err);
-    *reinterpret_cast<float4 *>(red + ((warp * p.slots + t) * 32 + lane) * 4) =
-        make_float4(sum[0], sum[1], sum[2], sum[3]);
+#pragma unroll
+    for (int G = 0; G < NG; ++G)
+      *reinterpret_cast<float4 *>(red + (((warp * p.slots + t) * NG + G) * 32 + lane) * 4) =
+          make_float4(sum[G][0], sum[G][1], sum[G][2], sum[G][3]);
   };
   // the next block's scales and biases (through L1, one block ahead of their
   // use), zero past N or K
@@ -333,30 +343,41 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
     // (a lane past N or K reads stale stage bytes: with scale and bias 0 they dequantise to 0)
     const uint32_t sa2 = sa * 0x00010001u, ba2 = ba * 0x00010001u;
     const uint32_t sb2 = sb * 0x00010001u, bb2 = bb * 0x00010001u;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float acc[NG][4];
+#pragma unroll
+    for (int G = 0; G < NG; ++G)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[G][q] = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       uint32_t pa4[4], pb4[4] = {0u, 0u, 0u, 0u};
       ca.dequant(j, sa2, ba2, pa4);
       if constexpr (DUAL) cb.dequant(j, sb2, bb2, pb4);
-      const uint4 xf = lds128(xb + j * xstep);
       // A rows g and g+8; k_local 2c,2c+1 <- pair 2h, k_local 2c+8,2c+9 <- pair 2h+1
       const uint32_t a0[4] = {pa4[0], pb4[0], pa4[1], pb4[1]};
       const uint32_t a1[4] = {pa4[2], pb4[2], pa4[3], pb4[3]};
-      mma_16816<A>(acc, a0, xf.x, xf.y);
-      mma_16816<A>(acc, a1, xf.z, xf.w);
+#pragma unroll
+      for (int G = 0; G < NG; ++G) {
+        const uint4 xf = lds128(xb + (G * 4 + j) * xstep);
+        mma_16816<A>(acc[G], a0, xf.x, xf.y);
+        mma_16816<A>(acc[G], a1, xf.z, xf.w);
+      }
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) sum[q] += acc[q];
+    for (int G = 0; G < NG; ++G)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sum[G][q] += acc[G][q];
     // the stage is read: refill it with the block kDepth items on
     cs = cs + SB == kDepth * SB ? 0 : cs + SB;
     issue_next();
-    xb += 4 * xstep;
+    xb += NG * 4 * xstep;
     ck += kBlockK;
     if (++ckb == nkb) {   // the unit's last block: its partial sum is complete
       flush();
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sum[q] = 0.0f;
+      for (int G = 0; G < NG; ++G)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sum[G][q] = 0.0f;
       ckb = 0;
       ++cu;
       xb = xbase;
@@ -374,43 +395,56 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_stream_kernel(const StreamPa
   // --- partial sums of each unit, in warp order, then the epilogue ---
   // The warp that holds a unit's last block finishes it: lane (g, c) adds the
   // partials of its own accumulator registers (A rows g and g+8, x columns 2c
-  // and 2c+1) over the unit's warps in warp order and applies the epilogue to
-  // its outputs (i = 8u + g, m = 2c and 2c+1).
+  // and 2c+1 of each row group G) over the unit's warps in warp order and
+  // applies the epilogue to its outputs (i = 8u + g, m = 8G + 2c and 8G + 2c + 1).
   if (i_begin < i_end) {
     const int u_last = (i_end - 1) / nkb;
     for (int u = u_first; u <= u_last; ++u) {
       if ((u + 1) * nkb - 1 >= i_end) continue;   // the unit ends in a later warp's range
-      float4 s4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      float4 s4[NG];
+#pragma unroll
+      for (int G = 0; G < NG; ++G) s4[G] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       for (int w = wfirst_tab[u]; w <= warp; ++w) {
         const int uf = ufirst_tab[w];
         if (uf < 0) continue;   // no items
         const int t = u - uf;
         debug_check(t >= 0 && t < p.slots, err);
-        const float4 v = *reinterpret_cast<const float4 *>(red + ((w * p.slots + t) * 32 + lane) * 4);
-        s4.x += v.x;
-        s4.y += v.y;
-        s4.z += v.z;
-        s4.w += v.w;
+#pragma unroll
+        for (int G = 0; G < NG; ++G) {
+          const float4 v = *reinterpret_cast<const float4 *>(red + (((w * p.slots + t) * NG + G) * 32 + lane) * 4);
+          s4[G].x += v.x;
+          s4[G].y += v.y;
+          s4[G].z += v.z;
+          s4[G].w += v.w;
+        }
       }
       const int64_t i_out = static_cast<int64_t>(u_begin + u) * 8 + g;
       if (i_out >= p.N) continue;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int m = 2 * c + q;
-        if (m >= p.M) break;
-        const float gv = q ? s4.y : s4.x, uv = q ? s4.w : s4.z;
-        const int64_t o = static_cast<int64_t>(m) * p.N + i_out;
-        const float v = DUAL ? swiglu_epilogue<A>(p.variant, gv, uv) : (p.res ? gv + A::lo(p.res[o]) : gv);
-        p.out[o] = A::store(v);
+      for (int G = 0; G < NG; ++G) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int m = 8 * G + 2 * c + q;
+          if (m >= p.M) break;
+          const float gv = q ? s4[G].y : s4[G].x, uv = q ? s4[G].w : s4[G].z;
+          const int64_t o = static_cast<int64_t>(m) * p.N + i_out;
+          const float v = DUAL ? swiglu_epilogue<A>(p.variant, gv, uv) : (p.res ? gv + A::lo(p.res[o]) : gv);
+          p.out[o] = A::store(v);
+        }
       }
     }
   }
 }
 
-// Rows of x staged per block: all 8 fragment rows while they take at most
-// 48 KB (K <= 3072), else only the real ones (so that two CTAs, e.g. of a
-// decode block's expansion and down projection, still fit on an SM).
+// x row groups of 8: one for M <= 8, two for M <= 16.
+int stream_groups(int64_t M) { return M > 8 ? 2 : 1; }
+
+// Rows of x staged per block: with one row group, all 8 fragment rows while
+// they take at most 48 KB (K <= 3072), else only the real ones (so that two
+// CTAs, e.g. of a decode block's expansion and down projection, still fit on
+// an SM); with two row groups, all 16.
 int64_t stream_x_rows(int64_t M, int64_t K) {
+  if (stream_groups(M) == 2) return 16;
   const int64_t nkb = (K + kBlockK - 1) / kBlockK;
   return nkb * 4 * 8 * 64 <= 48 * 1024 ? 8 : (M < 8 ? M : 8);
 }
@@ -422,7 +456,8 @@ struct StreamLayout {
 // Shared-memory layout; total == 0 when the shape does not fit.
 StreamLayout stream_plan(int64_t M, int64_t K, int64_t N, int num_sms, int stage) {
   StreamLayout l{};
-  if (M < 1 || M > 8 || K > kMaxK || num_sms < 1) return l;
+  if (M < 1 || M > 16 || K > kMaxK || num_sms < 1) return l;
+  const int64_t ng = stream_groups(M);
   const int64_t nkb = (K + kBlockK - 1) / kBlockK;
   const int64_t units = (N + 7) / 8;
   const int64_t grid = units < num_sms ? units : num_sms;
@@ -431,7 +466,7 @@ StreamLayout stream_plan(int64_t M, int64_t K, int64_t N, int num_sms, int stage
   int64_t slots = (ipw + nkb - 1) / nkb + 1;                  // units a contiguous item range can touch
   if (slots > ucta) slots = ucta;
   const int64_t x_bytes = (nkb * 4 * stream_x_rows(M, K) * 64 + 127) / 128 * 128;
-  const int64_t red_bytes = kWarps * slots * 512;
+  const int64_t red_bytes = kWarps * slots * 512 * ng;
   const int64_t ring_bytes = static_cast<int64_t>(kWarps) * kDepth * stage;
   const int64_t tab_bytes = (kWarps + ucta + 1) * 4;
   const int64_t total = x_bytes + red_bytes + ring_bytes + tab_bytes;
@@ -449,13 +484,13 @@ int stage_of(int bits0, int bits1, bool dual) {
   return chunk(bits0) + (dual ? chunk(bits1) : 0);
 }
 
-template <int BITS0, int BITS1, bool DUAL, bool XF, class A>
+template <int BITS0, int BITS1, bool DUAL, bool XF, int NG, class A>
 cudaError_t launch_x(const StreamParams &p, const StreamLayout &l, int grid, cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(attr_done.load() & (uint64_t(1) << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<BITS0, BITS1, DUAL, XF, A>,
+    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<BITS0, BITS1, DUAL, XF, NG, A>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(uint64_t(1) << dev);
@@ -470,7 +505,7 @@ cudaError_t launch_x(const StreamParams &p, const StreamLayout &l, int grid, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.early ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BITS0, BITS1, DUAL, XF, A>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BITS0, BITS1, DUAL, XF, NG, A>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -486,8 +521,9 @@ cudaError_t launch_cfg(StreamParams p, const StreamLayout &l, cudaStream_t strea
   p.red_off = l.red_off;
   p.ring_off = l.ring_off;
   p.tab_off = l.tab_off;
-  return p.x_rows == 8 ? launch_x<BITS0, BITS1, DUAL, true, A>(p, l, grid, stream)
-                       : launch_x<BITS0, BITS1, DUAL, false, A>(p, l, grid, stream);
+  if (p.x_rows == 16) return launch_x<BITS0, BITS1, DUAL, true, 2, A>(p, l, grid, stream);
+  return p.x_rows == 8 ? launch_x<BITS0, BITS1, DUAL, true, 1, A>(p, l, grid, stream)
+                       : launch_x<BITS0, BITS1, DUAL, false, 1, A>(p, l, grid, stream);
 }
 
 template <int BITS0, class A>

@@ -38,13 +38,13 @@ cudaError_t launch_gemv(const void *x, int64_t M, int64_t K, int64_t N, const Qu
 // that the waits on it run out.
 void gemv_withhold_next();
 
-// Warp-streamed small-M kernel (M <= 8): same arguments and result as
+// Warp-streamed small-M kernel (M <= 16): same arguments and result as
 // launch_gemv; it has no spin waits.
 cudaError_t launch_gemv_stream(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
                                const QuantOperand *op1, int variant, int act, void *out, const void *residual,
                                cudaStream_t stream, int num_sms, bool early_weights);
 
-// Whether the warp-streamed kernel applies (M <= 8, K <= 16384, x, the
+// Whether the warp-streamed kernel applies (M <= 16, K <= 16384, x, the
 // partial sums and the warps' rings fit in shared memory).
 bool gemv_stream_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const QuantOperand *op1,
                       int num_sms);

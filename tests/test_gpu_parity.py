@@ -44,19 +44,19 @@ def small_m_kernel():
 
 
 # the two small-M kernels: slot ring (bulk copies into CTA-shared slots) and
-# warp-streamed (M <= 8)
+# warp-streamed (M <= 16)
 SMALL_M_KERNELS = [ops.SMALL_M_RING, ops.SMALL_M_STREAM]
 KNAMES = {ops.SMALL_M_RING: "ring", ops.SMALL_M_STREAM: "stream"}
 
 
 def expect_small_m(before, kernel, M, counter=None):
     """The call(s) since `before` ran on the small-M path, on the selected
-    kernel (the warp-streamed one serves M <= 8)."""
+    kernel (the warp-streamed one serves M <= 16 at these shapes)."""
     after = ops.qsw_get_counters()
     if counter is not None:
         assert after[counter] > before[counter]
     reg = after[ops.CNT_GEMV_STREAM] > before[ops.CNT_GEMV_STREAM]
-    assert reg == (kernel == ops.SMALL_M_STREAM and M <= 8), (kernel, M)
+    assert reg == (kernel == ops.SMALL_M_STREAM and M <= 16), (kernel, M)
 
 
 def check(variant, got, want, dtype="bf16"):
@@ -184,6 +184,8 @@ MORE_SMALL_M_SHAPES = [
     (2, 4096, 3000, 2, 64, 4, 128),    # 2-bit gate, 32 K blocks per unit
     (5, 256, 17, 8, 32, 8, 32),        # 3 units, 2 K blocks: most warps idle
     (3, 2560, 10240, 4, 64, 8, 32),    # the mixed-spec workload's specs
+    (16, 1024, 2000, 4, 64, 8, 32),    # two x row groups, mixed specs
+    (13, 2048, 1203, 2, 64, 4, 64),    # two x row groups, odd M, 2-bit gate, ragged last unit
 ]
 
 
@@ -201,7 +203,7 @@ def test_small_m_kernel_more_shapes(dev, gemv_limit, small_m_kernel, kernel, sha
 
 
 @pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
-@pytest.mark.parametrize("M,K,N", [(1, 2048, 1000), (3, 1024, 203), (8, 512, 40), (2, 8192, 2048)])
+@pytest.mark.parametrize("M,K,N", [(1, 2048, 1000), (3, 1024, 203), (8, 512, 40), (2, 8192, 2048), (12, 2048, 520)])
 @pytest.mark.parametrize("with_residual", [False, True], ids=["plain", "residual"])
 def test_small_m_single_operand(dev, gemv_limit, small_m_kernel, kernel, M, K, N, with_residual):
     """affine_qmm on the small-M kernels (ragged units), with and without a
