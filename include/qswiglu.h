@@ -264,15 +264,16 @@ QSW_API qsw_status qsw_check_device_errors(void *stream);
  * qsw_check_device_errors() without trapping.  0 in the regular build. */
 QSW_API int qsw_debug_build(void);
 
-/* Largest M routed to the small-M kernel (default 16; 0 sends every M to the
+/* Largest M routed to the small-M kernels (default 32; 0 sends every M to the
  * tensor-core kernel).  Values above 32 are clamped to 32.  Process-wide. */
 QSW_API void qsw_set_gemv_max_m(int m);
 QSW_API int qsw_get_gemv_max_m(void);
 
 /* Which small-M kernel serves a call routed to the small-M path. */
 typedef enum {
-    QSW_SMALL_M_AUTO = 0,   /* the warp-streamed kernel where it applies (M <= 16, H <= 16384 and its
-                               staging fits in shared memory), else the slot-ring kernel (default) */
+    QSW_SMALL_M_AUTO = 0,   /* the warp-streamed kernel where it applies (H <= 16384 and its staging
+                               fits in shared memory; M > 16 runs as launches over row chunks of 16,
+                               each streaming the weights once), else the slot-ring kernel (default) */
     QSW_SMALL_M_RING = 1,   /* always the slot-ring kernel (bulk copies into shared-memory slots
                                shared by a CTA's warps) */
     QSW_SMALL_M_STREAM = 2  /* the warp-streamed kernel where it applies (each warp copies its own

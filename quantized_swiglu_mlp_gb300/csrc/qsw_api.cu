@@ -31,7 +31,7 @@ std::atomic<int> g_small_m_kernel{QSW_SMALL_M_AUTO};
 int gemv_max_m() {
   int v = g_gemv_max_m.load(std::memory_order_relaxed);
   if (v < 0) {
-    int init = 16;
+    int init = 32;
     if (const char *env = std::getenv("QSW_GEMV_MAX_M")) init = std::atoi(env);
     if (init < 0) init = 0;
     if (init > qsw::kGemvMaxM) init = static_cast<int>(qsw::kGemvMaxM);

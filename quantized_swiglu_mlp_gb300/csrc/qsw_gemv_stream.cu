@@ -1,5 +1,6 @@
-// Warp-streamed small-M kernel (M <= 16): the fused SwiGLU expansion and the
-// single quantised linear, for decode-sized batches.
+// Warp-streamed small-M kernel (M <= 16 per launch; up to 32 rows as launches
+// over row chunks of 16): the fused SwiGLU expansion and the single quantised
+// linear, for decode-sized batches.
 //
 // Method: mlx-bun pages, src/model/fused-swiglu-kernel.ts -- at decode the two
 // projections are weight-streaming GEMVs.  Measured on this GPU, such a call
@@ -562,15 +563,24 @@ uint32_t group_magic(int gs) {
 
 }  // namespace
 
+// Rows of x one launch takes; more rows run as consecutive launches over
+// row chunks of this size, each streaming the weights once.
+constexpr int64_t kStreamChunk = 16;
+
 bool gemv_stream_fits(int64_t M, int64_t K, int64_t N, const QuantOperand &op0, const QuantOperand *op1,
                       int num_sms) {
   const QuantOperand &o1 = op1 ? *op1 : op0;
-  return stream_plan(M, K, N, num_sms, stage_of(op0.bits, o1.bits, op1 != nullptr)).total > 0;
+  if (M < 1 || M > kGemvMaxM) return false;
+  const int64_t mc = M < kStreamChunk ? M : kStreamChunk;
+  return stream_plan(mc, K, N, num_sms, stage_of(op0.bits, o1.bits, op1 != nullptr)).total > 0 &&
+         stream_plan(1, K, N, num_sms, stage_of(op0.bits, o1.bits, op1 != nullptr)).total > 0;
 }
 
-cudaError_t launch_gemv_stream(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
-                               const QuantOperand *op1, int variant, int act, void *out, const void *residual,
-                               cudaStream_t stream, int num_sms, bool early_weights) {
+namespace {
+
+cudaError_t launch_chunk(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
+                         const QuantOperand *op1, int variant, int act, void *out, const void *residual,
+                         cudaStream_t stream, int num_sms, bool early_weights) {
   const QuantOperand &o1 = op1 ? *op1 : op0;
   const StreamLayout l = stream_plan(M, K, N, num_sms, stage_of(op0.bits, o1.bits, op1 != nullptr));
   if (l.total == 0) return cudaErrorInvalidValue;
@@ -596,6 +606,24 @@ cudaError_t launch_gemv_stream(const void *x, int64_t M, int64_t K, int64_t N, c
   if (act == ActF16::kId) return launch_act<ActF16>(p, l, op0.bits, o1.bits, op1 != nullptr, stream, num_sms);
   if (act == ActBf16::kId) return launch_act<ActBf16>(p, l, op0.bits, o1.bits, op1 != nullptr, stream, num_sms);
   return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_stream(const void *x, int64_t M, int64_t K, int64_t N, const QuantOperand &op0,
+                               const QuantOperand *op1, int variant, int act, void *out, const void *residual,
+                               cudaStream_t stream, int num_sms, bool early_weights) {
+  if (!gemv_stream_fits(M, K, N, op0, op1, num_sms)) return cudaErrorInvalidValue;
+  // rows [m0, m0 + mc) of x, of the output and of the residual (row-major, 2-byte elements)
+  for (int64_t m0 = 0; m0 < M; m0 += kStreamChunk) {
+    const int64_t mc = M - m0 < kStreamChunk ? M - m0 : kStreamChunk;
+    const cudaError_t e = launch_chunk(static_cast<const uint16_t *>(x) + m0 * K, mc, K, N, op0, op1, variant, act,
+                                       static_cast<uint16_t *>(out) + m0 * N,
+                                       residual ? static_cast<const uint16_t *>(residual) + m0 * N : nullptr,
+                                       stream, num_sms, early_weights);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // Read and clear the device error word of this translation unit's kernel.

@@ -51,12 +51,12 @@ KNAMES = {ops.SMALL_M_RING: "ring", ops.SMALL_M_STREAM: "stream"}
 
 def expect_small_m(before, kernel, M, counter=None):
     """The call(s) since `before` ran on the small-M path, on the selected
-    kernel (the warp-streamed one serves M <= 16 at these shapes)."""
+    kernel (the warp-streamed one serves M <= 32 at these shapes, in launches of up to 16 rows)."""
     after = ops.qsw_get_counters()
     if counter is not None:
         assert after[counter] > before[counter]
     reg = after[ops.CNT_GEMV_STREAM] > before[ops.CNT_GEMV_STREAM]
-    assert reg == (kernel == ops.SMALL_M_STREAM and M <= 16), (kernel, M)
+    assert reg == (kernel == ops.SMALL_M_STREAM and M <= 32), (kernel, M)
 
 
 def check(variant, got, want, dtype="bf16"):
@@ -186,6 +186,7 @@ MORE_SMALL_M_SHAPES = [
     (3, 2560, 10240, 4, 64, 8, 32),    # the mixed-spec workload's specs
     (16, 1024, 2000, 4, 64, 8, 32),    # two x row groups, mixed specs
     (13, 2048, 1203, 2, 64, 4, 64),    # two x row groups, odd M, 2-bit gate, ragged last unit
+    (27, 1024, 520, 4, 64, 8, 32),     # M > 16: launches over row chunks of 16 and 11
 ]
 
 
@@ -195,21 +196,23 @@ MORE_SMALL_M_SHAPES = [
 def test_small_m_kernel_more_shapes(dev, gemv_limit, small_m_kernel, kernel, shape, variant):
     M, H, I, bg, gg, bu, gu = shape
     case = inputs.make_case(M, H, I, bits_g=bg, gs_g=gg, bits_u=bu, gs_u=gu, seed=M * 13 + I)
-    gemv_limit(16)
+    gemv_limit(32)
     small_m_kernel(kernel)
     before = ops.qsw_get_counters()
     check_fused(case, dev, variant, rows=list(range(M)))
-    expect_small_m(before, kernel, M, ops.CNT_FUSED_GEMV)
+    if not (kernel == ops.SMALL_M_RING and M > 16):   # (where the slot-ring kernel may not fit)
+        expect_small_m(before, kernel, M, ops.CNT_FUSED_GEMV)
 
 
 @pytest.mark.parametrize("kernel", SMALL_M_KERNELS, ids=lambda k: KNAMES[k])
-@pytest.mark.parametrize("M,K,N", [(1, 2048, 1000), (3, 1024, 203), (8, 512, 40), (2, 8192, 2048), (12, 2048, 520)])
+@pytest.mark.parametrize("M,K,N", [(1, 2048, 1000), (3, 1024, 203), (8, 512, 40), (2, 8192, 2048), (12, 2048, 520),
+                                   (19, 1024, 300)])
 @pytest.mark.parametrize("with_residual", [False, True], ids=["plain", "residual"])
 def test_small_m_single_operand(dev, gemv_limit, small_m_kernel, kernel, M, K, N, with_residual):
     """affine_qmm on the small-M kernels (ragged units), with and without a
     residual."""
     case = inputs.make_case(M, K, N, bits_g=4, gs_g=64, seed=M + K + N)
-    gemv_limit(16)
+    gemv_limit(32)
     small_m_kernel(kernel)
     x, w, s, b, gs, bits = device_args(case, dev)[:6]
     h = inputs.make_x(M, N, seed=K) if with_residual else None
@@ -217,8 +220,9 @@ def test_small_m_single_operand(dev, gemv_limit, small_m_kernel, kernel, M, K, N
     y = ops.affine_qmm(x, w, s, b, gs, bits, residual=None if h is None else inputs.bits_to_device(h, dev))
     got = to_bits(y)
     ops.qsw_check_device_errors()
-    assert ops.qsw_get_counters()[ops.CNT_QMM_GEMV] == before[ops.CNT_QMM_GEMV] + 1
-    expect_small_m(before, kernel, M)
+    if not (kernel == ops.SMALL_M_RING and M > 16):   # (where the slot-ring kernel may not fit)
+        assert ops.qsw_get_counters()[ops.CNT_QMM_GEMV] == before[ops.CNT_QMM_GEMV] + 1
+        expect_small_m(before, kernel, M)
     want = oracle.qmm(case.x, case.gate.packed, case.gate.scales, case.gate.biases, gs, bits, residual=h)
     ok, info = check_projection(got, want)
     assert ok, info
