@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, NG == 1 ? 2 : 1) gemv_stream_kernel(
   constexpr uint32_t kStep0 = kBlockK * BITS0 / 32, kStep1 = kBlockK * BB / 32;   // words per block of a row
   const uint32_t wpr0 = K * BITS0 / 32, wpr1 = K * BB / 32;                       // words per packed row
   const bool k_full = (K % kBlockK) == 0;
+  // every lane of every item of this CTA in range (no ragged unit or block):
+  // the per-lane guards below are skipped (warp-uniform)
+  const bool all_in = k_full && 8 * (u_begin + ucount) <= p.N;
   int ld_left = i_end - i_begin;
   int ld_kb = i_begin - u_first * nkb;
   int ld_row0 = 8 * (u_begin + u_first);   // first A row of the unit being requested
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, NG == 1 ? 2 : 1) gemv_stream_kernel(
   auto issue_next = [&]() {
     if (ld_left > 0) {   // warp-uniform
       // lanes past N or K copy nothing: their scale and bias read as 0 below, so w = 0
-      if ((ld_row0 + 8 <= p.N && (k_full || ld_kb != nkb - 1)) || (ld_row0 + g < p.N && ld_k < K)) {
+      if (all_in || (ld_row0 + g < p.N && ld_k < K)) {
         debug_check(ld_k + kChunk <= K && ld_row0 + g < p.N, err);
         copy_chunk<BITS0>(ring + ld_stage + lane0, pa);
         if constexpr (DUAL) copy_chunk<BITS1>(ring + ld_stage + lane1, pb);
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, NG == 1 ? 2 : 1) gemv_stream_kernel(
   uint32_t sa = 0u, ba = 0u, sb = 0u, bb = 0u;
   auto load_scales = [&]() {
     sa = ba = sb = bb = 0u;
-    if (c_row < p.N && ck < K) {
+    if (all_in || (c_row < p.N && ck < K)) {
       const uint32_t gi0 = __umulhi(ck >> 4, p.gm0);
       debug_check(gi0 < p.ng0, err);
       sa = ldg_u16(p.s0 + so0 + gi0);
