@@ -60,7 +60,7 @@ for kernel in (ops.SMALL_M_RING, ops.SMALL_M_STREAM):
     for M, H, I, bg_, gg, bu_, gu in [(1, 512, 8, 4, 64, 4, 64), (3, 512, 203, 4, 64, 4, 64),
                                       (8, 512, 64, 2, 64, 4, 32), (17, 1024, 100, 4, 64, 4, 64),
                                       (6, 2048, 20000, 4, 64, 4, 64), (2, 2080, 64, 4, 32, 8, 32),
-                                      (12, 1024, 100, 4, 64, 8, 32)]:
+                                      (12, 1024, 100, 4, 64, 8, 32), (20, 512, 64, 4, 64, 4, 64)]:
         fused(inputs.make_case(M, H, I, bits_g=bg_, gs_g=gg, bits_u=bu_, gs_u=gu, seed=M * 3 + H), "small_m")
     fused(inputs.make_case(5, 512, 136, seed=9, dtype="f16"), "small_m")
 ops.qsw_set_gemv_max_m(0)

@@ -295,8 +295,10 @@ def test_small_m_projection_rate(dev, gemv_limit, small_m_kernel, kernel, M):
 
 
 @pytest.mark.parametrize("limit,M,kernel", [(0, 24, ops.SMALL_M_AUTO), (32, 24, ops.SMALL_M_RING),
-                                            (32, 6, ops.SMALL_M_RING), (32, 6, ops.SMALL_M_STREAM)],
-                         ids=["tensor_core", "small_m_ring_M24", "small_m_ring_M6", "small_m_stream_M6"])
+                                            (32, 6, ops.SMALL_M_RING), (32, 6, ops.SMALL_M_STREAM),
+                                            (32, 12, ops.SMALL_M_STREAM), (32, 24, ops.SMALL_M_STREAM)],
+                         ids=["tensor_core", "small_m_ring_M24", "small_m_ring_M6", "small_m_stream_M6",
+                              "small_m_stream_M12", "small_m_stream_M24_chunks"])
 def test_fused_match_equals_unfused(dev, gemv_limit, small_m_kernel, limit, M, kernel):
     """MATCH is the unfused composition op for op, and both kernels compute it
     bit for bit: each kernel folds every K block into the f32 accumulator the
