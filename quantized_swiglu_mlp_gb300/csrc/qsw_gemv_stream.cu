@@ -144,8 +144,10 @@ __device__ __forceinline__ void read_chunk(uint32_t (&w)[BITS], uint32_t src) {
 // XF: all 8 fragment rows of each x row group are staged (p.x_rows == 8 * NG),
 // so the staging layout is a compile-time constant.  NG: x row groups of 8
 // (M <= 8: 1; M <= 16: 2, which share every dequantised A fragment).
-template <int BITS0, int BITS1, bool DUAL, bool XF, int NG, class A>
-__global__ void __launch_bounds__(kThreads, NG == 1 ? 2 : 1) gemv_stream_kernel(const StreamParams p) {
+// MB: CTAs meant to share an SM (2 caps the registers at 64 a thread; used
+// where the shared memory of two CTAs fits).
+template <int BITS0, int BITS1, bool DUAL, bool XF, int NG, int MB, class A>
+__global__ void __launch_bounds__(kThreads, MB) gemv_stream_kernel(const StreamParams p) {
   constexpr int BB = DUAL ? BITS1 : BITS0;
   constexpr int SB = stage_bytes<BITS0, BITS1, DUAL>();
   extern __shared__ __align__(128) uint8_t smem[];
@@ -488,13 +490,13 @@ int stage_of(int bits0, int bits1, bool dual) {
   return chunk(bits0) + (dual ? chunk(bits1) : 0);
 }
 
-template <int BITS0, int BITS1, bool DUAL, bool XF, int NG, class A>
+template <int BITS0, int BITS1, bool DUAL, bool XF, int NG, int MB, class A>
 cudaError_t launch_x(const StreamParams &p, const StreamLayout &l, int grid, cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!(attr_done.load() & (uint64_t(1) << dev))) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<BITS0, BITS1, DUAL, XF, NG, A>,
+    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<BITS0, BITS1, DUAL, XF, NG, MB, A>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(uint64_t(1) << dev);
@@ -509,7 +511,7 @@ cudaError_t launch_x(const StreamParams &p, const StreamLayout &l, int grid, cud
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = p.early ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BITS0, BITS1, DUAL, XF, NG, A>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_stream_kernel<BITS0, BITS1, DUAL, XF, NG, MB, A>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -525,9 +527,13 @@ cudaError_t launch_cfg(StreamParams p, const StreamLayout &l, cudaStream_t strea
   p.red_off = l.red_off;
   p.ring_off = l.ring_off;
   p.tab_off = l.tab_off;
-  if (p.x_rows == 16) return launch_x<BITS0, BITS1, DUAL, true, 2, A>(p, l, grid, stream);
-  return p.x_rows == 8 ? launch_x<BITS0, BITS1, DUAL, true, 1, A>(p, l, grid, stream)
-                       : launch_x<BITS0, BITS1, DUAL, false, 1, A>(p, l, grid, stream);
+  if (p.x_rows == 16) return launch_x<BITS0, BITS1, DUAL, true, 2, 1, A>(p, l, grid, stream);
+  if (p.x_rows != 8) return launch_x<BITS0, BITS1, DUAL, false, 1, 2, A>(p, l, grid, stream);
+  // two CTAs per SM where their shared memory fits (228 KB per SM, 1 KB reserved
+  // per CTA), else one with twice the registers (measured: mixed specs, M <= 8,
+  // 4 % faster)
+  return 2 * (l.total + 1024) <= 228 * 1024 ? launch_x<BITS0, BITS1, DUAL, true, 1, 2, A>(p, l, grid, stream)
+                                            : launch_x<BITS0, BITS1, DUAL, true, 1, 1, A>(p, l, grid, stream);
 }
 
 template <int BITS0, class A>
