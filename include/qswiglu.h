@@ -287,11 +287,12 @@ typedef enum {
 QSW_API void qsw_set_small_m_kernel(int kernel);
 QSW_API int qsw_get_small_m_kernel(void);
 
-/* Early weight stream (default off).  When on, the small-M kernel is launched
- * as a programmatic dependent of the work before it on the stream: it may start
- * while the previous kernel is still running and streams the packed weights,
- * scales and biases of its first units into shared memory at once; it reads x
- * and writes hidden only after all earlier work on the stream has completed
+/* Early weight stream (default off).  When on, the small-M kernels are
+ * launched as programmatic dependents of the work before them on the stream:
+ * a call may start while the previous kernel is still running and requests
+ * the packed weights (and, on the slot-ring kernel, the scales and biases) of
+ * its first units or K blocks into shared memory at once; it reads x and
+ * writes its output only after all earlier work on the stream has completed
  * (griddepcontrol.wait).  Turn it on only when no earlier work on the stream
  * writes the weight, scale or bias arrays of the call -- the usual decode loop,
  * where weights are constant.  Process-wide. */
